@@ -1,0 +1,220 @@
+"""CPU oracle of the MoE AllToAllvDynamic data plane (dispatch + top-k combine).
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference arm may import this package.  The product
+path (``combine_device_resident_gb300``) never imports it and shares no code
+with it: the arithmetic lives in ``a2av_oracle.c`` (plain C, one thread, built
+with ``-O2 -ffp-contract=off`` so every fp32 product and sum is rounded on its
+own), and this module only marshals numpy arrays into it.
+
+What each function computes, and the passages and readings it follows, is
+written in ``a2av_oracle.c``.  Pinning status (what checks each function against
+something other than itself, in ``tests/test_oracle_pins.py``):
+
+* ``splits``     -- invariants (sum_e send = T*k, recv = transpose of per-rank
+                    send counts summed over each rank's experts, exclusive-scan
+                    offsets, window bases) and exhaustive brute force on tiny
+                    routings;
+* ``slot_map`` / ``dispatch`` -- brute force (window d = a stable sort of all
+                    assignments sent to d by key (source, expert, token, slot)),
+                    bijection onto [0, R*T*k), recv[slot] == x bit for bit;
+* ``combine``    -- closed forms independent of the layout (unit weights and
+                    identity experts give bf16(k*x), k in {1, 2, 4, 8}; gate sum
+                    times x), numpy float32 with separate roundings, and the fp64
+                    sum within 1 bf16 ulp;
+* ``expert_scale`` -- closed form bf16(x * (1 + e/E)) computed by torch.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "a2av_oracle.c")
+_LIB = os.path.join(_HERE, "liba2av_oracle.so")
+
+BAD_EXPERT = 1
+WINDOW_OVERFLOW = 2
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``liba2av_oracle.so`` next to its source."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+                               "-fPIC", "-shared", "-Wall", "-Wextra", "-o", tmp, _SRC])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def bind(L):
+    """Declare the C signatures on a loaded oracle library and return it."""
+    i32p = np.ctypeslib.ndpointer(np.int32, flags="C_CONTIGUOUS")
+    u16p = np.ctypeslib.ndpointer(np.uint16, flags="C_CONTIGUOUS")
+    f32p = np.ctypeslib.ndpointer(np.float32, flags="C_CONTIGUOUS")
+    f64p = np.ctypeslib.ndpointer(np.float64, flags="C_CONTIGUOUS")
+    i64p = np.ctypeslib.ndpointer(np.int64, flags="C_CONTIGUOUS")
+    ci, ci64 = ctypes.c_int, ctypes.c_int64
+    L.oracle_splits.restype = ctypes.c_uint32
+    L.oracle_splits.argtypes = [ci, ci, ci, ci, ci, ci64, i32p] + [i32p] * 7
+    L.oracle_slot_map.restype = ctypes.c_uint32
+    L.oracle_slot_map.argtypes = [ci, ci, ci, ci, ci, ci64, i32p, i32p, i32p, i32p, i32p]
+    L.oracle_dispatch.restype = ctypes.c_uint32
+    L.oracle_dispatch.argtypes = [ci, ci, ci, ci, ci, ci, ci64, u16p, i32p, i32p, i32p, i32p, i32p,
+                                  u16p, i32p]
+    L.oracle_expert_scale.restype = None
+    L.oracle_expert_scale.argtypes = [ci, ci, ci64, u16p, i32p, i32p, u16p]
+    L.oracle_combine.restype = None
+    L.oracle_combine.argtypes = [ci, ci, u16p, f32p, i32p, i64p, ci64, u16p]
+    L.oracle_combine_f64.restype = None
+    L.oracle_combine_f64.argtypes = [ci, ci, u16p, f32p, i32p, i64p, ci64, f64p]
+    L.oracle_bf16_to_f32.restype = ctypes.c_float
+    L.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    L.oracle_f32_to_bf16.restype = ctypes.c_uint16
+    L.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+    return L
+
+
+def compile_source(src: str, out: str) -> str:
+    """Compile C source text into a shared library at ``out`` with the oracle's flags."""
+    cfile = out + ".c"
+    with open(cfile, "w") as f:
+        f.write(src)
+    subprocess.check_call(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+                           "-fPIC", "-shared", "-w", "-o", out, cfile])
+    return out
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def _mode(window_mode) -> int:
+    if window_mode in (0, "packed"):
+        return 0
+    if window_mode in (1, "fixed"):
+        return 1
+    raise ValueError(window_mode)
+
+
+def splits(R: int, E: int, idx: np.ndarray, window_mode="packed", window_rows: int = 0) -> dict:
+    """Counts and offsets of one dispatch.  idx int32 [R][T][k]."""
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    _, T, k = idx.shape
+    if E % R:
+        raise ValueError("E must be a multiple of R")
+    epr = E // R
+    out = {
+        "send_counts": np.zeros((R, E), np.int32),
+        "send_offsets": np.zeros((R, E), np.int32),
+        "recv_counts": np.zeros((R, R), np.int32),
+        "recv_offsets": np.zeros((R, R), np.int32),
+        "recv_expert_counts": np.zeros((R, R, epr), np.int32),
+        "recv_total": np.zeros((R,), np.int32),
+        "window_base": np.zeros((R,), np.int32),
+    }
+    st = lib().oracle_splits(R, E, T, k, _mode(window_mode), int(window_rows), idx,
+                             out["send_counts"], out["send_offsets"], out["recv_counts"],
+                             out["recv_offsets"], out["recv_expert_counts"], out["recv_total"],
+                             out["window_base"])
+    out["status"] = int(st)
+    return out
+
+
+def slot_map(R: int, E: int, idx: np.ndarray, sp: dict, window_mode="packed", window_rows: int = 0):
+    """(slot_map int32 [R][T][k], status) without moving any payload."""
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    _, T, k = idx.shape
+    sm = np.empty((R, T, k), np.int32)
+    st = lib().oracle_slot_map(R, E, T, k, _mode(window_mode), int(window_rows), idx,
+                               sp["send_offsets"], sp["recv_offsets"], sp["window_base"], sm)
+    return sm, int(st)
+
+
+def arena_rows(R: int, T: int, k: int, window_mode="packed", window_rows: int = 0) -> int:
+    return R * T * k if _mode(window_mode) == 0 else R * int(window_rows)
+
+
+def dispatch(R: int, E: int, x: np.ndarray, idx: np.ndarray, sp: dict, window_mode="packed",
+             window_rows: int = 0, recv: Optional[np.ndarray] = None):
+    """(recv uint16 [rows][H], slot_map, status).  x uint16 bf16 bits [R][T][H].
+    Rows no assignment reaches keep their prior contents (zeros if recv is None)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    _, T, H = x.shape
+    k = idx.shape[2]
+    rows = arena_rows(R, T, k, window_mode, window_rows)
+    if recv is None:
+        recv = np.zeros((rows, H), np.uint16)
+    sm = np.empty((R, T, k), np.int32)
+    st = lib().oracle_dispatch(R, E, T, H, k, _mode(window_mode), int(window_rows), x, idx,
+                               sp["send_counts"], sp["send_offsets"], sp["recv_offsets"],
+                               sp["window_base"], recv, sm)
+    return recv, sm, int(st)
+
+
+def expert_scale(E: int, recv: np.ndarray, idx: np.ndarray, sm: np.ndarray, y: Optional[np.ndarray] = None):
+    """y[row] = bf16(recv[row] * (1 + e/E)) for every dispatched assignment."""
+    recv = np.ascontiguousarray(recv, dtype=np.uint16)
+    if y is None:
+        y = recv.copy()
+    H = recv.shape[1]
+    lib().oracle_expert_scale(E, H, int(idx.size), recv, np.ascontiguousarray(idx, np.int32),
+                              np.ascontiguousarray(sm, np.int32), y)
+    return y
+
+
+def combine(y: np.ndarray, gate: np.ndarray, sm: np.ndarray, tokens: Optional[np.ndarray] = None):
+    """out uint16 [n_tokens][H] for flat token ids ``tokens`` (default: all)."""
+    y = np.ascontiguousarray(y, dtype=np.uint16)
+    gate = np.ascontiguousarray(gate, dtype=np.float32)
+    sm = np.ascontiguousarray(sm, dtype=np.int32)
+    k = sm.shape[-1]
+    ntok_all = sm.size // k
+    if tokens is None:
+        tokens = np.arange(ntok_all, dtype=np.int64)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int64)
+    H = y.shape[1]
+    out = np.empty((len(tokens), H), np.uint16)
+    lib().oracle_combine(H, k, y, gate, sm, tokens, len(tokens), out)
+    return out
+
+
+def combine_f64(y: np.ndarray, gate: np.ndarray, sm: np.ndarray, tokens: Optional[np.ndarray] = None):
+    y = np.ascontiguousarray(y, dtype=np.uint16)
+    gate = np.ascontiguousarray(gate, dtype=np.float32)
+    sm = np.ascontiguousarray(sm, dtype=np.int32)
+    k = sm.shape[-1]
+    if tokens is None:
+        tokens = np.arange(sm.size // k, dtype=np.int64)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int64)
+    out = np.empty((len(tokens), y.shape[1]), np.float64)
+    lib().oracle_combine_f64(y.shape[1], k, y, gate, sm, tokens, len(tokens), out)
+    return out
+
+
+def bf16_to_f32(bits: int) -> float:
+    return float(lib().oracle_bf16_to_f32(int(bits)))
+
+
+def f32_to_bf16(v: float) -> int:
+    return int(lib().oracle_f32_to_bf16(float(v)))
+
+
+def run_all(R, E, x, idx, gate, window_mode="packed", window_rows=0, expert="identity"):
+    """The whole path on the CPU: splits, dispatch, expert stand-in, combine."""
+    sp = splits(R, E, idx, window_mode, window_rows)
+    recv, sm, st = dispatch(R, E, x, idx, sp, window_mode, window_rows)
+    y = expert_scale(E, recv, idx, sm) if expert == "scale" else recv
+    out = combine(y, gate, sm).reshape(x.shape)
+    return {"splits": sp, "recv": recv, "slot_map": sm, "y": y, "out": out,
+            "status": sp["status"] | st}

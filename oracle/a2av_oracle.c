@@ -1,0 +1,360 @@
+/*
+ * a2av_oracle.c -- plain, slow, single-threaded CPU oracle of the MoE
+ * AllToAllvDynamic data plane (dispatch, then top-k weighted combine).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path calls this file:
+ * only the tests, the smoke check and the benchmark's CPU baseline / reference
+ * arm load it.  It shares no code, header, table or constant with the CUDA
+ * library; both sides only consume the same seeded inputs.
+ *
+ * Source: NCCLX, "Collective Communication for 100k+ GPUs" (Meta), as
+ * described on the pages
+ *   [P1] abhik.ai/papers/ncclx, section "Inference: small messages, unknown
+ *        sizes" (Figure 13 pipeline; Section 6.1 AllToAllvDynamic);
+ *   [P2] hungchun0201 research digest, section 3.3 "AllToAllvDynamic";
+ *   [P3] qiguanping.github.io deep dive, section 7 (Figure 13 "token shuffle
+ *        (dispatch) and combine"; Figures 16-17 GPU-resident metadata).
+ * What the pages fix:
+ *   - a router chooses the experts of each token; the tokens are sorted by
+ *     expert into a send buffer; an AllToAllv sends each one to the rank
+ *     that holds its expert [P1, Inference, Figure 13];
+ *   - the split counts are computed on the GPU and read from GPU memory when
+ *     the collective runs; only real tokens are sent, no padding to the
+ *     worst case [P1 Inference; P2 3.3];
+ *   - the collective returns the counts it received [P1 Inference];
+ *   - the tokens come back and are combined [P3 section 7, Figure 13].
+ * Readings where the pages are silent (each is stated again where used):
+ *   R1  expert e lives on rank e / (E/R)   (contiguous blocks of E/R experts);
+ *   R2  "sorted by expert" is a stable sort: expert ascending, then token t,
+ *       then slot j;
+ *   R3  the AllToAllv convention: window d holds the segments of sources
+ *       0..R-1 back to back, in source order, with no gaps;
+ *   R4  windows: "packed" mode places window d right after window d-1 in one
+ *       arena; "fixed" mode gives window d the rows [d*W, (d+1)*W);
+ *   R5  combine: out = bf16_rne( sum_j w_j * y[slot(t,j)] ), accumulated in
+ *       fp32 from 0.0f in slot order j = 0..k-1, each product and each sum
+ *       rounded on its own (this file must be built with -ffp-contract=off);
+ *   R6  error handling: an expert id outside [0, E) is dropped (not counted,
+ *       slot -1, status bit 0); in fixed mode a row whose window-relative
+ *       position is >= W is dropped (slot -1, status bit 1) while the counts
+ *       still report the routed totals; combine skips slot -1.
+ *
+ * Layouts (all row-major, C order):
+ *   x          uint16 bf16 bits  [R][T][H]
+ *   idx        int32             [R][T][k]
+ *   gate       float32           [R][T][k]
+ *   send_counts, send_offsets    int32 [R][E]
+ *   recv_counts, recv_offsets    int32 [R][R]      (destination-major: [d][s])
+ *   recv_expert_counts           int32 [R][R][E/R] ([d][s][local expert])
+ *   recv_total, window_base      int32 [R]
+ *   recv, y    uint16 bf16 bits  [rows][H]
+ *   slot_map   int32             [R][T][k]
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_BAD_EXPERT 1u
+#define ORACLE_WINDOW_OVERFLOW 2u
+
+/* ---- bf16 <-> fp32 (bf16 = top 16 bits of an IEEE binary32) ---------------- */
+
+float oracle_bf16_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round to nearest, ties to even, on the 16 discarded bits; NaN stays NaN. */
+uint16_t oracle_f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t keep_lsb = (u >> 16) & 1u;
+    u += 0x7fffu + keep_lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* ---- step 1: the split counts (what the router's counts are) ---------------
+ * send_counts[s][e] = number of (t, j) on rank s with idx = e.
+ * send_offsets[s][e] = sum over e' < e of send_counts[s][e']: the start of
+ * expert e's block in rank s's expert-sorted send buffer (R2).
+ * recv_counts[d][s] = sum of send_counts[s][e] over the experts e of rank d
+ * (R1): the counts rank d receives, i.e. the transpose of the per-rank send
+ * counts summed over d's experts [P1 Inference: "returns the counts it
+ * received"].  recv_offsets[d][s] = sum over s' < s of recv_counts[d][s'] (R3).
+ * recv_expert_counts[d][s][le] = send_counts[s][d*(E/R) + le].
+ * recv_total[d] = sum over s of recv_counts[d][s].
+ * window_base[d] = sum over d' < d of recv_total[d'] (packed) or d*W (fixed).
+ * Returns the status bits.
+ */
+uint32_t oracle_splits(int R, int E, int T, int k, int window_mode, int64_t window_rows,
+                       const int32_t *idx,
+                       int32_t *send_counts, int32_t *send_offsets,
+                       int32_t *recv_counts, int32_t *recv_offsets,
+                       int32_t *recv_expert_counts, int32_t *recv_total,
+                       int32_t *window_base)
+{
+    uint32_t status = 0;
+    int epr = E / R;
+    for (int s = 0; s < R; ++s) {
+        int32_t *cnt = send_counts + (size_t)s * E;
+        for (int e = 0; e < E; ++e)
+            cnt[e] = 0;
+        for (int t = 0; t < T; ++t)
+            for (int j = 0; j < k; ++j) {
+                int32_t e = idx[((size_t)s * T + t) * k + j];
+                if (e < 0 || e >= E) {
+                    status |= ORACLE_BAD_EXPERT;
+                    continue;
+                }
+                cnt[e] += 1;
+            }
+        int32_t run = 0;
+        for (int e = 0; e < E; ++e) {
+            send_offsets[(size_t)s * E + e] = run;
+            run += cnt[e];
+        }
+    }
+    for (int d = 0; d < R; ++d) {
+        int32_t run = 0;
+        for (int s = 0; s < R; ++s) {
+            int32_t c = 0;
+            for (int le = 0; le < epr; ++le) {
+                int32_t v = send_counts[(size_t)s * E + d * epr + le];
+                recv_expert_counts[((size_t)d * R + s) * epr + le] = v;
+                c += v;
+            }
+            recv_counts[(size_t)d * R + s] = c;
+            recv_offsets[(size_t)d * R + s] = run;
+            run += c;
+        }
+        recv_total[d] = run;
+        if (window_mode == 1 && (int64_t)run > window_rows)
+            status |= ORACLE_WINDOW_OVERFLOW;
+    }
+    int64_t base = 0;
+    for (int d = 0; d < R; ++d) {
+        if (window_mode == 1)
+            window_base[d] = (int32_t)((int64_t)d * window_rows);
+        else
+            window_base[d] = (int32_t)base;
+        base += recv_total[d];
+    }
+    return status;
+}
+
+/* ---- step 2: the expert sort of one rank's send buffer ---------------------
+ * send_pos[t][j] = position of assignment (t, j) of rank s in its
+ * expert-sorted send buffer: send_offsets[s][e] + the number of earlier
+ * assignments (t', j') < (t, j) of rank s with the same expert (R2, a stable
+ * counting sort by expert key) [P1 Inference: "the tokens are sorted by
+ * expert into a send buffer"].  Dropped ids get -1.
+ */
+static void send_positions(int E, int T, int k, const int32_t *idx_s, const int32_t *send_offsets_s,
+                           int32_t *running, int32_t *send_pos)
+{
+    for (int e = 0; e < E; ++e)
+        running[e] = 0;
+    for (int t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            int32_t e = idx_s[(size_t)t * k + j];
+            if (e < 0 || e >= E) {
+                send_pos[(size_t)t * k + j] = -1;
+                continue;
+            }
+            send_pos[(size_t)t * k + j] = send_offsets_s[e] + running[e];
+            running[e] += 1;
+        }
+}
+
+/* ---- step 3: where each assignment lands -------------------------------------
+ * The AllToAllv copies the segment of rank s's send buffer that holds rank d's
+ * experts, [send_offsets[s][d*E/R], + recv_counts[d][s]), to window d at
+ * recv_offsets[d][s] (R3, R4).  So an assignment at send position p with
+ * expert e (on rank d = e / (E/R)) lands at
+ *   window-relative row  rel = recv_offsets[d][s] + (p - send_offsets[s][d*E/R])
+ *   arena row            window_base[d] + rel,
+ * dropped in fixed mode when rel >= W (R6).  slot_map records that row.
+ * Returns the status bits.
+ */
+uint32_t oracle_slot_map(int R, int E, int T, int k, int window_mode, int64_t window_rows,
+                         const int32_t *idx, const int32_t *send_offsets,
+                         const int32_t *recv_offsets, const int32_t *window_base,
+                         int32_t *slot_map)
+{
+    uint32_t status = 0;
+    int epr = E / R;
+    int32_t *running = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+    int32_t *pos = (int32_t *)malloc(sizeof(int32_t) * (size_t)T * k + 4);
+    for (int s = 0; s < R; ++s) {
+        const int32_t *idx_s = idx + (size_t)s * T * k;
+        const int32_t *so = send_offsets + (size_t)s * E;
+        send_positions(E, T, k, idx_s, so, running, pos);
+        for (size_t a = 0; a < (size_t)T * k; ++a) {
+            int32_t e = idx_s[a];
+            int32_t *slot = slot_map + (size_t)s * T * k + a;
+            if (pos[a] < 0) {
+                *slot = -1;
+                status |= ORACLE_BAD_EXPERT;
+                continue;
+            }
+            int d = e / epr;
+            int64_t rel = (int64_t)recv_offsets[(size_t)d * R + s] + (pos[a] - so[d * epr]);
+            if (window_mode == 1 && rel >= window_rows) {
+                *slot = -1;
+                status |= ORACLE_WINDOW_OVERFLOW;
+                continue;
+            }
+            *slot = (int32_t)(window_base[d] + rel);
+        }
+    }
+    free(pos);
+    free(running);
+    return status;
+}
+
+/* ---- steps 2+3 with the payload: the dispatch ----------------------------------
+ * Literally: per source rank s, build the expert-sorted send buffer (copy row
+ * x[s][t] to send position p for each of its assignments), then perform the
+ * AllToAllv: copy each destination's segment of the send buffer into that
+ * destination's window, rows in order.  Rows whose slot is -1 are not
+ * written (R6).  Also fills slot_map (as oracle_slot_map).  Returns status.
+ */
+uint32_t oracle_dispatch(int R, int E, int T, int H, int k, int window_mode, int64_t window_rows,
+                         const uint16_t *x, const int32_t *idx,
+                         const int32_t *send_counts, const int32_t *send_offsets,
+                         const int32_t *recv_offsets, const int32_t *window_base,
+                         uint16_t *recv, int32_t *slot_map)
+{
+    uint32_t status = 0;
+    int epr = E / R;
+    size_t row_bytes = sizeof(uint16_t) * (size_t)H;
+    int32_t *running = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+    int32_t *pos = (int32_t *)malloc(sizeof(int32_t) * (size_t)T * k + 4);
+    uint16_t *sendbuf = (uint16_t *)malloc(row_bytes * (size_t)T * k + 16);
+    for (int s = 0; s < R; ++s) {
+        const int32_t *idx_s = idx + (size_t)s * T * k;
+        const int32_t *so = send_offsets + (size_t)s * E;
+        const int32_t *sc = send_counts + (size_t)s * E;
+        send_positions(E, T, k, idx_s, so, running, pos);
+        /* the sort: rows into the send buffer in expert order */
+        for (int t = 0; t < T; ++t)
+            for (int j = 0; j < k; ++j) {
+                int32_t p = pos[(size_t)t * k + j];
+                if (p < 0) {
+                    status |= ORACLE_BAD_EXPERT;
+                    continue;
+                }
+                memcpy(sendbuf + (size_t)p * H, x + ((size_t)s * T + t) * H, row_bytes);
+            }
+        /* the AllToAllv: one contiguous segment per destination */
+        for (int d = 0; d < R; ++d) {
+            int32_t seg_start = so[d * epr];
+            int32_t seg_len = 0;
+            for (int le = 0; le < epr; ++le)
+                seg_len += sc[d * epr + le];
+            int64_t rel0 = recv_offsets[(size_t)d * R + s];
+            for (int32_t i = 0; i < seg_len; ++i) {
+                int64_t rel = rel0 + i;
+                if (window_mode == 1 && rel >= window_rows) {
+                    status |= ORACLE_WINDOW_OVERFLOW;
+                    break;
+                }
+                memcpy(recv + ((size_t)window_base[d] + (size_t)rel) * H,
+                       sendbuf + ((size_t)seg_start + i) * H, row_bytes);
+            }
+        }
+        /* where each assignment went */
+        for (size_t a = 0; a < (size_t)T * k; ++a) {
+            int32_t *slot = slot_map + (size_t)s * T * k + a;
+            if (pos[a] < 0) {
+                *slot = -1;
+                continue;
+            }
+            int d = idx_s[a] / epr;
+            int64_t rel = (int64_t)recv_offsets[(size_t)d * R + s] + (pos[a] - so[d * epr]);
+            *slot = (window_mode == 1 && rel >= window_rows) ? -1 : (int32_t)(window_base[d] + rel);
+        }
+    }
+    free(sendbuf);
+    free(pos);
+    free(running);
+    return status;
+}
+
+/* ---- the expert stand-in used by the scaled workload -------------------------
+ * y[row] = bf16_rne( float(recv[row]) * (1 + e/E) ), e = the assignment's global
+ * expert id, for every assignment with slot >= 0.  (1 + e/E is computed in
+ * fp32: e/E then 1 + that.)  Rows that no assignment owns are left as they
+ * are.
+ */
+void oracle_expert_scale(int E, int H, int64_t n_assign, const uint16_t *recv, const int32_t *idx,
+                         const int32_t *slot_map, uint16_t *y)
+{
+    for (int64_t a = 0; a < n_assign; ++a) {
+        int32_t row = slot_map[a];
+        if (row < 0)
+            continue;
+        float q = (float)idx[a] / (float)E;
+        float scale = 1.0f + q;
+        const uint16_t *src = recv + (size_t)row * H;
+        uint16_t *dst = y + (size_t)row * H;
+        for (int h = 0; h < H; ++h) {
+            float v = oracle_bf16_to_f32(src[h]) * scale;
+            dst[h] = oracle_f32_to_bf16(v);
+        }
+    }
+}
+
+/* ---- step 4: the combine ---------------------------------------------------------
+ * For each requested token u (a flat index s*T + t):
+ *   acc = 0.0f; for j = 0..k-1 with slot >= 0:  acc = acc + (w_j * y[slot][h])
+ *   out[u][h] = bf16_rne(acc)                            (R5, R6)
+ * [P3 section 7, Figure 13: dispatch, experts, combine.]
+ */
+void oracle_combine(int H, int k, const uint16_t *y, const float *gate, const int32_t *slot_map,
+                    const int64_t *tokens, int64_t n_tokens, uint16_t *out)
+{
+    for (int64_t i = 0; i < n_tokens; ++i) {
+        int64_t u = tokens[i];
+        const int32_t *slots = slot_map + (size_t)u * k;
+        const float *w = gate + (size_t)u * k;
+        uint16_t *o = out + (size_t)i * H;
+        for (int h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                if (slots[j] < 0)
+                    continue;
+                float prod = w[j] * oracle_bf16_to_f32(y[(size_t)slots[j] * H + h]);
+                acc = acc + prod;
+            }
+            o[h] = oracle_f32_to_bf16(acc);
+        }
+    }
+}
+
+/* The same sum in fp64 (exact products of bf16 x fp32 values, one rounding per
+ * add in fp64), returned unrounded so tests can bound the fp32 oracle. */
+void oracle_combine_f64(int H, int k, const uint16_t *y, const float *gate, const int32_t *slot_map,
+                        const int64_t *tokens, int64_t n_tokens, double *out)
+{
+    for (int64_t i = 0; i < n_tokens; ++i) {
+        int64_t u = tokens[i];
+        const int32_t *slots = slot_map + (size_t)u * k;
+        const float *w = gate + (size_t)u * k;
+        for (int h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int j = 0; j < k; ++j) {
+                if (slots[j] < 0)
+                    continue;
+                acc += (double)w[j] * (double)oracle_bf16_to_f32(y[(size_t)slots[j] * H + h]);
+            }
+            out[(size_t)i * H + h] = acc;
+        }
+    }
+}

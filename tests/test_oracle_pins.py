@@ -1,0 +1,387 @@
+"""Pins for the CPU oracle: it is checked against things other than itself.
+
+* a hand-worked tiny example (derivation in the comments);
+* an exhaustive brute force written as a *different* formulation: window d is
+  a sort of every assignment routed to rank d by key (source, expert, token,
+  slot), and every count/offset is read off those sorted lists;
+* the invariants the method fixes: split counts sum to T*k, received counts
+  are the transpose of the per-rank send counts (summed over the destination's
+  experts), no padding (slot_map is a bijection onto the packed arena), and
+  dispatch followed by combine with identity experts and unit weights gives
+  k*x [NCCLX pages: P1 "Inference", P2 section 3.3];
+* closed forms of the combine computed without any dispatch (torch / numpy
+  float32 / fp64), and bf16 rounding against torch's own conversion;
+* mutation checks: plausible mistakes planted in a *copy* of the oracle's C
+  source must each make at least one of these pins fail.
+"""
+import itertools
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.bf16util import bits_to_f32, f32_to_bits_torch, ulp_diff
+
+SPLIT_KEYS = ["send_counts", "send_offsets", "recv_counts", "recv_offsets",
+              "recv_expert_counts", "recv_total", "window_base"]
+
+
+# ----------------------------------------------------------------------------
+# brute force: an independent formulation from sorted per-destination lists
+# ----------------------------------------------------------------------------
+def brute_force(R, E, idx, window_mode="packed", window_rows=0):
+    idx = np.asarray(idx)
+    _, T, k = idx.shape
+    epr = E // R
+    items = [(s, int(idx[s, t, j]), t, j) for s in range(R) for t in range(T) for j in range(k)]
+    valid = [it for it in items if 0 <= it[1] < E]
+    status = 0 if len(valid) == len(items) else oracle.BAD_EXPERT
+    windows = [sorted(it for it in valid if it[1] // epr == d) for d in range(R)]
+    per_src = [sorted((e, t, j) for (s2, e, t, j) in valid if s2 == s) for s in range(R)]
+    out = {
+        "send_counts": np.array([[sum(1 for it in per_src[s] if it[0] == e) for e in range(E)] for s in range(R)]),
+        "send_offsets": np.array([[next((i for i, it in enumerate(per_src[s]) if it[0] >= e), len(per_src[s]))
+                                   for e in range(E)] for s in range(R)]),
+        "recv_counts": np.array([[sum(1 for it in windows[d] if it[0] == s) for s in range(R)] for d in range(R)]),
+        "recv_offsets": np.array([[next((i for i, it in enumerate(windows[d]) if it[0] >= s), len(windows[d]))
+                                   for s in range(R)] for d in range(R)]),
+        "recv_expert_counts": np.array([[[sum(1 for it in windows[d] if it[0] == s and it[1] == d * epr + le)
+                                          for le in range(epr)] for s in range(R)] for d in range(R)]),
+        "recv_total": np.array([len(w) for w in windows]),
+    }
+    if window_mode == "fixed":
+        out["window_base"] = np.array([d * window_rows for d in range(R)])
+        if any(len(w) > window_rows for w in windows):
+            status |= oracle.WINDOW_OVERFLOW
+    else:
+        out["window_base"] = np.array([sum(len(w) for w in windows[:d]) for d in range(R)])
+    slot = -np.ones((R, T, k), dtype=np.int64)
+    for d, w in enumerate(windows):
+        for pos, (s, e, t, j) in enumerate(w):
+            if window_mode == "fixed" and pos >= window_rows:
+                continue
+            slot[s, t, j] = out["window_base"][d] + pos
+    out["slot_map"] = slot
+    out["status"] = status
+    return out
+
+
+def check_against_brute(R, E, idx, window_mode="packed", window_rows=0):
+    bf = brute_force(R, E, idx, window_mode, window_rows)
+    sp = oracle.splits(R, E, idx, window_mode, window_rows)
+    for key in SPLIT_KEYS:
+        np.testing.assert_array_equal(sp[key], bf[key].reshape(sp[key].shape), err_msg=key)
+    sm, st = oracle.slot_map(R, E, idx, sp, window_mode, window_rows)
+    np.testing.assert_array_equal(sm, bf["slot_map"], err_msg="slot_map")
+    assert (sp["status"] | st) == bf["status"]
+    return sp, sm
+
+
+# ----------------------------------------------------------------------------
+def test_hand_worked_example():
+    # R=2 ranks, E=4 experts: experts {0,1} on rank 0, {2,3} on rank 1; T=3, k=1.
+    # rank 0 routes tokens to experts [3, 0, 3]; rank 1 to [1, 2, 1].
+    # send_counts: rank0 e0:1 e3:2 -> [1,0,0,2]; rank1 e1:2 e2:1 -> [0,2,1,0]
+    # send_offsets (exclusive over e): [0,1,1,1] and [0,0,2,3]
+    # recv_counts[d][s]: d0 gets e0+e1: s0 1, s1 2; d1 gets e2+e3: s0 2, s1 1
+    # recv_offsets (exclusive over s): d0 [0,1], d1 [0,2]; totals [3,3];
+    # packed window bases [0,3].
+    # Window 0 in (source, expert, token) order: (s0,e0,t1) (s1,e1,t0) (s1,e1,t2) -> rows 0,1,2
+    # Window 1: (s0,e3,t0) (s0,e3,t2) (s1,e2,t1) -> rows 3,4,5
+    idx = np.array([[[3], [0], [3]], [[1], [2], [1]]], np.int32)
+    sp = oracle.splits(2, 4, idx)
+    assert sp["send_counts"].tolist() == [[1, 0, 0, 2], [0, 2, 1, 0]]
+    assert sp["send_offsets"].tolist() == [[0, 1, 1, 1], [0, 0, 2, 3]]
+    assert sp["recv_counts"].tolist() == [[1, 2], [2, 1]]
+    assert sp["recv_offsets"].tolist() == [[0, 1], [0, 2]]
+    assert sp["recv_expert_counts"].tolist() == [[[1, 0], [0, 2]], [[0, 2], [1, 0]]]
+    assert sp["recv_total"].tolist() == [3, 3]
+    assert sp["window_base"].tolist() == [0, 3]
+    sm, st = oracle.slot_map(2, 4, idx, sp)
+    assert st == 0
+    assert sm[..., 0].tolist() == [[3, 0, 4], [1, 5, 2]]
+    # payload: rows carry the token they came from
+    x = np.arange(2 * 3 * 2, dtype=np.uint16).reshape(2, 3, 2) + 0x3F00
+    recv, sm2, st2 = oracle.dispatch(2, 4, x, idx, sp)
+    np.testing.assert_array_equal(sm2, sm)
+    assert recv.tolist() == [x[0, 1].tolist(), x[1, 0].tolist(), x[1, 2].tolist(),
+                             x[0, 0].tolist(), x[0, 2].tolist(), x[1, 1].tolist()]
+
+
+@pytest.mark.parametrize("T", [1, 2, 3])
+def test_exhaustive_top1_r2_e4(T):
+    R, E, k = 2, 4, 1
+    for combo in itertools.product(range(E), repeat=R * T * k):
+        idx = np.array(combo, np.int32).reshape(R, T, k)
+        check_against_brute(R, E, idx)
+
+
+def test_exhaustive_top2_distinct_r2_e4():
+    R, E, k, T = 2, 4, 2, 1
+    pairs = [p for p in itertools.product(range(E), repeat=2) if p[0] != p[1]]
+    for combo in itertools.product(pairs, repeat=R * T):
+        idx = np.array(combo, np.int32).reshape(R, T, k)
+        check_against_brute(R, E, idx)
+
+
+def test_exhaustive_top2_with_duplicates_r2_e4():
+    # duplicates inside one token are allowed and ordered by slot j
+    R, E, k, T = 2, 4, 2, 1
+    for combo in itertools.product(range(E), repeat=R * T * k):
+        idx = np.array(combo, np.int32).reshape(R, T, k)
+        check_against_brute(R, E, idx)
+
+
+@pytest.mark.parametrize("R,E,T,k", [(1, 3, 5, 2), (2, 2, 4, 1), (3, 6, 7, 2), (4, 8, 9, 3), (4, 16, 33, 4)])
+def test_random_against_brute(R, E, T, k):
+    rng = np.random.default_rng(R * 1000 + E * 10 + k)
+    for _ in range(20):
+        idx = rng.integers(0, E, size=(R, T, k), dtype=np.int32)
+        check_against_brute(R, E, idx)
+
+
+def test_fixed_windows_and_overflow_against_brute():
+    rng = np.random.default_rng(7)
+    R, E, T, k = 3, 6, 6, 2
+    for W in (R * T * k, 8, 5, 1, 0):
+        for _ in range(10):
+            idx = rng.integers(0, E, size=(R, T, k), dtype=np.int32)
+            check_against_brute(R, E, idx, "fixed", W)
+    # all tokens to one expert with a window of T*k rows must overflow
+    idx = np.zeros((R, T, k), np.int32)
+    sp = oracle.splits(R, E, idx, "fixed", T * k)
+    assert sp["status"] & oracle.WINDOW_OVERFLOW
+    sm, st = oracle.slot_map(R, E, idx, sp, "fixed", T * k)
+    assert st & oracle.WINDOW_OVERFLOW
+    assert (sm[0] >= 0).all() and (sm[1:] == -1).all()
+
+
+def test_bad_expert_ids_are_dropped():
+    R, E, T, k = 2, 4, 4, 2
+    rng = np.random.default_rng(3)
+    idx = rng.integers(0, E, size=(R, T, k), dtype=np.int32)
+    idx[0, 1, 0] = -1
+    idx[1, 3, 1] = E
+    sp, sm = check_against_brute(R, E, idx)
+    assert sp["status"] & oracle.BAD_EXPERT
+    assert sm[0, 1, 0] == -1 and sm[1, 3, 1] == -1
+    assert sp["send_counts"].sum() == R * T * k - 2
+
+
+# ----------------------------------------------------------------------------
+# invariants on the synthetic workloads (full routing, no payload)
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
+def test_invariants_on_workloads(wid):
+    import workloads as W
+
+    w = W.WORKLOADS[wid]
+    idx = W.make_routing_gate(w)["topk_idx"]
+    sp = oracle.splits(w.R, w.E, idx, w.window_mode, w.window_rows)
+    assert sp["status"] == 0
+    T, k, R, E = w.T, w.k, w.R, w.E
+    epr = E // R
+    # split counts sum to T*k on every rank
+    assert (sp["send_counts"].sum(axis=1) == T * k).all()
+    # per-rank counts equal a direct bincount of that rank's routing
+    for s in range(R):
+        np.testing.assert_array_equal(sp["send_counts"][s], np.bincount(idx[s].ravel(), minlength=E))
+    # received counts: transpose of send counts summed over each rank's experts
+    np.testing.assert_array_equal(sp["recv_counts"], sp["send_counts"].reshape(R, R, epr).sum(-1).T)
+    assert sp["recv_total"].sum() == R * T * k
+    sm, st = oracle.slot_map(R, E, idx, sp, w.window_mode, w.window_rows)
+    assert st == 0
+    if w.window_mode == "packed":
+        # no padding: a bijection onto [0, R*T*k)
+        assert np.array_equal(np.sort(sm.ravel()), np.arange(R * T * k))
+    else:
+        rel = sm - sp["window_base"][idx // epr]
+        assert (rel >= 0).all() and (rel < w.window_rows).all()
+        for d in range(R):
+            rows = np.sort(rel[(idx // epr) == d])
+            assert np.array_equal(rows, np.arange(sp["recv_total"][d]))
+
+
+def test_workload_routing_laws():
+    import workloads as W
+
+    # top-k experts are distinct where the workload asks for it
+    for wid in (4, 5):
+        w = W.WORKLOADS[wid]
+        idx = W.make_routing_gate(w)["topk_idx"].reshape(-1, w.k)
+        srt = np.sort(idx, axis=1)
+        assert (np.diff(srt, axis=1) > 0).all()
+    # the hot expert of workload 5 holds close to the 1/k cap of assignments,
+    # and four ranks receive nothing
+    w = W.WORKLOADS[5]
+    idx = W.make_routing_gate(w)["topk_idx"]
+    share0 = (idx == 0).mean()
+    assert 0.11 < share0 <= 1.0 / w.k
+    per_rank = np.bincount(idx.ravel() // (w.E // w.R), minlength=w.R)
+    assert (per_rank == 0).sum() == 4 and per_rank[0] > 0
+    # workload 3 leaves some experts empty
+    w = W.WORKLOADS[3]
+    idx = W.make_routing_gate(w)["topk_idx"]
+    assert (np.bincount(idx.ravel(), minlength=w.E) == 0).any()
+
+
+# ----------------------------------------------------------------------------
+# dispatch payload and the combine closed forms
+# ----------------------------------------------------------------------------
+def _small(wid, T, H, seed=0):
+    import workloads as W
+
+    w = W.WORKLOADS[wid].scaled(T=T, H=H)
+    x = W.bf16_bits(W.make_x(w, seed))
+    rg = W.make_routing_gate(w, seed)
+    return w, x, rg["topk_idx"], rg["gate_w"]
+
+
+@pytest.mark.parametrize("wid,T,H", [(1, 128, 256), (2, 40, 72), (3, 64, 40), (4, 50, 24), (5, 12, 16)])
+def test_dispatch_places_every_row(wid, T, H):
+    w, x, idx, gate = _small(wid, T, H)
+    res = oracle.run_all(w.R, w.E, x, idx, gate, w.window_mode, w.window_rows, w.expert)
+    sm, recv = res["slot_map"], res["recv"]
+    assert res["status"] == 0
+    R, k = w.R, w.k
+    for s in range(R):
+        for t in range(T):
+            for j in range(k):
+                assert np.array_equal(recv[sm[s, t, j]], x[s, t])
+    if w.window_mode == "packed":
+        assert np.array_equal(np.sort(sm.ravel()), np.arange(R * T * k))
+
+
+@pytest.mark.parametrize("k", [1, 2, 4, 8])
+def test_identity_unit_weights_give_k_times_x(k):
+    # dispatch then combine with identity experts and unit weights returns k*x,
+    # which is exact in bf16 for a power of two k.
+    import torch
+    import workloads as W
+
+    w = W.Workload("t", R=4, E=16, T=37, H=48, k=k, routing="zipf_distinct", zipf_s=1.0)
+    x = W.bf16_bits(W.make_x(w, 1))
+    idx = W.make_routing_gate(w, 1)["topk_idx"]
+    gate = np.ones_like(idx, dtype=np.float32)
+    res = oracle.run_all(w.R, w.E, x, idx, gate)
+    xt = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).float()
+    want = (xt * k).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(res["out"], want)
+
+
+def test_identity_softmax_weights_close_to_gate_sum_times_x():
+    import workloads as W
+
+    w, x, idx, gate = _small(5, 20, 64)
+    res = oracle.run_all(w.R, w.E, x, idx, gate)
+    exact = bits_to_f32(x).astype(np.float64) * gate.astype(np.float64).sum(-1, keepdims=True)
+    d = ulp_diff(res["out"], f32_to_bits_torch(exact.astype(np.float32)))
+    assert d.max() <= 1
+
+
+def test_scaled_experts_closed_form_numpy_f32():
+    # out = bf16( sum_j w_j * bf16(x * (1 + e_j/E)) ), accumulated in fp32 in j order
+    # from 0, products and sums rounded separately -- computed straight from
+    # (x, idx, w) with numpy float32 and no dispatch at all.
+    w, x, idx, gate = _small(4, 64, 40)
+    res = oracle.run_all(w.R, w.E, x, idx, gate, expert="scale")
+    xf = bits_to_f32(x)
+    acc = np.zeros(xf.shape, np.float32)
+    for j in range(w.k):
+        scale = (np.float32(1.0) + idx[..., j].astype(np.float32) / np.float32(w.E)).astype(np.float32)
+        yj = bits_to_f32(f32_to_bits_torch(xf * scale[..., None]))
+        acc = (acc + (gate[..., j][..., None] * yj).astype(np.float32)).astype(np.float32)
+    np.testing.assert_array_equal(res["out"], f32_to_bits_torch(acc))
+
+
+def test_expert_scale_closed_form_torch():
+    import torch
+
+    w, x, idx, gate = _small(4, 33, 24)
+    sp = oracle.splits(w.R, w.E, idx)
+    recv, sm, _ = oracle.dispatch(w.R, w.E, x, idx, sp)
+    y = oracle.expert_scale(w.E, recv, idx, sm)
+    xt = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).float()
+    for s in range(w.R):
+        for t in range(0, w.T, 5):
+            for j in range(w.k):
+                e = int(idx[s, t, j])
+                want = (xt[s, t] * (1.0 + e / w.E)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+                np.testing.assert_array_equal(y[sm[s, t, j]], want)
+
+
+def test_combine_fp32_within_one_ulp_of_fp64():
+    import workloads as W
+
+    for wid, T, H in [(4, 64, 64), (5, 16, 64)]:
+        w, x, idx, gate = _small(wid, T, H)
+        res = oracle.run_all(w.R, w.E, x, idx, gate, expert=w.expert)
+        f64 = oracle.combine_f64(res["y"], gate, res["slot_map"])
+        want = f32_to_bits_torch(f64.astype(np.float32))  # fp64 -> fp32 is within fp32's half ulp
+        assert ulp_diff(res["out"].reshape(-1, H), want).max() <= 1
+
+
+def test_bf16_rounding_matches_torch():
+    rng = np.random.default_rng(11)
+    vals = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32),
+        (rng.standard_normal(2000) * 1e30).astype(np.float32),
+        (rng.standard_normal(2000) * 1e-38).astype(np.float32),
+        # exact ties: bf16 value + half an ulp, both parities
+        ((np.arange(1, 500, dtype=np.uint32) << 16) | 0x8000).view(np.float32),
+        np.array([0.0, -0.0, 3.3895314e38, -3.3895314e38, np.inf, -np.inf], np.float32),
+    ])
+    want = f32_to_bits_torch(vals)
+    got = np.array([oracle.f32_to_bf16(v) for v in vals], np.uint16)
+    np.testing.assert_array_equal(got, want)
+    bits = rng.integers(0, 1 << 16, 5000).astype(np.uint16)
+    bits = bits[(bits & 0x7F80) != 0x7F80]
+    back = np.array([oracle.bf16_to_f32(b) for b in bits], np.float32)
+    np.testing.assert_array_equal(back, bits_to_f32(bits))
+
+
+# ----------------------------------------------------------------------------
+# mutation checks: plant a mistake in a copy of the oracle, the pins must fail
+# ----------------------------------------------------------------------------
+MUTANTS = {
+    "transposed recv_offsets": ("(int64_t)recv_offsets[(size_t)d * R + s] + (pos[a] - so[d * epr]);\n            if (window_mode == 1 && rel >= window_rows) {\n                *slot = -1;\n                status",
+                                "(int64_t)recv_offsets[(size_t)s * R + d] + (pos[a] - so[d * epr]);\n            if (window_mode == 1 && rel >= window_rows) {\n                *slot = -1;\n                status"),
+    "inclusive send_offsets": ("            send_offsets[(size_t)s * E + e] = run;\n            run += cnt[e];",
+                               "            run += cnt[e];\n            send_offsets[(size_t)s * E + e] = run;"),
+    "unstable sort": ("    for (int t = 0; t < T; ++t)\n        for (int j = 0; j < k; ++j) {\n            int32_t e = idx_s[(size_t)t * k + j];\n            if (e < 0 || e >= E) {\n                send_pos",
+                      "    for (int t = T - 1; t >= 0; --t)\n        for (int j = 0; j < k; ++j) {\n            int32_t e = idx_s[(size_t)t * k + j];\n            if (e < 0 || e >= E) {\n                send_pos"),
+    "dropped gate weight": ("float prod = w[j] * oracle_bf16_to_f32(", "float prod = 1.0f * oracle_bf16_to_f32("),
+    "truncating bf16 rounding": ("u += 0x7fffu + keep_lsb;", "u += 0u * keep_lsb;"),
+    "window base off by one window": ("            window_base[d] = (int32_t)base;\n        base += recv_total[d];",
+                                      "        base += recv_total[d];\n            window_base[d] = (int32_t)base;"),
+    "wrong expert-to-rank map": ("            int d = e / epr;\n            int64_t rel", "            int d = e % R;\n            int64_t rel"),
+    "expert scale sign": ("float scale = 1.0f + q;", "float scale = 1.0f - q;"),
+}
+
+
+def _pin_suite():
+    """The pins above, run against whatever library ``oracle._lib`` holds."""
+    test_hand_worked_example()
+    test_exhaustive_top1_r2_e4(2)
+    test_exhaustive_top2_distinct_r2_e4()
+    test_random_against_brute(4, 8, 9, 3)
+    test_identity_unit_weights_give_k_times_x(2)
+    test_identity_softmax_weights_close_to_gate_sum_times_x()
+    test_scaled_experts_closed_form_numpy_f32()
+    test_expert_scale_closed_form_torch()
+    test_bf16_rounding_matches_torch()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path, monkeypatch):
+    import ctypes
+
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "a2av_oracle.c")).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site for {name!r} not found exactly once"
+    path = oracle.compile_source(src.replace(old, new), str(tmp_path / "mutant.so"))
+    monkeypatch.setattr(oracle, "_lib", oracle.bind(ctypes.CDLL(path)))
+    with pytest.raises(AssertionError):
+        _pin_suite()
