@@ -1,0 +1,471 @@
+#!/usr/bin/env python3
+"""Benchmark of the device-resident MoE dispatch + combine data plane.
+
+One step = one pass of the whole path on one batch: splits (histogram + scan),
+pack + exchange into the destination windows, and the top-k combine, replayed
+from one CUDA graph, with the inputs already resident in HBM.  The L2 is
+flushed (a 512 MiB write) between timed steps, outside the step's events.
+
+Prints ONE JSON line (rank 0).  ``value`` is dispatch+combine algorithmic
+bytes / step time in GB/s, summed over all GPUs; tokens/s and microseconds per
+call ride along.  ``--impl reference`` times the CPU oracle instead (rank 0
+only), on a bounded sample of the same workload.
+
+Multi-GPU (torchrun): each rank runs an independent replica of the workload
+on its own GPU (the R ranks of the method are emulated inside one GPU), so
+scaling is weak and there is no data-path collective; a barrier brackets the
+timed region and the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "dispatch+combine HBM GB/s (% of GB300 peak), tokens/s and µs per call at 1 GPU"
+DEFAULT_WORKLOAD = 2
+FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--flags", type=int, default=0, help="a2av_config_t.flags (1 = LSU pack)")
+    ap.add_argument("--pack-ctas-per-sm", type=int, default=0)
+    ap.add_argument("--pack-stage-bytes", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--reference-seconds", type=float, default=90.0, help="reference arm: total budget")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "combine_device_resident_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "a2av.h"), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        d = json.load(open(p))
+    except Exception:
+        return None
+    if d.get("source_sha") != csrc_hash():
+        return None
+    ent = d.get("kernels", {}).get(kernel, {})
+    if ent.get("workload") != workload:
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling in the background (timestamps kept)."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, enabled=True):
+        self.proc = None
+        self.path = None
+        if not enabled:
+            return
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None or not self.path:
+            return None
+        import datetime
+
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            rows.append((ts, parts))
+        os.unlink(self.path)
+        inside = [p for ts, p in rows if t0 - 0.06 <= ts <= t1 + 0.06] or [p for _, p in rows]
+        if not inside:
+            return None
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(p[2]) for p in inside if num(p[2]) is not None]
+        mx = [num(p[3]) for p in inside if num(p[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for p in inside for n, v in zip(names, p[6:10]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+def cpu_baseline(w: W.Workload, x_host_bits, idx, gate, budget_s: float):
+    """Time the CPU oracle (as it stands, one thread) on a bounded sample."""
+    import oracle
+
+    def run(wl, xb, ix, gt):
+        t = time.perf_counter()
+        oracle.run_all(wl.R, wl.E, xb, ix, gt, wl.window_mode, wl.window_rows, wl.expert)
+        return time.perf_counter() - t
+
+    # probe with a small slice of tokens, then size the sample to the budget
+    probe_T = max(1, min(w.T, 64))
+    wp = w.scaled(T=probe_T)
+    tp = run(wp, x_host_bits[:, :probe_T], idx[:, :probe_T], gate[:, :probe_T])
+    per_token = tp / probe_T
+    T_s = int(min(w.T, max(probe_T, budget_s / 2 / max(per_token, 1e-9))))
+    ws = w.scaled(T=T_s)
+    xs, ixs, gs = x_host_bits[:, :T_s], idx[:, :T_s], gate[:, :T_s]
+    reps, spent = 0, 0.0
+    while spent < budget_s / 2 or reps == 0:
+        spent += run(ws, xs, ixs, gs)
+        reps += 1
+    value = ws.algorithmic_bytes() * reps / spent / 1e9
+    sample = (f"oracle (splits, dispatch, combine) on the first {T_s} of {w.T} tokens per rank "
+              f"of every rank, {reps} rep(s), {spent:.1f} s")
+    return {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
+            "tokens_per_s": round(ws.R * ws.T * reps / spent, 1)}
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args, w: W.Workload):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import torch
+
+    import oracle
+
+    rg = W.make_routing_gate(w, 0)
+    idx, gate = rg["topk_idx"], rg["gate_w"]
+    steps, warm = args.steps, args.warmup
+    per_step = args.reference_seconds / max(1, steps + warm)
+    # token sample per step, sized from a probe
+    probe_T = max(1, min(w.T, 16))
+    xs = W.bf16_bits(W.make_x(w.scaled(T=probe_T), 0))
+    wp = w.scaled(T=probe_T)
+    t = time.perf_counter()
+    oracle.run_all(wp.R, wp.E, xs, idx[:, :probe_T], gate[:, :probe_T], wp.window_mode, wp.window_rows, wp.expert)
+    per_token = (time.perf_counter() - t) / probe_T
+    T_s = int(max(1, min(w.T, per_step / max(per_token, 1e-9))))
+    ws = w.scaled(T=T_s)
+    x_s = W.bf16_bits(W.make_x(ws, 0))
+    ix, gt = np.ascontiguousarray(idx[:, :T_s]), np.ascontiguousarray(gate[:, :T_s])
+    for _ in range(warm):
+        oracle.run_all(ws.R, ws.E, x_s, ix, gt, ws.window_mode, ws.window_rows, ws.expert)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.run_all(ws.R, ws.E, x_s, ix, gt, ws.window_mode, ws.window_rows, ws.expert)
+    dt = (time.perf_counter() - t0) / steps
+    value = ws.algorithmic_bytes() / dt / 1e9
+    sample = f"CPU oracle, one thread, first {T_s} of {w.T} tokens per rank of every rank per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": steps, "warmup": warm, "ms_per_step": round(dt * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_block(w, "none (host memory)"),
+        "tokens_per_s": round(ws.R * ws.T / dt, 2), "us_per_call": round(dt * 1e6, 2),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    del torch
+    return 0
+
+
+def config_block(w: W.Workload, l2: str):
+    return {"workload": w.name, "R": w.R, "E": w.E, "T": w.T, "H": w.H, "k": w.k, "routing": w.routing,
+            "gate": w.gate, "window": w.window_mode, "l2": l2, "accumulate": "fp32", "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------------------
+def main():
+    args = parse()
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import numpy as np
+    import torch
+
+    import combine_device_resident_gb300 as A
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    # ---- inputs (seeded, synthetic) ----------------------------------------------
+    rg = W.make_routing_gate(w, 0)
+    idx_h, gate_h = rg["topk_idx"], rg["gate_w"]
+    x = W.make_x(w, 0, device=dev)
+    idx = torch.from_numpy(idx_h).to(dev)
+    gate = torch.from_numpy(gate_h).to(dev)
+    plan = A.Plan(w.R, w.E, w.T, w.H, w.k, w.window_mode, w.window_rows, device=dev, flags=args.flags,
+                  pack_ctas_per_sm=args.pack_ctas_per_sm, pack_stage_bytes=args.pack_stage_bytes)
+    recv, slot_map, out = plan.new_buffers()
+    sp = plan.new_splits()
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def path(s):
+        plan.splits(idx, sp, slot_map, stream=s)
+        plan.pack(x, idx, sp, recv, slot_map, stream=s)
+        plan.combine(recv, gate, slot_map, out, stream=s)
+
+    # warm-up outside capture, then capture the path once
+    with torch.cuda.stream(stream):
+        path(stream)
+    torch.cuda.synchronize(dev)
+    if plan.read_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    # graph with event nodes between the kernels (per-kernel durations)
+    ev_ok = True
+    try:
+        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+    except TypeError:
+        ev_ok = False
+    graph = torch.cuda.CUDAGraph()
+    launches0 = plan.launches
+    with torch.cuda.graph(graph, stream=stream):
+        s = torch.cuda.current_stream(dev)
+        if ev_ok:
+            evs[0].record(s)
+        plan.splits(idx, sp, slot_map, stream=s)
+        if ev_ok:
+            evs[1].record(s)
+        plan.pack(x, idx, sp, recv, slot_map, stream=s)
+        if ev_ok:
+            evs[2].record(s)
+        plan.combine(recv, gate, slot_map, out, stream=s)
+        if ev_ok:
+            evs[3].record(s)
+    kernels_per_step = plan.launches - launches0
+
+    def flush_l2():
+        flush.zero_()
+
+    # ---- warm-up -----------------------------------------------------------------
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            flush_l2()
+            graph.replay()
+    torch.cuda.synchronize(dev)
+    if ev_ok:
+        try:
+            evs[0].elapsed_time(evs[3])
+        except Exception:
+            ev_ok = False
+
+    # ---- timed region ----------------------------------------------------------------
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    kt = {"splits": [], "pack": [], "combine": []}
+    sampler = ClockSampler(local, enabled=not args.no_clocks)
+    time.sleep(0.15 if sampler.proc else 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush_l2()
+            starts[i].record(stream)
+            graph.replay()
+            ends[i].record(stream)
+            if ev_ok:
+                # the graph's own event nodes are re-recorded each replay: read them now
+                ends[i].synchronize()
+                kt["splits"].append(evs[0].elapsed_time(evs[1]))
+                kt["pack"].append(evs[1].elapsed_time(evs[2]))
+                kt["combine"].append(evs[2].elapsed_time(evs[3]))
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    t_wall1 = time.time()
+    sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(step_ms) / K
+    if world > 1:
+        tt = torch.tensor([ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    status = plan.read_status()
+    if status != 0:
+        raise RuntimeError(f"device status word set during the timed region: {status:#x}")
+
+    if not ev_ok:
+        # fallback: time the three kernels as separate graphs, same stream
+        graphs = {}
+        for name, fn in (("splits", lambda s: plan.splits(idx, sp, slot_map, stream=s)),
+                         ("pack", lambda s: plan.pack(x, idx, sp, recv, slot_map, stream=s)),
+                         ("combine", lambda s: plan.combine(recv, gate, slot_map, out, stream=s))):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn(torch.cuda.current_stream(dev))
+            graphs[name] = g
+        with torch.cuda.stream(stream):
+            for _ in range(min(K, 200)):
+                for name in ("splits", "pack", "combine"):
+                    flush_l2() if name == "splits" else None
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    graphs[name].replay()
+                    b.record(stream)
+                    b.synchronize()
+                    kt[name].append(a.elapsed_time(b))
+
+    # ---- results -------------------------------------------------------------------
+    bytes_step = w.algorithmic_bytes()
+    gbs = bytes_step / (ms * 1e-3) / 1e9 * world
+    peak, peak_kind = read_peaks()
+    A_ = w.R * w.T * w.k
+    # algorithmic bytes per launch: pack reads x once and writes k copies (+ idx
+    # read, slot_map write); combine reads k rows and writes out (+ slot_map and
+    # gate reads).  pack + combine = Workload.algorithmic_bytes().
+    kbytes = {
+        "splits": 8 * A_,
+        "pack": w.R * w.T * w.H * 2 * (1 + w.k) + 8 * A_,
+        "combine": w.R * w.T * w.H * 2 * (1 + w.k) + 8 * A_,
+    }
+    kus = {n: 1e3 * sum(v) / len(v) for n, v in kt.items() if v}
+    dom = max(("pack", "combine"), key=lambda n: kus.get(n, 0.0))
+    ach = kbytes[dom] / (kus[dom] * 1e-6) / 1e9
+    traffic = ncu_traffic(dom, w.name)
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
+                "kernel_us": {n: round(v, 3) for n, v in kus.items()},
+                "kernel_gbs": {n: round(kbytes[n] / (kus[n] * 1e-6) / 1e9, 1) for n in kus},
+                "timing": "event nodes inside the graph" if ev_ok else "separate per-kernel graphs"}
+
+    # ---- end to end through host buffers ----------------------------------------
+    x_pin = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    x_pin.copy_(x)
+    idx_pin = torch.from_numpy(idx_h).pin_memory()
+    gate_pin = torch.from_numpy(gate_h).pin_memory()
+    out_pin = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = x_pin.numel() * 2 + idx_pin.numel() * 4 + gate_pin.numel() * 4
+    d2h = out_pin.numel() * 2
+    e2e_ms = []
+    with torch.cuda.stream(stream):
+        for i in range(args.e2e_steps + 3):
+            flush_l2()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            x.copy_(x_pin, non_blocking=True)
+            idx.copy_(idx_pin, non_blocking=True)
+            gate.copy_(gate_pin, non_blocking=True)
+            graph.replay()
+            out_pin.copy_(out, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            if i >= 3:
+                e2e_ms.append(a.elapsed_time(b))
+    e2e_t = sum(e2e_ms) / len(e2e_ms)
+    if world > 1:
+        tt = torch.tensor([e2e_t], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_t = float(tt.item())
+    e2e = {"value": round(bytes_step / (e2e_t * 1e-3) / 1e9 * world, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_t, 4),
+           "path": "pinned host x/idx/gate -> HBM, graph replay, out -> pinned host"}
+
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, W.bf16_bits(x), idx_h, gate_h, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_block(w, f"flushed between steps ({FLUSH_BYTES >> 20} MiB write)"),
+            "pct_of_peak": round(100 * gbs / world / peak, 2), "peak_gbs": peak,
+            "tokens_per_s": round(w.R * w.T * world / (ms * 1e-3), 1), "us_per_call": round(ms * 1e3, 3),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": int(kernels_per_step * K), "kernels_per_step": int(kernels_per_step),
+            "clocks": clocks, "variant": {"flags": args.flags, "pack_ctas_per_sm": args.pack_ctas_per_sm,
+                                          "pack_stage_bytes": args.pack_stage_bytes},
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    plan.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,282 @@
+"""ctypes binding of ``liba2av.so`` (declared in ``include/a2av.h``).
+
+Argument marshalling only: torch tensors are checked (device, dtype, shape,
+contiguity) and their device pointers, together with the current CUDA stream,
+are handed to the C ABI.  Every step of the data path runs in the library's
+CUDA kernels; there is no CPU fallback, and loading fails loudly when the
+library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import build as _build
+
+A2AV_OK = 0
+A2AV_ERR_INVALID_ARG = 1
+A2AV_ERR_CUDA = 2
+A2AV_ERR_NO_MEMORY = 3
+
+DEV_BAD_EXPERT = 1 << 0
+DEV_WINDOW_OVERFLOW = 1 << 1
+DEV_WAIT_TIMEOUT = 1 << 31
+
+WINDOW_PACKED = 0
+WINDOW_FIXED = 1
+FLAG_PACK_LSU = 1 << 0
+
+# Every function the header declares, for load checks.
+EXPORTED = [
+    "a2av_config_check", "a2av_recv_arena_rows", "a2av_plan_create", "a2av_plan_destroy",
+    "a2av_dispatch", "a2av_splits", "a2av_pack", "a2av_combine", "a2av_expert_scale",
+    "a2av_read_device_status", "a2av_device_status_ptr", "a2av_plan_launches",
+    "a2av_status_string", "a2av_last_error",
+]
+
+
+class Config(ctypes.Structure):
+    _fields_ = [
+        ("num_ranks", ctypes.c_int32),
+        ("num_experts", ctypes.c_int32),
+        ("tokens_per_rank", ctypes.c_int32),
+        ("hidden", ctypes.c_int32),
+        ("topk", ctypes.c_int32),
+        ("window_mode", ctypes.c_int32),
+        ("window_rows", ctypes.c_int64),
+        ("device", ctypes.c_int32),
+        ("flags", ctypes.c_uint32),
+        ("pack_ctas_per_sm", ctypes.c_int32),
+        ("pack_stage_bytes", ctypes.c_int32),
+    ]
+
+
+class SplitsPtrs(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_void_p) for name in (
+        "send_counts", "send_offsets", "recv_counts", "recv_offsets", "recv_expert_counts",
+        "recv_total", "window_base")]
+
+
+class A2avError(RuntimeError):
+    pass
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(path: Optional[str] = None):
+    """Load liba2av.so (declaring the C signatures).  Raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build.LIB
+    if not os.path.exists(p):
+        raise A2avError(f"{p} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    L = ctypes.CDLL(p)
+    vp, i32 = ctypes.c_void_p, ctypes.c_int32
+    cfgp = ctypes.POINTER(Config)
+    spp = ctypes.POINTER(SplitsPtrs)
+    L.a2av_config_check.argtypes = [cfgp]
+    L.a2av_config_check.restype = i32
+    L.a2av_recv_arena_rows.argtypes = [cfgp]
+    L.a2av_recv_arena_rows.restype = ctypes.c_int64
+    L.a2av_plan_create.argtypes = [cfgp, ctypes.POINTER(vp)]
+    L.a2av_plan_create.restype = i32
+    L.a2av_plan_destroy.argtypes = [vp]
+    L.a2av_plan_destroy.restype = i32
+    L.a2av_dispatch.argtypes = [vp, vp, vp, spp, vp, vp, vp]
+    L.a2av_dispatch.restype = i32
+    L.a2av_splits.argtypes = [vp, vp, spp, vp, vp]
+    L.a2av_splits.restype = i32
+    L.a2av_pack.argtypes = [vp, vp, vp, spp, vp, vp, vp]
+    L.a2av_pack.restype = i32
+    L.a2av_combine.argtypes = [vp, vp, vp, vp, vp, vp]
+    L.a2av_combine.restype = i32
+    L.a2av_expert_scale.argtypes = [vp, vp, vp, vp, vp, vp]
+    L.a2av_expert_scale.restype = i32
+    L.a2av_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, vp]
+    L.a2av_read_device_status.restype = i32
+    L.a2av_device_status_ptr.argtypes = [vp]
+    L.a2av_device_status_ptr.restype = vp
+    L.a2av_plan_launches.argtypes = [vp]
+    L.a2av_plan_launches.restype = ctypes.c_int64
+    L.a2av_status_string.argtypes = [i32]
+    L.a2av_status_string.restype = ctypes.c_char_p
+    L.a2av_last_error.argtypes = []
+    L.a2av_last_error.restype = ctypes.c_char_p
+    if path is None:
+        _lib = L
+    return L
+
+
+def _check(L, rc: int, what: str):
+    if rc != A2AV_OK:
+        msg = L.a2av_status_string(rc).decode()
+        detail = L.a2av_last_error().decode()
+        raise A2avError(f"{what}: {msg}" + (f" ({detail})" if detail else ""))
+
+
+def make_config(R, E, T, H, k, window_mode="packed", window_rows=0, device=0, flags=0,
+                pack_ctas_per_sm=0, pack_stage_bytes=0) -> Config:
+    mode = {"packed": WINDOW_PACKED, "fixed": WINDOW_FIXED}.get(window_mode, window_mode)
+    return Config(int(R), int(E), int(T), int(H), int(k), int(mode), int(window_rows), int(device),
+                  int(flags), int(pack_ctas_per_sm), int(pack_stage_bytes))
+
+
+class Splits:
+    """Device-resident split counts/offsets of one dispatch (int32 tensors)."""
+
+    NAMES = ("send_counts", "send_offsets", "recv_counts", "recv_offsets", "recv_expert_counts",
+             "recv_total", "window_base")
+
+    def __init__(self, R: int, E: int, device):
+        import torch
+
+        epr = E // R
+        shapes = {"send_counts": (R, E), "send_offsets": (R, E), "recv_counts": (R, R),
+                  "recv_offsets": (R, R), "recv_expert_counts": (R, R, epr), "recv_total": (R,),
+                  "window_base": (R,)}
+        for n in self.NAMES:
+            setattr(self, n, torch.zeros(shapes[n], dtype=torch.int32, device=device))
+        self._ptrs = SplitsPtrs(*[getattr(self, n).data_ptr() for n in self.NAMES])
+
+    @property
+    def ptrs(self) -> SplitsPtrs:
+        return self._ptrs
+
+    def to_numpy(self) -> dict:
+        return {n: getattr(self, n).cpu().numpy() for n in self.NAMES}
+
+
+def _stream_ptr(stream, device):
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Plan:
+    """A configured data plane: R emulated ranks, E experts, T tokens per rank,
+    hidden H, top-k.  Owns only the library's small workspace."""
+
+    def __init__(self, R, E, T, H, k, window_mode="packed", window_rows=0, device=None, flags=0,
+                 pack_ctas_per_sm=0, pack_stage_bytes=0):
+        import torch
+
+        self.lib = load_library()
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        if dev.type != "cuda":
+            raise A2avError("a2av plans live on a CUDA device")
+        self.device = dev
+        self.R, self.E, self.T, self.H, self.k = int(R), int(E), int(T), int(H), int(k)
+        self.window_mode = window_mode
+        self.window_rows = int(window_rows)
+        self.cfg = make_config(R, E, T, H, k, window_mode, window_rows, dev.index, flags,
+                               pack_ctas_per_sm, pack_stage_bytes)
+        handle = ctypes.c_void_p()
+        _check(self.lib, self.lib.a2av_plan_create(ctypes.byref(self.cfg), ctypes.byref(handle)), "a2av_plan_create")
+        self.handle = handle
+        self.arena_rows = int(self.lib.a2av_recv_arena_rows(ctypes.byref(self.cfg)))
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            _check(self.lib, self.lib.a2av_plan_destroy(self.handle), "a2av_plan_destroy")
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ---- tensors ------------------------------------------------------------
+    def new_splits(self) -> Splits:
+        return Splits(self.R, self.E, self.device)
+
+    def new_buffers(self):
+        """(recv [arena_rows][H] bf16, slot_map [R][T][k] int32, out [R][T][H] bf16), uninitialised."""
+        import torch
+
+        recv = torch.empty((self.arena_rows, self.H), dtype=torch.bfloat16, device=self.device)
+        slot_map = torch.empty((self.R, self.T, self.k), dtype=torch.int32, device=self.device)
+        out = torch.empty((self.R, self.T, self.H), dtype=torch.bfloat16, device=self.device)
+        return recv, slot_map, out
+
+    def _t(self, t, dtype, shape, name):
+        import torch
+
+        if not isinstance(t, torch.Tensor):
+            raise A2avError(f"{name} must be a torch tensor")
+        if t.device != self.device:
+            raise A2avError(f"{name} is on {t.device}, the plan is on {self.device}")
+        if t.dtype != dtype:
+            raise A2avError(f"{name} must be {dtype}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise A2avError(f"{name} must be contiguous")
+        if shape is not None and tuple(t.shape) != tuple(shape):
+            raise A2avError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+        return ctypes.c_void_p(t.data_ptr())
+
+    def _rows(self, t, name):
+        import torch
+
+        return self._t(t, torch.bfloat16, (self.arena_rows, self.H), name)
+
+    # ---- calls ----------------------------------------------------------------
+    def dispatch(self, x, topk_idx, splits: Splits, recv, slot_map, stream=None):
+        import torch
+
+        args = (self.handle, self._t(x, torch.bfloat16, (self.R, self.T, self.H), "x"),
+                self._t(topk_idx, torch.int32, (self.R, self.T, self.k), "topk_idx"), ctypes.byref(splits.ptrs),
+                self._rows(recv, "recv"), self._t(slot_map, torch.int32, (self.R, self.T, self.k), "slot_map"),
+                _stream_ptr(stream, self.device))
+        _check(self.lib, self.lib.a2av_dispatch(*args), "a2av_dispatch")
+
+    def splits(self, topk_idx, splits: Splits, slot_map, stream=None):
+        import torch
+
+        _check(self.lib, self.lib.a2av_splits(
+            self.handle, self._t(topk_idx, torch.int32, (self.R, self.T, self.k), "topk_idx"),
+            ctypes.byref(splits.ptrs), self._t(slot_map, torch.int32, (self.R, self.T, self.k), "slot_map"),
+            _stream_ptr(stream, self.device)), "a2av_splits")
+
+    def pack(self, x, topk_idx, splits: Splits, recv, slot_map, stream=None):
+        import torch
+
+        _check(self.lib, self.lib.a2av_pack(
+            self.handle, self._t(x, torch.bfloat16, (self.R, self.T, self.H), "x"),
+            self._t(topk_idx, torch.int32, (self.R, self.T, self.k), "topk_idx"), ctypes.byref(splits.ptrs),
+            self._rows(recv, "recv"), self._t(slot_map, torch.int32, (self.R, self.T, self.k), "slot_map"),
+            _stream_ptr(stream, self.device)), "a2av_pack")
+
+    def combine(self, y, gate_w, slot_map, out, stream=None):
+        import torch
+
+        _check(self.lib, self.lib.a2av_combine(
+            self.handle, self._rows(y, "y"), self._t(gate_w, torch.float32, (self.R, self.T, self.k), "gate_w"),
+            self._t(slot_map, torch.int32, (self.R, self.T, self.k), "slot_map"),
+            self._t(out, torch.bfloat16, (self.R, self.T, self.H), "out"),
+            _stream_ptr(stream, self.device)), "a2av_combine")
+
+    def expert_scale(self, recv, topk_idx, slot_map, y, stream=None):
+        import torch
+
+        _check(self.lib, self.lib.a2av_expert_scale(
+            self.handle, self._rows(recv, "recv"), self._t(topk_idx, torch.int32, (self.R, self.T, self.k), "topk_idx"),
+            self._t(slot_map, torch.int32, (self.R, self.T, self.k), "slot_map"), self._rows(y, "y"),
+            _stream_ptr(stream, self.device)), "a2av_expert_scale")
+
+    def read_status(self, clear: bool = False, stream=None) -> int:
+        bits = ctypes.c_uint32(0)
+        _check(self.lib, self.lib.a2av_read_device_status(self.handle, ctypes.byref(bits), int(clear),
+                                                          _stream_ptr(stream, self.device)), "a2av_read_device_status")
+        return int(bits.value)
+
+    @property
+    def launches(self) -> int:
+        return int(self.lib.a2av_plan_launches(self.handle))

@@ -1,0 +1,294 @@
+// C ABI of the device-resident dispatch/combine data plane: validation, plans,
+// and the enqueueing calls.  All allocation happens in a2av_plan_create; the
+// enqueueing calls only launch kernels on the caller's stream (no sync, no
+// allocation, no device-to-host reads), so they can be captured in a CUDA
+// graph and replayed while the routing in device memory changes.
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+
+#include "a2av_internal.cuh"
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+a2av_status_t cuda_fail(cudaError_t e, const char *where) {
+    snprintf(g_last_error, sizeof g_last_error, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+    return A2AV_ERR_CUDA;
+}
+
+// Makes the plan's device current for the duration of a call and restores the
+// caller's device afterwards.
+struct DeviceGuard {
+    int prev = -1;
+    cudaError_t err = cudaSuccess;
+    explicit DeviceGuard(int dev) {
+        err = cudaGetDevice(&prev);
+        if (err == cudaSuccess && prev != dev) err = cudaSetDevice(dev);
+        else if (err == cudaSuccess) prev = -1;
+    }
+    ~DeviceGuard() {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+bool aligned(const void *p, size_t a) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool splits_ok(const a2av_splits_t *sp) {
+    return sp && aligned(sp->send_counts, 4) && aligned(sp->send_offsets, 4) && aligned(sp->recv_counts, 4) &&
+           aligned(sp->recv_offsets, 4) && aligned(sp->recv_expert_counts, 4) && aligned(sp->recv_total, 4) &&
+           aligned(sp->window_base, 4);
+}
+
+a2av::Splits to_internal(const a2av_splits_t *sp) {
+    return a2av::Splits{sp->send_counts, sp->send_offsets, sp->recv_counts, sp->recv_offsets,
+                        sp->recv_expert_counts, sp->recv_total, sp->window_base};
+}
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+size_t row_bytes(const a2av_plan_s *p) { return (size_t)p->g.H * 2; }
+size_t tokens(const a2av_plan_s *p) { return (size_t)p->g.R * p->g.T; }
+
+}  // namespace
+
+extern "C" {
+
+a2av_status_t a2av_config_check(const a2av_config_t *c) {
+    if (!c) return A2AV_ERR_INVALID_ARG;
+    if (c->num_ranks < 1 || c->num_ranks > a2av::kMaxRanks) return A2AV_ERR_INVALID_ARG;
+    if (c->num_experts < c->num_ranks || c->num_experts > a2av::kMaxExperts) return A2AV_ERR_INVALID_ARG;
+    if (c->num_experts % c->num_ranks != 0) return A2AV_ERR_INVALID_ARG;
+    if (c->tokens_per_rank < 1) return A2AV_ERR_INVALID_ARG;
+    if (c->hidden < 8 || c->hidden % 8 != 0) return A2AV_ERR_INVALID_ARG;
+    if (c->topk < 1 || c->topk > a2av::kMaxTopk) return A2AV_ERR_INVALID_ARG;
+    const long long assignments = (long long)c->num_ranks * c->tokens_per_rank * c->topk;
+    if (assignments >= (1ll << 31)) return A2AV_ERR_INVALID_ARG;
+    if ((long long)c->tokens_per_rank * c->topk >= (1ll << 31) - a2av::kHistTile) return A2AV_ERR_INVALID_ARG;
+    if (c->window_mode == A2AV_WINDOW_FIXED) {
+        if (c->window_rows < 0 || (long long)c->num_ranks * c->window_rows >= (1ll << 31)) return A2AV_ERR_INVALID_ARG;
+    } else if (c->window_mode != A2AV_WINDOW_PACKED) {
+        return A2AV_ERR_INVALID_ARG;
+    }
+    if (c->device < 0) return A2AV_ERR_INVALID_ARG;
+    if (c->flags & ~(uint32_t)A2AV_FLAG_PACK_LSU) return A2AV_ERR_INVALID_ARG;
+    if (c->pack_ctas_per_sm < 0 || c->pack_ctas_per_sm > 4) return A2AV_ERR_INVALID_ARG;
+    if (c->pack_stage_bytes < 0 || c->pack_stage_bytes % 16 != 0 || c->pack_stage_bytes > 65536)
+        return A2AV_ERR_INVALID_ARG;
+    return A2AV_OK;
+}
+
+int64_t a2av_recv_arena_rows(const a2av_config_t *c) {
+    if (a2av_config_check(c) != A2AV_OK) return -1;
+    if (c->window_mode == A2AV_WINDOW_FIXED) return (int64_t)c->num_ranks * c->window_rows;
+    return (int64_t)c->num_ranks * c->tokens_per_rank * c->topk;
+}
+
+a2av_status_t a2av_plan_create(const a2av_config_t *cfg, a2av_plan_t *out_plan) {
+    if (!out_plan) return A2AV_ERR_INVALID_ARG;
+    *out_plan = nullptr;
+    a2av_status_t st = a2av_config_check(cfg);
+    if (st != A2AV_OK) {
+        snprintf(g_last_error, sizeof g_last_error, "invalid configuration");
+        return st;
+    }
+    DeviceGuard guard(cfg->device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+
+    a2av_plan_s *p = new (std::nothrow) a2av_plan_s();
+    if (!p) return A2AV_ERR_NO_MEMORY;
+    p->cfg = *cfg;
+    a2av::Geometry &g = p->g;
+    g.R = cfg->num_ranks;
+    g.E = cfg->num_experts;
+    g.T = cfg->tokens_per_rank;
+    g.H = cfg->hidden;
+    g.k = cfg->topk;
+    g.epr = g.E / g.R;
+    g.tiles = (int32_t)(((long long)g.T * g.k + a2av::kHistTile - 1) / a2av::kHistTile);
+    g.window_mode = cfg->window_mode;
+    g.window_rows = cfg->window_mode == A2AV_WINDOW_FIXED ? cfg->window_rows : 0;
+    p->pack_tma = (cfg->flags & A2AV_FLAG_PACK_LSU) ? 0 : 1;
+
+    cudaError_t e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, cfg->device);
+    if (e != cudaSuccess) {
+        delete p;
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+    }
+
+    // Workspace: tile bases [R][tiles][E], dest bases [R][E], counters [R+1], status.
+    const size_t n_tile = (size_t)g.R * g.tiles * g.E;
+    const size_t n_dest = (size_t)g.R * g.E;
+    const size_t off_dest = ((n_tile * 4) + 255) / 256 * 256;
+    const size_t off_cnt = off_dest + ((n_dest * 4) + 255) / 256 * 256;
+    const size_t off_status = off_cnt + (((size_t)g.R + 1) * 4 + 255) / 256 * 256;
+    p->workspace_bytes = off_status + 256;
+    e = cudaMalloc(&p->workspace, p->workspace_bytes);
+    if (e != cudaSuccess) {
+        delete p;
+        cuda_fail(e, "cudaMalloc(workspace)");
+        return A2AV_ERR_NO_MEMORY;
+    }
+    char *base = static_cast<char *>(p->workspace);
+    p->tile_base = reinterpret_cast<int32_t *>(base);
+    p->dest_base = reinterpret_cast<int32_t *>(base + off_dest);
+    p->counters = reinterpret_cast<uint32_t *>(base + off_cnt);
+    p->status = reinterpret_cast<uint32_t *>(base + off_status);
+    e = cudaMemset(p->workspace, 0, p->workspace_bytes);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = a2av::configure_hist(*p);
+    if (e == cudaSuccess) e = a2av::configure_pack(*p);
+    if (e == cudaSuccess) e = a2av::configure_combine(*p);
+    if (e != cudaSuccess) {
+        cudaFree(p->workspace);
+        delete p;
+        return cuda_fail(e, "plan configuration");
+    }
+    *out_plan = p;
+    return A2AV_OK;
+}
+
+a2av_status_t a2av_plan_destroy(a2av_plan_t p) {
+    if (!p) return A2AV_OK;
+    DeviceGuard guard(p->cfg.device);
+    cudaError_t e = cudaFree(p->workspace);
+    delete p;
+    return e == cudaSuccess ? A2AV_OK : cuda_fail(e, "cudaFree(workspace)");
+}
+
+a2av_status_t a2av_splits(a2av_plan_t p, const int32_t *topk_idx, const a2av_splits_t *splits, int32_t *slot_map,
+                          void *stream) {
+    if (!p || !aligned(topk_idx, 4) || !aligned(slot_map, 4) || !splits_ok(splits)) return A2AV_ERR_INVALID_ARG;
+    DeviceGuard guard(p->cfg.device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    a2av::HistArgs a;
+    a.g = p->g;
+    a.idx = topk_idx;
+    a.slot_map = slot_map;
+    a.tile_base = p->tile_base;
+    a.dest_base = p->dest_base;
+    a.counters = p->counters;
+    a.status = p->status;
+    a.sp = to_internal(splits);
+    cudaError_t e = a2av::launch_hist(*p, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "splits kernel launch");
+    p->launches += 1;
+    return A2AV_OK;
+}
+
+a2av_status_t a2av_pack(a2av_plan_t p, const void *x, const int32_t *topk_idx, const a2av_splits_t *splits,
+                        void *recv, int32_t *slot_map, void *stream) {
+    if (!p || !aligned(x, 16) || !aligned(recv, 16) || !aligned(topk_idx, 4) || !aligned(slot_map, 4) ||
+        !splits_ok(splits))
+        return A2AV_ERR_INVALID_ARG;
+    const int64_t rows = a2av_recv_arena_rows(&p->cfg);
+    if (overlap(x, tokens(p) * row_bytes(p), recv, (size_t)rows * row_bytes(p))) return A2AV_ERR_INVALID_ARG;
+    DeviceGuard guard(p->cfg.device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    a2av::PackArgs a;
+    memset(&a, 0, sizeof a);
+    a.g = p->g;
+    a.x = static_cast<const uint16_t *>(x);
+    a.idx = topk_idx;
+    a.slot_map = slot_map;
+    a.tile_base = p->tile_base;
+    a.dest_base = p->dest_base;
+    a.window_base = splits->window_base;
+    a.recv = static_cast<uint16_t *>(recv);
+    a.status = p->status;
+    cudaError_t e = a2av::launch_pack(*p, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pack kernel launch");
+    p->launches += 1;
+    return A2AV_OK;
+}
+
+a2av_status_t a2av_dispatch(a2av_plan_t p, const void *x, const int32_t *topk_idx, const a2av_splits_t *splits,
+                            void *recv, int32_t *slot_map, void *stream) {
+    if (!p || !aligned(x, 16) || !aligned(recv, 16) || !aligned(topk_idx, 4) || !aligned(slot_map, 4) ||
+        !splits_ok(splits))
+        return A2AV_ERR_INVALID_ARG;
+    const int64_t rows = a2av_recv_arena_rows(&p->cfg);
+    if (overlap(x, tokens(p) * row_bytes(p), recv, (size_t)rows * row_bytes(p))) return A2AV_ERR_INVALID_ARG;
+    a2av_status_t st = a2av_splits(p, topk_idx, splits, slot_map, stream);
+    if (st != A2AV_OK) return st;
+    return a2av_pack(p, x, topk_idx, splits, recv, slot_map, stream);
+}
+
+a2av_status_t a2av_combine(a2av_plan_t p, const void *y, const float *gate_w, const int32_t *slot_map, void *out,
+                           void *stream) {
+    if (!p || !aligned(y, 16) || !aligned(out, 16) || !aligned(gate_w, 4) || !aligned(slot_map, 4))
+        return A2AV_ERR_INVALID_ARG;
+    const int64_t rows = a2av_recv_arena_rows(&p->cfg);
+    if (overlap(y, (size_t)rows * row_bytes(p), out, tokens(p) * row_bytes(p))) return A2AV_ERR_INVALID_ARG;
+    DeviceGuard guard(p->cfg.device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    a2av::CombineArgs a;
+    a.g = p->g;
+    a.y = static_cast<const uint16_t *>(y);
+    a.gate = gate_w;
+    a.slot_map = slot_map;
+    a.out = static_cast<uint16_t *>(out);
+    a.arena_rows = rows;
+    a.status = p->status;
+    cudaError_t e = a2av::launch_combine(*p, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
+    p->launches += 1;
+    return A2AV_OK;
+}
+
+a2av_status_t a2av_expert_scale(a2av_plan_t p, const void *recv, const int32_t *topk_idx, const int32_t *slot_map,
+                                void *y, void *stream) {
+    if (!p || !aligned(recv, 16) || !aligned(y, 16) || !aligned(topk_idx, 4) || !aligned(slot_map, 4))
+        return A2AV_ERR_INVALID_ARG;
+    DeviceGuard guard(p->cfg.device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    a2av::ScaleArgs a;
+    a.g = p->g;
+    a.recv = static_cast<const uint16_t *>(recv);
+    a.idx = topk_idx;
+    a.slot_map = slot_map;
+    a.y = static_cast<uint16_t *>(y);
+    a.arena_rows = a2av_recv_arena_rows(&p->cfg);
+    a.status = p->status;
+    cudaError_t e = a2av::launch_scale(*p, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "expert scale kernel launch");
+    p->launches += 1;
+    return A2AV_OK;
+}
+
+a2av_status_t a2av_read_device_status(a2av_plan_t p, uint32_t *bits, int clear, void *stream) {
+    if (!p || !bits) return A2AV_ERR_INVALID_ARG;
+    DeviceGuard guard(p->cfg.device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(bits, p->status, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && clear) {
+        e = cudaMemsetAsync(p->status, 0, sizeof(uint32_t), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    }
+    return e == cudaSuccess ? A2AV_OK : cuda_fail(e, "read device status");
+}
+
+const void *a2av_device_status_ptr(a2av_plan_t p) { return p ? p->status : nullptr; }
+
+int64_t a2av_plan_launches(a2av_plan_t p) { return p ? p->launches : -1; }
+
+const char *a2av_status_string(a2av_status_t s) {
+    switch (s) {
+        case A2AV_OK: return "ok";
+        case A2AV_ERR_INVALID_ARG: return "invalid argument";
+        case A2AV_ERR_CUDA: return "CUDA error";
+        case A2AV_ERR_NO_MEMORY: return "out of device memory";
+    }
+    return "unknown status";
+}
+
+const char *a2av_last_error(void) { return g_last_error; }
+
+}  // extern "C"

@@ -1,0 +1,298 @@
+// Fused pack + exchange: every token row x[s][t] is read once and stored
+// straight into the destination window of each of its k experts, at the row
+// its stable expert order gives it.  No send buffer, no padding: only routed
+// rows move, from the caller's buffer straight into the caller's windows
+// (NCCLX pages: the abhik.ai sections on CTran's zero-copy transfers and on
+// inference; the hungchun0201 digest, 3.3 AllToAllvDynamic).
+//
+// Row of assignment (s, t, j) with expert e on rank d = e / (E/R):
+//   rel = dest_base[s][e] + tile_base[s][tile(t*k+j)][e] + rank_in_tile
+//   row = window_base[d] + rel        (dropped if rel >= window_rows, fixed mode)
+// where dest_base = recv_offsets[d][s] + send_offsets[s][e] - send_offsets[s][d*E/R]
+// (all produced on the device by the splits kernel).
+//
+// Two variants:
+//   * TMA bulk (default): persistent grid, one warp per CTA.  Row chunks are
+//     brought into a ring of shared-memory stages by cp.async.bulk
+//     (completion on an mbarrier) and written out by k cp.async.bulk stores,
+//     one per destination row; the ring keeps many KB in flight per SM with a
+//     single issuing thread.  Lanes compute the destination rows of the next
+//     batch of tokens while the copies run.
+//   * LSU: warp per token, 16-byte vector loads (no L1 allocation) and stores.
+#include "a2av_internal.cuh"
+
+namespace a2av {
+namespace {
+
+constexpr uint32_t kFull = 0xffffffffu;
+constexpr long long kWaitLimit = 1ll << 22;  // bounded spin on our own copies
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    for (long long it = 0; it < kWaitLimit; ++it)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst_smem)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_store(void *dst, const void *src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src_smem)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Final arena row of assignment j of flat token `tok` (reads the rank inside
+// its histogram tile from slot_map), or -1 if dropped.
+__device__ __forceinline__ int32_t final_row(const PackArgs &a, long long tok, int j, uint32_t &ovf) {
+    const Geometry &g = a.g;
+    const size_t ga = (size_t)tok * g.k + j;
+    const int e = __ldg(a.idx + ga);
+    const int r = a.slot_map[ga];
+    if (e < 0 || e >= g.E || r < 0) return -1;
+    const int s = (int)(tok / g.T);
+    const int t = (int)(tok - (long long)s * g.T);
+    const int tl = (t * g.k + j) / kHistTile;
+    const int d = e / g.epr;
+    const long long rel = (long long)__ldg(a.dest_base + (size_t)s * g.E + e) +
+                          __ldg(a.tile_base + ((size_t)s * g.tiles + tl) * g.E + e) + r;
+    const long long cap = g.window_mode == A2AV_WINDOW_FIXED ? g.window_rows : (long long)g.R * g.T * g.k;
+    if (rel < 0 || rel >= cap) {
+        ovf = 1;
+        return -1;
+    }
+    const long long row = (long long)__ldg(a.window_base + d) + rel;
+    const long long arena = g.window_mode == A2AV_WINDOW_FIXED ? (long long)g.R * g.window_rows
+                                                               : (long long)g.R * g.T * g.k;
+    if (row < 0 || row >= arena) {
+        ovf = 1;
+        return -1;
+    }
+    return (int32_t)row;
+}
+
+// Rows of a batch of `bt` tokens starting at tok0: lane l holds assignment
+// (tok0 + l / k, l % k); also writes them to slot_map.
+__device__ __forceinline__ int32_t batch_rows(const PackArgs &a, long long tok0, long long tok_end, int bt,
+                                              int lane, uint32_t &ovf) {
+    const int k = a.g.k;
+    const int b = lane / k, j = lane - b * k;
+    const long long tok = tok0 + b;
+    if (b >= bt || tok >= tok_end) return -1;
+    const int32_t row = final_row(a, tok, j, ovf);
+    a.slot_map[(size_t)tok * k + j] = row;
+    return row;
+}
+
+__global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const Geometry &g = a.g;
+    const int lane = threadIdx.x;
+    const int NS = a.stages, CH = a.chunk_bytes, nch = a.nchunks;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)NS * CH);
+
+    const long long ntok = (long long)g.R * g.T;
+    const long long per = (ntok + gridDim.x - 1) / gridDim.x;
+    const long long tb = min(ntok, (long long)blockIdx.x * per);
+    const long long te = min(ntok, tb + per);
+    if (tb >= te) return;
+    const long long n = (te - tb) * nch;
+    const size_t rowb = (size_t)g.H * 2;
+    const int BT = max(1, 32 / g.k);
+    const char *x = reinterpret_cast<const char *>(a.x);
+    char *recv = reinterpret_cast<char *>(a.recv);
+
+    if (lane == 0) {
+        for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    auto issue_load = [&](long long p) {
+        const long long tok = tb + p / nch;
+        const uint32_t off = (uint32_t)(p % nch) * CH;
+        const uint32_t bytes = (uint32_t)min((size_t)CH, rowb - off);
+        uint64_t *bar = &bars[p % NS];
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_load(smem + (size_t)(p % NS) * CH, x + (size_t)tok * rowb + off, bytes, bar);
+    };
+    const long long pre = min(n, (long long)NS);
+    if (lane == 0)
+        for (long long p = 0; p < pre; ++p) issue_load(p);
+    long long issued = pre;  // loads issued so far (units 0..issued-1)
+
+    uint32_t ovf = 0;
+    long long batch_tok0 = tb;
+    int32_t cur = batch_rows(a, batch_tok0, te, BT, lane, ovf);
+    int32_t nxt = batch_rows(a, batch_tok0 + BT, te, BT, lane, ovf);
+    bool timed_out = false;
+    long long i = 0;
+    for (; i < n; ++i) {
+        const long long tok = tb + i / nch;
+        const int c = (int)(i % nch);
+        if (tok >= batch_tok0 + BT) {
+            batch_tok0 += BT;
+            cur = nxt;
+            nxt = batch_rows(a, batch_tok0 + BT, te, BT, lane, ovf);
+        }
+        const int st = (int)(i % NS);
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait_bounded(&bars[st], (uint32_t)((i / NS) & 1));
+        ok = __shfl_sync(kFull, ok, 0);
+        if (!ok) {
+            timed_out = true;
+            break;
+        }
+        const uint32_t off = (uint32_t)c * CH;
+        const uint32_t bytes = (uint32_t)min((size_t)CH, rowb - off);
+        const int lb = (int)(tok - batch_tok0);
+        if (lane == 0) fence_proxy_async_smem();
+        for (int j = 0; j < g.k; ++j) {
+            const int32_t rj = __shfl_sync(kFull, cur, lb * g.k + j);
+            if (lane == 0 && rj >= 0) bulk_store(recv + (size_t)rj * rowb + off, smem + (size_t)st * CH, bytes);
+        }
+        if (lane == 0) {
+            bulk_commit();
+            const long long p = i - 1 + NS;
+            if (i >= 1 && p < n) {
+                bulk_wait_read_1();
+                issue_load(p);
+            }
+        }
+        issued = min(n, max(issued, i - 1 + NS + 1));
+        __syncwarp();
+    }
+    if (lane == 0) {
+        bulk_wait_all();
+        if (timed_out) {
+            // Leave only after every load this CTA issued has landed (bounded).
+            for (long long p = i; p < issued; ++p) mbar_wait_bounded(&bars[p % NS], (uint32_t)((p / NS) & 1));
+            atomicOr(a.status, kDevWaitTimeout);
+        }
+    }
+    if (__any_sync(kFull, ovf != 0) && lane == 0) atomicOr(a.status, (uint32_t)A2AV_DEV_WINDOW_OVERFLOW);
+}
+
+template <int U>
+__global__ void __launch_bounds__(256) pack_lsu_kernel(const PackArgs a) {
+    const Geometry &g = a.g;
+    const int lane = threadIdx.x & 31;
+    const long long ntok = (long long)g.R * g.T;
+    const int nv = g.H >> 3;
+    const size_t rowb = (size_t)g.H * 2;
+    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+    uint32_t ovf = 0;
+    for (long long u = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < ntok; u += nw) {
+        int32_t row = -1;
+        if (lane < g.k) {
+            row = final_row(a, u, lane, ovf);
+            a.slot_map[(size_t)u * g.k + lane] = row;
+        }
+        const char *src = reinterpret_cast<const char *>(a.x) + (size_t)u * rowb;
+        for (int vb = 0; vb < nv; vb += 32 * U) {
+            uint4 buf[U];
+#pragma unroll
+            for (int q = 0; q < U; ++q) {
+                const int v = vb + q * 32 + lane;
+                if (v < nv) buf[q] = ld_stream_v4(src + (size_t)v * 16);
+            }
+            for (int j = 0; j < g.k; ++j) {
+                const int32_t rj = __shfl_sync(kFull, row, j);
+                if (rj < 0) continue;
+                char *dst = reinterpret_cast<char *>(a.recv) + (size_t)rj * rowb;
+#pragma unroll
+                for (int q = 0; q < U; ++q) {
+                    const int v = vb + q * 32 + lane;
+                    if (v < nv) st_v4(dst + (size_t)v * 16, buf[q]);
+                }
+            }
+        }
+    }
+    if (__any_sync(kFull, ovf != 0) && lane == 0) atomicOr(a.status, (uint32_t)A2AV_DEV_WINDOW_OVERFLOW);
+}
+
+constexpr int kLsuUnroll = 4;
+constexpr size_t kTmaChunkMax = 16384;
+
+}  // namespace
+
+cudaError_t configure_pack(a2av_plan_s &p) {
+    const size_t rowb = (size_t)p.g.H * 2;
+    if (!p.pack_tma) {
+        p.pack.block = 256;
+        int per_sm = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pack_lsu_kernel<kLsuUnroll>, 256, 0);
+        if (e != cudaSuccess) return e;
+        p.pack.grid = p.num_sms * (per_sm > 0 ? per_sm : 1);
+        p.pack.smem = 0;
+        return cudaSuccess;
+    }
+    const int ctas_per_sm = p.cfg.pack_ctas_per_sm > 0 ? p.cfg.pack_ctas_per_sm : 1;
+    size_t chunk = p.cfg.pack_stage_bytes > 0 ? (size_t)p.cfg.pack_stage_bytes : kTmaChunkMax;
+    chunk = (chunk + 15) / 16 * 16;
+    if (chunk > rowb) chunk = rowb;
+    const int nch = (int)((rowb + chunk - 1) / chunk);
+    int max_optin = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p.cfg.device);
+    if (e != cudaSuccess) return e;
+    size_t budget = (size_t)max_optin / ctas_per_sm;
+    budget = budget > 2048 ? budget - 2048 : budget;  // leave room for the static/runtime reservation
+    int stages = (int)((budget) / (chunk + 8));
+    if (stages > 32) stages = 32;
+    if (stages < 2) return cudaErrorInvalidConfiguration;
+    p.pack_chunk_bytes = (int32_t)chunk;
+    p.pack_nchunks = nch;
+    p.pack_stages = stages;
+    p.pack.block = 32;
+    p.pack.smem = (size_t)stages * chunk + (size_t)stages * 8;
+    p.pack.grid = p.num_sms * ctas_per_sm;
+    return cudaFuncSetAttribute(pack_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.pack.smem);
+}
+
+cudaError_t launch_pack(const a2av_plan_s &p, const PackArgs &a, cudaStream_t s) {
+    if (p.pack_tma) {
+        PackArgs b = a;
+        b.chunk_bytes = p.pack_chunk_bytes;
+        b.nchunks = p.pack_nchunks;
+        b.stages = p.pack_stages;
+        pack_tma_kernel<<<p.pack.grid, p.pack.block, p.pack.smem, s>>>(b);
+    } else {
+        pack_lsu_kernel<kLsuUnroll><<<p.pack.grid, p.pack.block, 0, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace a2av

@@ -1,0 +1,212 @@
+/*
+ * a2av.h -- C ABI of a device-resident MoE dispatch/combine data plane for
+ * GB300 (sm_103a): the data path of an AllToAllv whose split counts never
+ * leave GPU memory.
+ *
+ * What the operation is.  NCCLX, "Collective Communication for 100k+ GPUs"
+ * (Meta), Section 6.1, as told on the pages
+ *   abhik.ai/papers/ncclx, section "Inference: small messages, unknown sizes";
+ *   hungchun0201 research digest, section 3.3 "AllToAllvDynamic";
+ *   qiguanping.github.io deep dive, section 7 (Figures 13, 16, 17):
+ * a router picks the experts of each token, the tokens are sorted by expert
+ * into a send buffer and an AllToAllv sends each one to the rank that holds
+ * its expert (Figure 13); the counts live in GPU memory, are read when the
+ * collective runs, only real tokens are sent (no padding to the worst case),
+ * and the collective returns the counts it received; afterwards the expert
+ * outputs come back and are combined.
+ *
+ * Here the R ranks are R windows in one GPU's memory, and the exchange is a
+ * direct store of each token row into its destination window (no
+ * intermediate send buffer).  Readings of what the pages leave open:
+ *   - expert e lives on rank e / (E/R) (contiguous blocks);
+ *   - "sorted by expert" is stable: expert, then token t, then slot j;
+ *   - window d holds the segments of sources 0..R-1 back to back, in source
+ *     order, with no gaps;
+ *   - combine: out = bf16_rne(sum_j w_j * y[slot(t,j)]) accumulated in fp32
+ *     from 0 in slot order, product and sum each rounded on its own.
+ *
+ * Conventions for every call below.
+ *   - Every tensor pointer is a DEVICE pointer into memory of the plan's
+ *     device, owned by the caller, row-major (C order), and must stay valid
+ *     until the work enqueued on `stream` has finished.  The library never
+ *     frees or retains them.
+ *   - Row buffers (x, recv, y, out) must be 16-byte aligned and H % 8 == 0
+ *     (rows move as 16-byte vectors); integer/float arrays 4-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Enqueueing calls are asynchronous: they return after
+ *     launching, never synchronise, allocate, or read device memory back, and
+ *     can be captured into a CUDA graph.  A returned A2AV_OK means "enqueued".
+ *   - Host-side argument errors are returned synchronously
+ *     (A2AV_ERR_INVALID_ARG) and nothing is enqueued.  Data errors found on
+ *     the device (expert id out of range, fixed window too small) set sticky
+ *     bits in the plan's device status word (A2AV_DEV_*), skip the offending
+ *     store and never write out of bounds; read them with
+ *     a2av_read_device_status outside capture.
+ *   - A plan's workspace is shared by its calls: use one plan from one
+ *     stream at a time (or order the streams).  Calls that overlap on the
+ *     device through one plan race.
+ *
+ * Layouts (int32 unless said otherwise; R ranks, E experts, T tokens per
+ * rank, H hidden, k experts per token, Epr = E/R):
+ *   x            bf16  [R][T][H]           token rows, per source rank
+ *   topk_idx     int32 [R][T][k]           global expert ids
+ *   gate_w       fp32  [R][T][k]           combine weights
+ *   recv, y      bf16  [arena_rows][H]     windows (recv layout)
+ *   slot_map     int32 [R][T][k]           arena row of each assignment, -1 if dropped
+ *   out          bf16  [R][T][H]
+ *   splits.send_counts        [R][E]       rows rank s sends to expert e
+ *   splits.send_offsets       [R][E]       exclusive scan of send_counts over e
+ *   splits.recv_counts        [R][R]       [d][s] rows window d receives from s
+ *   splits.recv_offsets       [R][R]       [d][s] exclusive scan over s
+ *   splits.recv_expert_counts [R][R][Epr]  [d][s][le] = send_counts[s][d*Epr+le]
+ *   splits.recv_total         [R]          rows window d receives
+ *   splits.window_base        [R]          arena row where window d starts
+ */
+#ifndef A2AV_H
+#define A2AV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct a2av_plan_s *a2av_plan_t;
+
+/* Host-side result of every call. */
+typedef enum {
+    A2AV_OK = 0,
+    A2AV_ERR_INVALID_ARG = 1, /* bad config, null/misaligned pointer, size limit */
+    A2AV_ERR_CUDA = 2,        /* a CUDA runtime call failed (message: a2av_last_error) */
+    A2AV_ERR_NO_MEMORY = 3,   /* workspace allocation failed */
+} a2av_status_t;
+
+/* Sticky bits of the device status word. */
+enum {
+    A2AV_DEV_BAD_EXPERT = 1u << 0,      /* an expert id outside [0, E): dropped, slot -1 */
+    A2AV_DEV_WINDOW_OVERFLOW = 1u << 1, /* fixed mode: a window got more than window_rows rows */
+    A2AV_DEV_BAD_SLOT = 1u << 2,        /* combine/expert stand-in: a slot_map entry past the arena, skipped */
+    A2AV_DEV_WAIT_TIMEOUT = 1u << 31,   /* a bounded wait on the kernel's own copies gave up (not expected) */
+};
+
+/* Window placement of the R destination windows in the recv arena. */
+enum {
+    A2AV_WINDOW_PACKED = 0, /* window d starts right after window d-1: arena of exactly R*T*k rows */
+    A2AV_WINDOW_FIXED = 1,  /* window d owns rows [d*window_rows, (d+1)*window_rows) */
+};
+
+/* Variant flags (a2av_config_t.flags). */
+enum {
+    A2AV_FLAG_PACK_LSU = 1u << 0, /* pack+exchange with 16-byte vector loads/stores instead of TMA bulk copies */
+};
+
+typedef struct {
+    int32_t num_ranks;       /* R >= 1, <= 64 */
+    int32_t num_experts;     /* E, a multiple of R, <= 2048 */
+    int32_t tokens_per_rank; /* T >= 1; R*T*k < 2^31 */
+    int32_t hidden;          /* H, a multiple of 8, >= 8 */
+    int32_t topk;            /* k, 1..32 */
+    int32_t window_mode;     /* A2AV_WINDOW_PACKED or A2AV_WINDOW_FIXED */
+    int64_t window_rows;     /* fixed mode: rows per window (R*window_rows < 2^31); ignored when packed */
+    int32_t device;          /* CUDA device ordinal the plan and all its tensors live on */
+    uint32_t flags;          /* A2AV_FLAG_* */
+    int32_t pack_ctas_per_sm; /* TMA pack: resident CTAs per SM, 1..4 (0 = 1) */
+    int32_t pack_stage_bytes; /* TMA pack: bytes per shared-memory stage, multiple of 16 (0 = min(row, 16 KiB)) */
+} a2av_config_t;
+
+/* Caller-owned device arrays the split counts and offsets are written to
+ * (layouts above).  They are GPU-resident outputs: the host never needs them
+ * for the data path. */
+typedef struct {
+    int32_t *send_counts;
+    int32_t *send_offsets;
+    int32_t *recv_counts;
+    int32_t *recv_offsets;
+    int32_t *recv_expert_counts;
+    int32_t *recv_total;
+    int32_t *window_base;
+} a2av_splits_t;
+
+/* Host-only check of a configuration against the limits above; touches no GPU. */
+a2av_status_t a2av_config_check(const a2av_config_t *cfg);
+
+/* Rows the recv arena needs: R*T*k (packed) or R*window_rows (fixed); -1 for
+ * an invalid configuration.  Host-only. */
+int64_t a2av_recv_arena_rows(const a2av_config_t *cfg);
+
+/* Create a plan: validates `cfg`, allocates the plan's small device
+ * workspace (per-tile counts, completion counters, status word) on
+ * cfg->device and sets kernel attributes.  Synchronous; not capturable.
+ * Call it once, outside graph capture, and reuse the plan. */
+a2av_status_t a2av_plan_create(const a2av_config_t *cfg, a2av_plan_t *out_plan);
+
+/* Free the plan's workspace.  The caller must have finished all work
+ * enqueued with it.  NULL is accepted. */
+a2av_status_t a2av_plan_destroy(a2av_plan_t plan);
+
+/* Dispatch = a2av_splits followed by a2av_pack on `stream` (two kernels).
+ * Counts the routing on the device (the counts never go to the host), scans
+ * them into send/recv splits and window bases, and stores every token row
+ * x[s][t] once per routed expert straight into its destination window:
+ * recv[slot_map[s][t][j]] = x[s][t].  Only routed rows move; rows of the
+ * arena beyond each window's recv_total are left untouched.  recv must not
+ * overlap x.  [Inference section and Figure 13; digest 3.3: the counts are
+ * taken from device memory at execution time, nothing is padded, and the
+ * received counts are handed back -- here in splits.] */
+a2av_status_t a2av_dispatch(a2av_plan_t plan, const void *x, const int32_t *topk_idx,
+                            const a2av_splits_t *splits, void *recv, int32_t *slot_map, void *stream);
+
+/* First half of dispatch (one kernel): per-rank expert histogram with a
+ * fused device-side scan.  Fills every array of `splits` and leaves in
+ * slot_map an intermediate per-assignment rank that a2av_pack consumes
+ * (slot_map is final only after a2av_pack).  [Digest 3.3 and the Inference
+ * section: counts made and kept on the GPU; the received counts are part of
+ * the result.] */
+a2av_status_t a2av_splits(a2av_plan_t plan, const int32_t *topk_idx, const a2av_splits_t *splits,
+                          int32_t *slot_map, void *stream);
+
+/* Second half of dispatch (one kernel): pack + exchange.  Must follow
+ * a2av_splits with the same topk_idx, splits and slot_map on the same
+ * stream.  Writes recv rows and the final slot_map. */
+a2av_status_t a2av_pack(a2av_plan_t plan, const void *x, const int32_t *topk_idx,
+                        const a2av_splits_t *splits, void *recv, int32_t *slot_map, void *stream);
+
+/* Combine (one kernel): out[s][t] = bf16_rne(sum_{j=0..k-1, slot>=0}
+ * gate_w[s][t][j] * y[slot_map[s][t][j]]), fp32 accumulation from 0 in slot
+ * order with separately rounded products and sums.  y has the recv layout
+ * (the expert outputs written in place of, or beside, the received rows).
+ * out must not overlap y.  [Deep dive section 7, Figure 13: the token
+ * shuffle is followed by the combine.] */
+a2av_status_t a2av_combine(a2av_plan_t plan, const void *y, const float *gate_w, const int32_t *slot_map,
+                           void *out, void *stream);
+
+/* Expert stand-in used by checkable workloads (not part of the collective):
+ * for every assignment with slot >= 0, y[slot] = bf16_rne(float(recv[slot]) *
+ * (1 + e/E)), e its global expert id, computed in fp32 (e/E, then 1 + that,
+ * then the product).  y may equal recv (in place). */
+a2av_status_t a2av_expert_scale(a2av_plan_t plan, const void *recv, const int32_t *topk_idx,
+                                const int32_t *slot_map, void *y, void *stream);
+
+/* Copy the device status word to *bits (synchronises `stream`); if `clear`,
+ * reset it to 0 afterwards.  Not capturable. */
+a2av_status_t a2av_read_device_status(a2av_plan_t plan, uint32_t *bits, int clear, void *stream);
+
+/* Device address of the plan's 32-bit status word, for callers that read it
+ * themselves (for instance inside their own graph). */
+const void *a2av_device_status_ptr(a2av_plan_t plan);
+
+/* Number of kernels the plan has enqueued (or had captured) so far. */
+int64_t a2av_plan_launches(a2av_plan_t plan);
+
+/* Static text for a status value. */
+const char *a2av_status_string(a2av_status_t status);
+
+/* Text of the last CUDA error seen by this library on the calling thread
+ * (empty if none). */
+const char *a2av_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* A2AV_H */

@@ -12,8 +12,8 @@
  *   [P1] abhik.ai/papers/ncclx, section "Inference: small messages, unknown
  *        sizes" (Figure 13 pipeline; Section 6.1 AllToAllvDynamic);
  *   [P2] hungchun0201 research digest, section 3.3 "AllToAllvDynamic";
- *   [P3] qiguanping.github.io deep dive, section 7 (Figure 13 "token shuffle
- *        (dispatch) and combine"; Figures 16-17 GPU-resident metadata).
+ *   [P3] qiguanping.github.io deep dive, section 7 (Figure 13, dispatch
+ *        shuffle and combine; Figures 16-17, GPU-resident metadata).
  * What the pages fix:
  *   - a router chooses the experts of each token; the tokens are sorted by
  *     expert into a send buffer; an AllToAllv sends each one to the rank
@@ -25,7 +25,7 @@
  *   - the tokens come back and are combined [P3 section 7, Figure 13].
  * Readings where the pages are silent (each is stated again where used):
  *   R1  expert e lives on rank e / (E/R)   (contiguous blocks of E/R experts);
- *   R2  "sorted by expert" is a stable sort: expert ascending, then token t,
+ *   R2  the sort by expert is stable: expert ascending, then token t,
  *       then slot j;
  *   R3  the AllToAllv convention: window d holds the segments of sources
  *       0..R-1 back to back, in source order, with no gaps;
@@ -85,8 +85,8 @@ uint16_t oracle_f32_to_bf16(float f)
  * expert e's block in rank s's expert-sorted send buffer (R2).
  * recv_counts[d][s] = sum of send_counts[s][e] over the experts e of rank d
  * (R1): the counts rank d receives, i.e. the transpose of the per-rank send
- * counts summed over d's experts [P1 Inference: "returns the counts it
- * received"].  recv_offsets[d][s] = sum over s' < s of recv_counts[d][s'] (R3).
+ * counts summed over d's experts [P1 Inference: the collective hands back
+ * the counts it received].  recv_offsets[d][s] = sum over s' < s of recv_counts[d][s'] (R3).
  * recv_expert_counts[d][s][le] = send_counts[s][d*(E/R) + le].
  * recv_total[d] = sum over s of recv_counts[d][s].
  * window_base[d] = sum over d' < d of recv_total[d'] (packed) or d*W (fixed).
@@ -152,8 +152,8 @@ uint32_t oracle_splits(int R, int E, int T, int k, int window_mode, int64_t wind
  * send_pos[t][j] = position of assignment (t, j) of rank s in its
  * expert-sorted send buffer: send_offsets[s][e] + the number of earlier
  * assignments (t', j') < (t, j) of rank s with the same expert (R2, a stable
- * counting sort by expert key) [P1 Inference: "the tokens are sorted by
- * expert into a send buffer"].  Dropped ids get -1.
+ * counting sort by expert key) [P1 Inference, Figure 13: the send buffer is
+ * ordered by expert].  Dropped ids get -1.
  */
 static void send_positions(int E, int T, int k, const int32_t *idx_s, const int32_t *send_offsets_s,
                            int32_t *running, int32_t *send_pos)

@@ -1,0 +1,108 @@
+"""The C-ABI library builds, loads without a GPU, and exports every function
+that include/*.h declares; host-only calls validate configurations."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(a2av_\w+)\s*\(", src, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from combine_device_resident_gb300 import build
+
+    build.build()
+    from combine_device_resident_gb300 import load_library
+
+    return load_library()
+
+
+def test_header_declares_the_calls():
+    names = _declared_functions()
+    for must in ("a2av_dispatch", "a2av_combine", "a2av_splits", "a2av_pack", "a2av_plan_create"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from combine_device_resident_gb300 import EXPORTED
+
+    declared = _declared_functions()
+    assert declared, "no declarations found"
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared but not exported"
+    assert sorted(EXPORTED) == sorted(declared), "binding's symbol list out of step with the header"
+
+
+def _cfg(**kw):
+    from combine_device_resident_gb300 import make_config
+
+    base = dict(R=8, E=16, T=1024, H=5120, k=1)
+    base.update(kw)
+    return make_config(**base)
+
+
+def test_config_check_host_only(lib):
+    ok = [_cfg(), _cfg(R=1, E=1, T=1, H=8, k=1), _cfg(R=64, E=2048, T=3, H=8, k=32),
+          _cfg(window_mode="fixed", window_rows=100)]
+    bad = [_cfg(R=0), _cfg(R=65, E=130), _cfg(E=12, R=8), _cfg(E=4096, R=8), _cfg(H=12), _cfg(H=0), _cfg(k=0),
+           _cfg(k=33), _cfg(T=0), _cfg(window_mode=2), _cfg(window_mode="fixed", window_rows=-1),
+           _cfg(R=64, E=64, T=1 << 20, k=32), _cfg(flags=1 << 7), _cfg(pack_stage_bytes=24),
+           _cfg(pack_ctas_per_sm=9)]
+    for c in ok:
+        assert lib.a2av_config_check(ctypes.byref(c)) == 0
+    for c in bad:
+        assert lib.a2av_config_check(ctypes.byref(c)) == 1
+    assert lib.a2av_config_check(None) == 1
+
+
+def test_arena_rows(lib):
+    assert lib.a2av_recv_arena_rows(ctypes.byref(_cfg(R=32, E=256, T=2048, k=8))) == 32 * 2048 * 8
+    assert lib.a2av_recv_arena_rows(ctypes.byref(_cfg(window_mode="fixed", window_rows=2048))) == 8 * 2048
+    assert lib.a2av_recv_arena_rows(ctypes.byref(_cfg(H=7))) == -1
+
+
+def test_plan_create_rejects_bad_config_without_touching_a_gpu(lib):
+    h = ctypes.c_void_p()
+    assert lib.a2av_plan_create(ctypes.byref(_cfg(H=12)), ctypes.byref(h)) == 1
+    assert not h.value
+    assert lib.a2av_plan_create(ctypes.byref(_cfg()), None) == 1
+
+
+def test_null_arguments_are_rejected(lib):
+    from combine_device_resident_gb300.binding import SplitsPtrs
+
+    sp = SplitsPtrs()
+    assert lib.a2av_dispatch(None, None, None, ctypes.byref(sp), None, None, None) == 1
+    assert lib.a2av_combine(None, None, None, None, None, None) == 1
+    assert lib.a2av_plan_destroy(None) == 0
+    assert lib.a2av_status_string(0) == b"ok"
+    assert lib.a2av_status_string(1) == b"invalid argument"
+
+
+def test_product_path_fails_loudly_without_library(tmp_path):
+    from combine_device_resident_gb300 import binding
+
+    with pytest.raises(binding.A2avError):
+        binding.load_library(str(tmp_path / "missing.so"))
+
+
+def test_product_package_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "combine_device_resident_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in re.sub(r"#.*|//.*", "", src).replace("the oracle", ""), f
