@@ -279,7 +279,9 @@ cudaError_t configure_pack(a2av_plan_s &p) {
     p.pack.block = 32;
     p.pack.smem = (size_t)stages * chunk + (size_t)stages * 8;
     p.pack.grid = p.num_sms * ctas_per_sm;
-    return cudaFuncSetAttribute(pack_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.pack.smem);
+    // The attribute is a per-kernel cap shared by every plan: raise it to the
+    // device maximum (never lower it to this plan's size).
+    return cudaFuncSetAttribute(pack_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
 }
 
 cudaError_t launch_pack(const a2av_plan_s &p, const PackArgs &a, cudaStream_t s) {

@@ -225,7 +225,12 @@ cudaError_t configure_hist(a2av_plan_s &p) {
     p.hist.block = kHistThreads;
     p.hist.smem = hist_smem_bytes(p.g);
     p.hist.grid = p.g.tiles;
-    return cudaFuncSetAttribute(hist_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.hist.smem);
+    // Per-kernel cap shared by every plan: the largest any valid plan needs.
+    Geometry worst{};
+    worst.R = kMaxRanks;
+    worst.E = kMaxExperts;
+    return cudaFuncSetAttribute(hist_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)hist_smem_bytes(worst));
 }
 
 cudaError_t launch_hist(const a2av_plan_s &p, const HistArgs &a, cudaStream_t s) {

@@ -196,3 +196,16 @@ def test_graph_replay_with_new_routing_each_time():
         seen_totals.add(tuple(ref["splits"]["recv_total"].tolist()))
     assert len(seen_totals) > 1
     assert plan.read_status() == 0
+
+
+def test_plans_with_different_shapes_coexist():
+    # Kernel attributes are per kernel, not per plan: a plan made later with a
+    # small row must not break an earlier plan with a large one.
+    big = W.WORKLOADS[5].scaled(T=200, H=7168)
+    small = _uniform(2, 4, 64, 8, 1)
+    xb = W.make_x(big, 0, device=P.device())
+    rgb = W.make_routing_gate(big, 0)
+    gbig = P.gpu_run(big, xb, rgb["topk_idx"], rgb["gate_w"])
+    P.full_parity(small)
+    P.full_parity(big, x=xb, idx=rgb["topk_idx"], gate=rgb["gate_w"])
+    P.gpu_run(big, xb, rgb["topk_idx"], rgb["gate_w"], plan=gbig["plan"])
