@@ -32,7 +32,7 @@ EXPORTED = [
     "a2av_config_check", "a2av_recv_arena_rows", "a2av_plan_create", "a2av_plan_destroy",
     "a2av_dispatch", "a2av_splits", "a2av_pack", "a2av_combine", "a2av_expert_scale",
     "a2av_read_device_status", "a2av_device_status_ptr", "a2av_plan_launches",
-    "a2av_status_string", "a2av_last_error",
+    "a2av_status_string", "a2av_last_error", "a2av_dispatch_static",
 ]
 
 
@@ -109,6 +109,8 @@ def load_library(path: Optional[str] = None):
     L.a2av_status_string.restype = ctypes.c_char_p
     L.a2av_last_error.argtypes = []
     L.a2av_last_error.restype = ctypes.c_char_p
+    L.a2av_dispatch_static.argtypes = [cfgp, vp, vp, spp, vp, vp, vp, vp]
+    L.a2av_dispatch_static.restype = i32
     if path is None:
         _lib = L
     return L
@@ -280,3 +282,30 @@ class Plan:
     @property
     def launches(self) -> int:
         return int(self.lib.a2av_plan_launches(self.handle))
+
+
+def dispatch_static(x, topk_idx, splits: Splits, recv, slot_map, dev_status, R, E, T, H, k,
+                    window_mode="packed", window_rows=0, flags=0, stream=None):
+    """Dispatch without a plan and without any allocation (a2av_dispatch_static).
+
+    For callers that cannot allocate device memory at the point of dispatch:
+    the kernels' scratch lives in a static device array of the library (1 MiB
+    per GPU), so shapes are bounded; ``dev_status`` is a caller-owned int32
+    device tensor of one element that receives the A2AV_DEV_* bits.  The first
+    call on a device does a one-time set-up, so make it before any graph
+    capture; calls that overlap on the GPU share the array and race.
+    """
+    import torch
+
+    L = load_library()
+    dev = x.device
+    cfg = make_config(R, E, T, H, k, window_mode, window_rows, dev.index, flags)
+    for t, dt, name in ((x, torch.bfloat16, "x"), (topk_idx, torch.int32, "topk_idx"), (recv, torch.bfloat16, "recv"),
+                        (slot_map, torch.int32, "slot_map"), (dev_status, torch.int32, "dev_status")):
+        if t.device != dev or t.dtype != dt or not t.is_contiguous():
+            raise A2avError(f"{name}: expected a contiguous {dt} tensor on {dev}")
+    rc = L.a2av_dispatch_static(ctypes.byref(cfg), ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(topk_idx.data_ptr()),
+                                ctypes.byref(splits.ptrs), ctypes.c_void_p(recv.data_ptr()),
+                                ctypes.c_void_p(slot_map.data_ptr()), ctypes.c_void_p(dev_status.data_ptr()),
+                                _stream_ptr(stream, dev))
+    _check(L, rc, "a2av_dispatch_static")

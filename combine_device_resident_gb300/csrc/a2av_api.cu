@@ -57,6 +57,10 @@ size_t tokens(const a2av_plan_s *p) { return (size_t)p->g.R * p->g.T; }
 
 }  // namespace
 
+namespace a2av {
+void set_last_error(const char *msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+}  // namespace a2av
+
 extern "C" {
 
 a2av_status_t a2av_config_check(const a2av_config_t *c) {

@@ -120,6 +120,9 @@ cudaError_t launch_pack(const a2av_plan_s &p, const PackArgs &a, cudaStream_t s)
 cudaError_t launch_combine(const a2av_plan_s &p, const CombineArgs &a, cudaStream_t s);
 cudaError_t launch_scale(const a2av_plan_s &p, const ScaleArgs &a, cudaStream_t s);
 
+// Records the text a2av_last_error() returns on the calling thread.
+void set_last_error(const char *msg);
+
 // Plan-time configuration of each kernel (attributes, occupancy, grid).
 cudaError_t configure_hist(a2av_plan_s &p);
 cudaError_t configure_pack(a2av_plan_s &p);

@@ -1,0 +1,158 @@
+// Dispatch without any allocation: a2av_dispatch_static.
+//
+// Some callers cannot call cudaMalloc: code that runs while a CUDA graph is
+// being captured in a mode that forbids allocation, code inside a framework
+// whose caching allocator owns all device memory and must not be bypassed,
+// or processes with a fixed device-memory budget that is exhausted by the
+// time this library runs.  For them this entry point keeps its scratch (the
+// per-tile histogram bases, the per-(source, expert) window bases and the
+// completion counters the splits kernel needs) in one file-scope __device__
+// array, so the only device memory it touches besides the caller's buffers
+// is memory the library already owns from the moment it is loaded.
+//
+// The same splits and pack kernels as a2av_dispatch run; only where their
+// scratch lives differs.  The array is shared by every call in the process,
+// and every GPU that loads the library holds a copy of it until the process
+// exits.
+#include <stdio.h>
+
+#include <mutex>
+
+#include "a2av_internal.cuh"
+
+namespace {
+
+// 1 MiB of scratch per GPU (262144 int32).  Enough for, e.g., R=32 ranks,
+// E=256 experts and 16384 assignments per rank (about 74k entries).
+constexpr size_t kStaticScratchInts = 262144;
+static __device__ __align__(256) int32_t g_dispatch_scratch[kStaticScratchInts];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+int32_t *g_scratch_addr[kMaxDevices];  // device address of the array, per device
+
+size_t round64(size_t n) { return (n + 63) / 64 * 64; }
+
+// Address of the array on `dev`, looked up once per device with `dev` current.
+cudaError_t scratch_on(int dev, int32_t **out) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (!g_scratch_addr[dev]) {
+        void *ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_dispatch_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = static_cast<int32_t *>(ptr);
+    }
+    *out = g_scratch_addr[dev];
+    return cudaSuccess;
+}
+
+bool aligned(const void *p, size_t a) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" a2av_status_t a2av_dispatch_static(const a2av_config_t *cfg, const void *x, const int32_t *topk_idx,
+                                              const a2av_splits_t *splits, void *recv, int32_t *slot_map,
+                                              uint32_t *dev_status, void *stream) {
+    if (a2av_config_check(cfg) != A2AV_OK) {
+        a2av::set_last_error("a2av_dispatch_static: invalid configuration");
+        return A2AV_ERR_INVALID_ARG;
+    }
+    if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(topk_idx, 4) || !aligned(slot_map, 4) ||
+        !aligned(dev_status, 4) || !splits || !aligned(splits->send_counts, 4) || !aligned(splits->send_offsets, 4) ||
+        !aligned(splits->recv_counts, 4) || !aligned(splits->recv_offsets, 4) ||
+        !aligned(splits->recv_expert_counts, 4) || !aligned(splits->recv_total, 4) ||
+        !aligned(splits->window_base, 4)) {
+        a2av::set_last_error("a2av_dispatch_static: null or misaligned pointer");
+        return A2AV_ERR_INVALID_ARG;
+    }
+
+    a2av_plan_s p;  // host-side description only; nothing is allocated
+    p.cfg = *cfg;
+    a2av::Geometry &g = p.g;
+    g.R = cfg->num_ranks;
+    g.E = cfg->num_experts;
+    g.T = cfg->tokens_per_rank;
+    g.H = cfg->hidden;
+    g.k = cfg->topk;
+    g.epr = g.E / g.R;
+    g.tiles = (int32_t)(((long long)g.T * g.k + a2av::kHistTile - 1) / a2av::kHistTile);
+    g.window_mode = cfg->window_mode;
+    g.window_rows = cfg->window_mode == A2AV_WINDOW_FIXED ? cfg->window_rows : 0;
+    p.pack_tma = (cfg->flags & A2AV_FLAG_PACK_LSU) ? 0 : 1;
+
+    const size_t row_bytes = (size_t)g.H * 2;
+    const size_t x_bytes = (size_t)g.R * g.T * row_bytes;
+    const size_t recv_bytes = (size_t)a2av_recv_arena_rows(cfg) * row_bytes;
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x), ra = reinterpret_cast<uintptr_t>(recv);
+    if (xa < ra + recv_bytes && ra < xa + x_bytes) {
+        a2av::set_last_error("a2av_dispatch_static: recv overlaps x");
+        return A2AV_ERR_INVALID_ARG;
+    }
+
+    const size_t n_tile = round64((size_t)g.R * g.tiles * g.E);
+    const size_t n_dest = round64((size_t)g.R * g.E);
+    const size_t n_cnt = round64((size_t)g.R + 1);
+    if (n_tile + n_dest + n_cnt > kStaticScratchInts) {
+        char msg[256];
+        snprintf(msg, sizeof msg,
+                 "a2av_dispatch_static: this shape needs %zu int32 of scratch, the static array holds %zu "
+                 "(use a plan and a2av_dispatch instead)",
+                 n_tile + n_dest + n_cnt, kStaticScratchInts);
+        a2av::set_last_error(msg);
+        return A2AV_ERR_INVALID_ARG;
+    }
+
+    int prev = -1;
+    cudaError_t e = cudaGetDevice(&prev);
+    if (e == cudaSuccess && prev != cfg->device) e = cudaSetDevice(cfg->device);
+    int32_t *scratch = nullptr;
+    if (e == cudaSuccess) e = scratch_on(cfg->device, &scratch);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p.num_sms, cudaDevAttrMultiProcessorCount, cfg->device);
+    if (e == cudaSuccess) {
+        p.tile_base = scratch;
+        p.dest_base = scratch + n_tile;
+        p.counters = reinterpret_cast<uint32_t *>(scratch + n_tile + n_dest);
+        p.status = dev_status;
+        e = a2av::configure_hist(p);
+    }
+    if (e == cudaSuccess) e = a2av::configure_pack(p);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // The completion counters must start at zero; the previous call leaves them
+    // at zero, but clear them anyway so that nothing depends on earlier calls.
+    if (e == cudaSuccess) e = cudaMemsetAsync(p.counters, 0, ((size_t)g.R + 1) * sizeof(uint32_t), s);
+    if (e == cudaSuccess) {
+        a2av::HistArgs h;
+        h.g = g;
+        h.idx = topk_idx;
+        h.slot_map = slot_map;
+        h.tile_base = p.tile_base;
+        h.dest_base = p.dest_base;
+        h.counters = p.counters;
+        h.status = dev_status;
+        h.sp = a2av::Splits{splits->send_counts, splits->send_offsets, splits->recv_counts, splits->recv_offsets,
+                            splits->recv_expert_counts, splits->recv_total, splits->window_base};
+        e = a2av::launch_hist(p, h, s);
+    }
+    if (e == cudaSuccess) {
+        a2av::PackArgs a{};
+        a.g = g;
+        a.x = static_cast<const uint16_t *>(x);
+        a.idx = topk_idx;
+        a.slot_map = slot_map;
+        a.tile_base = p.tile_base;
+        a.dest_base = p.dest_base;
+        a.window_base = splits->window_base;
+        a.recv = static_cast<uint16_t *>(recv);
+        a.status = dev_status;
+        e = a2av::launch_pack(p, a, s);
+    }
+    if (prev >= 0 && prev != cfg->device) cudaSetDevice(prev);
+    if (e != cudaSuccess) {
+        char msg[256];
+        snprintf(msg, sizeof msg, "a2av_dispatch_static: %s (%s)", cudaGetErrorName(e), cudaGetErrorString(e));
+        a2av::set_last_error(msg);
+        return A2AV_ERR_CUDA;
+    }
+    return A2AV_OK;
+}

@@ -187,6 +187,28 @@ a2av_status_t a2av_combine(a2av_plan_t plan, const void *y, const float *gate_w,
 a2av_status_t a2av_expert_scale(a2av_plan_t plan, const void *recv, const int32_t *topk_idx,
                                 const int32_t *slot_map, void *y, void *stream);
 
+/* Dispatch that allocates nothing (no plan, no cudaMalloc, no allocating
+ * library call).  The paper has no counterpart; it exists for callers that
+ * cannot allocate device memory where they dispatch -- for example code that
+ * runs while a graph is captured in a mode that forbids allocation, or inside
+ * a framework whose allocator owns all device memory.  Same inputs, outputs
+ * and results as a2av_dispatch on a plan made from `cfg`; the scratch the
+ * splits and pack kernels need lives in one static device array of the
+ * library (1 MiB per GPU that loads the library, held until process exit),
+ * which bounds the shapes it accepts: R*ceil(T*k/2048)*E + R*E + R + 1 int32
+ * (each term rounded up to 64) must fit in 262144, else A2AV_ERR_INVALID_ARG
+ * with the sizes in a2av_last_error().  `dev_status` is a caller-owned device
+ * uint32 that the kernels OR the A2AV_DEV_* bits into (the caller clears it).
+ * The first call on each device looks up the array's device address (a
+ * synchronous runtime call), so make that first call before any stream
+ * capture.  Every call uses the same array and leaves its last contents there
+ * (the counters that must start at zero are cleared on the stream by each
+ * call): calls that overlap on the GPU -- on different streams, or from
+ * different threads without ordering -- race on it. */
+a2av_status_t a2av_dispatch_static(const a2av_config_t *cfg, const void *x, const int32_t *topk_idx,
+                                   const a2av_splits_t *splits, void *recv, int32_t *slot_map,
+                                   uint32_t *dev_status, void *stream);
+
 /* Copy the device status word to *bits (synchronises `stream`); if `clear`,
  * reset it to 0 afterwards.  Not capturable. */
 a2av_status_t a2av_read_device_status(a2av_plan_t plan, uint32_t *bits, int clear, void *stream);

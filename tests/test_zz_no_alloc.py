@@ -1,0 +1,89 @@
+"""a2av_dispatch_static: the dispatch for callers that cannot allocate device
+memory where they dispatch (for instance while a graph is captured in a mode
+that forbids allocation, or inside a framework whose allocator owns all device
+memory).  It keeps its kernels' scratch in a static device array of the
+library instead of a plan's workspace.
+
+Checked through the C ABI against the plan-based a2av_dispatch on the same
+inputs, on two calls in a row with different routings (so contents the first
+call leaves in the shared array cannot leak into the second): splits, offsets,
+slot_map and every dispatched recv row bit-exact, as the integer/byte work of
+dispatch is everywhere in these tests.  This file is collected last on
+purpose; it also passes when run alone in a fresh process.
+"""
+import pytest
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _plan_dispatch(w, x, idx_t):
+    import combine_device_resident_gb300 as A
+
+    plan = A.Plan(w.R, w.E, w.T, w.H, w.k, w.window_mode, w.window_rows, device=x.device)
+    recv, slot_map, _ = plan.new_buffers()
+    recv.zero_()
+    sp = plan.new_splits()
+    plan.dispatch(x, idx_t, sp, recv, slot_map)
+    return plan, sp, recv, slot_map
+
+
+def _static_dispatch(w, x, idx_t):
+    import torch
+
+    import combine_device_resident_gb300 as A
+    from combine_device_resident_gb300.binding import dispatch_static
+
+    dev = x.device
+    sp = A.Splits(w.R, w.E, dev)
+    arena = w.R * w.T * w.k if w.window_mode == "packed" else w.R * w.window_rows
+    recv = torch.zeros((arena, w.H), dtype=torch.bfloat16, device=dev)
+    slot_map = torch.full((w.R, w.T, w.k), -5, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    dispatch_static(x, idx_t, sp, recv, slot_map, status, w.R, w.E, w.T, w.H, w.k, w.window_mode, w.window_rows)
+    return sp, recv, slot_map, status
+
+
+@pytest.mark.parametrize("wid,T,H", [(5, 700, 264), (3, 900, 136), (4, 3000, 72)])
+def test_static_dispatch_matches_plan_dispatch_on_two_calls(wid, T, H):
+    import torch
+
+    dev = torch.device("cuda", 0)
+    w = W.WORKLOADS[wid].scaled(T=T, H=H)
+    x = W.make_x(w, 0, device=dev)
+    for seed in (11, 12):
+        idx_t = torch.from_numpy(W.make_routing_gate(w, seed)["topk_idx"]).to(dev)
+        plan, sp_ref, recv_ref, sm_ref = _plan_dispatch(w, x, idx_t)
+        sp, recv, sm, status = _static_dispatch(w, x, idx_t)
+        torch.cuda.synchronize()
+        for name in sp.NAMES:
+            assert torch.equal(getattr(sp, name), getattr(sp_ref, name)), name
+        assert torch.equal(sm, sm_ref)
+        rows = sm_ref.flatten()
+        rows = rows[rows >= 0].long()
+        assert torch.equal(recv.index_select(0, rows).view(torch.int16),
+                           recv_ref.index_select(0, rows).view(torch.int16))
+        assert int(status.item()) == 0 and plan.read_status() == 0
+        plan.close()
+
+
+def test_static_dispatch_rejects_shapes_beyond_its_scratch():
+    import torch
+
+    import combine_device_resident_gb300 as A
+    from combine_device_resident_gb300.binding import dispatch_static
+
+    dev = torch.device("cuda", 0)
+    # 64 ranks x 2048 experts x 2 tiles needs far more than 262144 int32
+    R, E, T, H, k = 64, 2048, 600, 8, 4
+    x = torch.zeros((R, T, H), dtype=torch.bfloat16, device=dev)
+    idx = torch.zeros((R, T, k), dtype=torch.int32, device=dev)
+    sp = A.Splits(R, E, dev)
+    recv = torch.zeros((R * T * k, H), dtype=torch.bfloat16, device=dev)
+    sm = torch.zeros((R, T, k), dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    with pytest.raises(A.A2avError, match="scratch"):
+        dispatch_static(x, idx, sp, recv, sm, status, R, E, T, H, k)
+    torch.cuda.synchronize()
+    assert int(sp.recv_total.sum().item()) == 0  # nothing was enqueued
