@@ -15,6 +15,8 @@ from .binding import (  # noqa: F401
     DEV_WINDOW_OVERFLOW,
     EXPORTED,
     FLAG_PACK_LSU,
+    FLAG_SPLITS_TILED,
+    FLAG_COMBINE_TMA,
     Plan,
     Splits,
     load_library,

@@ -26,6 +26,8 @@ DEV_WAIT_TIMEOUT = 1 << 31
 WINDOW_PACKED = 0
 WINDOW_FIXED = 1
 FLAG_PACK_LSU = 1 << 0
+FLAG_SPLITS_TILED = 1 << 1
+FLAG_COMBINE_TMA = 1 << 2
 
 # Every function the header declares, for load checks.
 EXPORTED = [
@@ -49,6 +51,9 @@ class Config(ctypes.Structure):
         ("flags", ctypes.c_uint32),
         ("pack_ctas_per_sm", ctypes.c_int32),
         ("pack_stage_bytes", ctypes.c_int32),
+        ("pack_store_lag", ctypes.c_int32),
+        ("combine_ctas_per_sm", ctypes.c_int32),
+        ("combine_stage_bytes", ctypes.c_int32),
     ]
 
 
@@ -124,10 +129,12 @@ def _check(L, rc: int, what: str):
 
 
 def make_config(R, E, T, H, k, window_mode="packed", window_rows=0, device=0, flags=0,
-                pack_ctas_per_sm=0, pack_stage_bytes=0) -> Config:
+                pack_ctas_per_sm=0, pack_stage_bytes=0, pack_store_lag=0, combine_ctas_per_sm=0,
+                combine_stage_bytes=0) -> Config:
     mode = {"packed": WINDOW_PACKED, "fixed": WINDOW_FIXED}.get(window_mode, window_mode)
     return Config(int(R), int(E), int(T), int(H), int(k), int(mode), int(window_rows), int(device),
-                  int(flags), int(pack_ctas_per_sm), int(pack_stage_bytes))
+                  int(flags), int(pack_ctas_per_sm), int(pack_stage_bytes), int(pack_store_lag),
+                  int(combine_ctas_per_sm), int(combine_stage_bytes))
 
 
 class Splits:
@@ -167,7 +174,8 @@ class Plan:
     hidden H, top-k.  Owns only the library's small workspace."""
 
     def __init__(self, R, E, T, H, k, window_mode="packed", window_rows=0, device=None, flags=0,
-                 pack_ctas_per_sm=0, pack_stage_bytes=0):
+                 pack_ctas_per_sm=0, pack_stage_bytes=0, pack_store_lag=0, combine_ctas_per_sm=0,
+                 combine_stage_bytes=0):
         import torch
 
         self.lib = load_library()
@@ -179,7 +187,8 @@ class Plan:
         self.window_mode = window_mode
         self.window_rows = int(window_rows)
         self.cfg = make_config(R, E, T, H, k, window_mode, window_rows, dev.index, flags,
-                               pack_ctas_per_sm, pack_stage_bytes)
+                               pack_ctas_per_sm, pack_stage_bytes, pack_store_lag, combine_ctas_per_sm,
+                               combine_stage_bytes)
         handle = ctypes.c_void_p()
         _check(self.lib, self.lib.a2av_plan_create(ctypes.byref(self.cfg), ctypes.byref(handle)), "a2av_plan_create")
         self.handle = handle

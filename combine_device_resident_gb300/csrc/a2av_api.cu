@@ -80,7 +80,12 @@ a2av_status_t a2av_config_check(const a2av_config_t *c) {
         return A2AV_ERR_INVALID_ARG;
     }
     if (c->device < 0) return A2AV_ERR_INVALID_ARG;
-    if (c->flags & ~(uint32_t)A2AV_FLAG_PACK_LSU) return A2AV_ERR_INVALID_ARG;
+    if (c->flags & ~(uint32_t)(A2AV_FLAG_PACK_LSU | A2AV_FLAG_SPLITS_TILED | A2AV_FLAG_COMBINE_TMA))
+        return A2AV_ERR_INVALID_ARG;
+    if (c->pack_store_lag < 0 || c->pack_store_lag > 8) return A2AV_ERR_INVALID_ARG;
+    if (c->combine_ctas_per_sm < 0 || c->combine_ctas_per_sm > 8) return A2AV_ERR_INVALID_ARG;
+    if (c->combine_stage_bytes < 0 || c->combine_stage_bytes % 16 != 0 || c->combine_stage_bytes > 131072)
+        return A2AV_ERR_INVALID_ARG;
     if (c->pack_ctas_per_sm < 0 || c->pack_ctas_per_sm > 4) return A2AV_ERR_INVALID_ARG;
     if (c->pack_stage_bytes < 0 || c->pack_stage_bytes % 16 != 0 || c->pack_stage_bytes > 65536)
         return A2AV_ERR_INVALID_ARG;
@@ -114,6 +119,8 @@ a2av_status_t a2av_plan_create(const a2av_config_t *cfg, a2av_plan_t *out_plan) 
     g.H = cfg->hidden;
     g.k = cfg->topk;
     g.epr = g.E / g.R;
+    g.key_bits = 1;
+    while ((1 << g.key_bits) <= g.E) ++g.key_bits;
     g.tiles = (int32_t)(((long long)g.T * g.k + a2av::kHistTile - 1) / a2av::kHistTile);
     g.window_mode = cfg->window_mode;
     g.window_rows = cfg->window_mode == A2AV_WINDOW_FIXED ? cfg->window_rows : 0;

@@ -31,6 +31,7 @@ struct Splits {
 // Geometry every kernel needs.
 struct Geometry {
     int32_t R, E, T, H, k, epr;
+    int32_t key_bits;     // bits of an expert key in [0, E] (E marks a dropped id)
     int32_t tiles;        // histogram tiles per rank
     int32_t window_mode;  // 0 packed, 1 fixed
     int64_t window_rows;
@@ -61,6 +62,8 @@ struct PackArgs {
     int32_t chunk_bytes;  // bytes per stage buffer (multiple of 16)
     int32_t nchunks;      // chunks per row
     int32_t stages;
+    int32_t rows_final;   // 1: slot_map already holds final rows (single-CTA splits)
+    int32_t lag;          // store groups allowed to read a stage before it is refilled
 };
 
 struct CombineArgs {
@@ -71,6 +74,11 @@ struct CombineArgs {
     uint16_t *out;
     int64_t arena_rows;  // rows of y; a slot outside [0, arena_rows) is skipped and flagged
     uint32_t *status;
+    // TMA variant
+    int32_t chunk_bytes;  // bytes of a row per stage slot (multiple of 16)
+    int32_t nchunks;      // chunks per row
+    int32_t stages;
+    int32_t nsplit;       // LSU variant: pieces per row
 };
 
 struct ScaleArgs {
@@ -107,12 +115,32 @@ struct a2av_plan_s {
     uint32_t *counters = nullptr;
     uint32_t *status = nullptr;
     a2av::LaunchShape hist, pack, combine, scale;
+    int splits_small = 0;  // 1: one-CTA splits kernel that writes final rows
+    int combine_tma = 1;
+    int32_t comb_chunk_bytes = 0, comb_nchunks = 0, comb_stages = 0, comb_nsplit = 1;
     int pack_tma = 1;
-    int32_t pack_chunk_bytes = 0, pack_nchunks = 0, pack_stages = 0;
+    int32_t pack_chunk_bytes = 0, pack_nchunks = 0, pack_stages = 0, pack_lag = 1;
     int64_t launches = 0;
 };
 
 namespace a2av {
+
+// Launch with the programmatic stream-serialization attribute (the kernel
+// calls grid_dependency_wait() before reading its predecessor's output).
+template <typename Kernel, typename Args>
+cudaError_t launch_pdl(Kernel kernel, int grid, int block, size_t smem, cudaStream_t s, const Args &args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args);
+}
 
 // Launchers (return the cudaGetLastError() after the launch).
 cudaError_t launch_hist(const a2av_plan_s &p, const HistArgs &a, cudaStream_t s);
@@ -151,9 +179,105 @@ __device__ __forceinline__ void st_v4(void *p, const uint4 &v) {
                  : "memory");
 }
 
+// Lanes of the warp whose `key` equals this lane's, for keys in [0, 2^nbits):
+// one ballot per key bit (a warp multisplit), all of them full-rate
+// instructions.
+__device__ __forceinline__ uint32_t peers_by_ballot(uint32_t key, int nbits) {
+    uint32_t peers = 0xffffffffu;
+    for (int b = 0; b < nbits; ++b) {
+        const uint32_t bit = (key >> b) & 1u;
+        const uint32_t set = __ballot_sync(0xffffffffu, bit);
+        peers &= bit ? set : ~set;
+    }
+    return peers;
+}
+
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while its predecessor runs; it
+// must wait here before touching anything the predecessor writes.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the dependent grid begin launching (its wait still covers our writes).
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void st_stream_v4(void *p, const uint4 &v) {
     asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
 }
+
+// ---------------------------------------------------------------------------
+// mbarrier + bulk-copy (TMA) helpers.  Every wait is bounded: a kernel that
+// gives up sets a status bit and returns instead of hanging the GPU.
+// ---------------------------------------------------------------------------
+constexpr long long kWaitLimit = 1ll << 22;  // bounded spin on our own copies
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    for (long long it = 0; it < kWaitLimit; ++it)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst_smem)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_store(void *dst, const void *src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src_smem)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until at most `n` of this thread's newest bulk groups still read smem.
+__device__ __forceinline__ void bulk_wait_read_upto(int n) {
+    switch (n) {
+        case 0: bulk_wait_read<0>(); break;
+        case 1: bulk_wait_read<1>(); break;
+        case 2: bulk_wait_read<2>(); break;
+        case 3: bulk_wait_read<3>(); break;
+        case 4: bulk_wait_read<4>(); break;
+        case 5: bulk_wait_read<5>(); break;
+        case 6: bulk_wait_read<6>(); break;
+        default: bulk_wait_read<7>(); break;
+    }
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 
 }  // namespace a2av

@@ -6,9 +6,13 @@
 // result does not depend on the launch shape.  NCCLX pages: qiguanping deep
 // dive section 7, Figure 13 (the dispatch shuffle and the combine).
 //
-// Warp per token; 16-byte vector gathers.  The kernel is instantiated for
-// k in {1, 2, 4, 8} so that all k*U loads of a step are in flight before the
-// ordered accumulation; other k use the generic loop.
+// Work unit = one of `nsplit` pieces of one token's row (nsplit is chosen so
+// that there are several units per warp: whole rows for many tokens, pieces
+// for few), taken by the warps in a token-major grid stride, with 16-byte
+// vector gathers of 32*U vectors per step.  The kernel is
+// instantiated for k in {1, 2, 4, 8} so that all k*U loads of a unit are in
+// flight before the ordered accumulation; other k use the generic loop.
+// Launched as a programmatic dependent of the pack kernel.
 //
 // Also here: the expert stand-in of the checkable workload,
 // y = bf16_rne(recv * (1 + e/E)), and its launcher.
@@ -57,75 +61,226 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
     const int k = KT > 0 ? KT : g.k;
     const int lane = threadIdx.x & 31;
     const long long ntok = (long long)g.R * g.T;
-    const int nv = g.H >> 3;
-    const size_t rowb = (size_t)g.H * 2;
+    const int nv = g.H >> 3;               // 16-byte vectors per row
+    const int step = 32 * U;               // vectors per inner step
+    const int nsplit = a.nsplit;           // pieces per row (1 = whole-row units)
+    const int steps_per_row = (nv + step - 1) / step;
+    const int steps_per_unit = (steps_per_row + nsplit - 1) / nsplit;
+    const long long units = ntok * nsplit;
     const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+    const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const size_t rowb = (size_t)g.H * 2;
     const char *y = reinterpret_cast<const char *>(a.y);
     bool bad_slot = false;
-    for (long long u = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < ntok; u += nw) {
-        int32_t row = -1;
-        float w = 0.f;
-        if (lane < k) {
-            row = __ldg(a.slot_map + (size_t)u * k + lane);
-            w = __ldg(a.gate + (size_t)u * k + lane);
-            if (row >= a.arena_rows) {
-                bad_slot = true;
-                row = -1;
+    grid_dependency_wait();  // slot_map and y come from the kernels before
+    long long cur = -1;
+    int32_t row = -1;
+    float w = 0.f;
+    // token-major grid stride: the warps active at one time cover a compact
+    // stretch of `out` (and of each token's gathered rows)
+    for (long long un = gw; un < units; un += nw) {
+        const long long u = un / nsplit;
+        const int piece = (int)(un - u * nsplit);
+        if (u != cur) {
+            cur = u;
+            row = -1;
+            w = 0.f;
+            if (lane < k) {
+                row = __ldg(a.slot_map + (size_t)u * k + lane);
+                w = __ldg(a.gate + (size_t)u * k + lane);
+                if (row >= a.arena_rows) {
+                    bad_slot = true;
+                    row = -1;
+                }
             }
         }
         char *dst = reinterpret_cast<char *>(a.out) + (size_t)u * rowb;
-        for (int vb = 0; vb < nv; vb += 32 * U) {
-            float acc[U][8];
+        const int vb_end = min(nv, (piece + 1) * steps_per_unit * step);
+        for (int vb = piece * steps_per_unit * step; vb < vb_end; vb += step) {
+        float acc[U][8];
 #pragma unroll
-            for (int q = 0; q < U; ++q)
+        for (int q = 0; q < U; ++q)
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[q][i] = 0.f;
-            if constexpr (KT > 0) {
-                uint4 buf[KT][U];
-                int32_t rows[KT];
+            for (int i = 0; i < 8; ++i) acc[q][i] = 0.f;
+        if constexpr (KT > 0) {
+            uint4 buf[KT][U];
+            int32_t rows[KT];
 #pragma unroll
-                for (int j = 0; j < KT; ++j)
+            for (int j = 0; j < KT; ++j) {
+                rows[j] = __shfl_sync(kFull, row, j);
 #pragma unroll
-                    for (int q = 0; q < U; ++q) buf[j][q] = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                for (int j = 0; j < KT; ++j) {
-                    rows[j] = __shfl_sync(kFull, row, j);
-#pragma unroll
-                    for (int q = 0; q < U; ++q) {
-                        const int v = vb + q * 32 + lane;
-                        if (rows[j] >= 0 && v < nv) buf[j][q] = ld_stream_v4(y + (size_t)rows[j] * rowb + (size_t)v * 16);
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < KT; ++j) {
-                    const float wj = __shfl_sync(kFull, w, j);
-                    if (rows[j] < 0) continue;
-#pragma unroll
-                    for (int q = 0; q < U; ++q) accumulate(acc[q], buf[j][q], wj);
-                }
-            } else {
-                for (int j = 0; j < k; ++j) {
-                    const int32_t rj = __shfl_sync(kFull, row, j);
-                    const float wj = __shfl_sync(kFull, w, j);
-                    if (rj < 0) continue;
-                    uint4 buf[U];
-#pragma unroll
-                    for (int q = 0; q < U; ++q) {
-                        const int v = vb + q * 32 + lane;
-                        buf[q] = make_uint4(0u, 0u, 0u, 0u);
-                        if (v < nv) buf[q] = ld_stream_v4(y + (size_t)rj * rowb + (size_t)v * 16);
-                    }
-#pragma unroll
-                    for (int q = 0; q < U; ++q) accumulate(acc[q], buf[q], wj);
+                for (int q = 0; q < U; ++q) {
+                    const int v = vb + q * 32 + lane;
+                    buf[j][q] = make_uint4(0u, 0u, 0u, 0u);
+                    if (rows[j] >= 0 && v < vb_end) buf[j][q] = ld_stream_v4(y + (size_t)rows[j] * rowb + (size_t)v * 16);
                 }
             }
 #pragma unroll
-            for (int q = 0; q < U; ++q) {
-                const int v = vb + q * 32 + lane;
-                if (v < nv) st_stream_v4(dst + (size_t)v * 16, to_bf16x8(acc[q]));
+            for (int j = 0; j < KT; ++j) {
+                const float wj = __shfl_sync(kFull, w, j);
+                if (rows[j] < 0) continue;
+#pragma unroll
+                for (int q = 0; q < U; ++q) accumulate(acc[q], buf[j][q], wj);
+            }
+        } else {
+            for (int j = 0; j < k; ++j) {
+                const int32_t rj = __shfl_sync(kFull, row, j);
+                const float wj = __shfl_sync(kFull, w, j);
+                if (rj < 0) continue;
+                uint4 buf[U];
+#pragma unroll
+                for (int q = 0; q < U; ++q) {
+                    const int v = vb + q * 32 + lane;
+                    buf[q] = make_uint4(0u, 0u, 0u, 0u);
+                    if (v < vb_end) buf[q] = ld_stream_v4(y + (size_t)rj * rowb + (size_t)v * 16);
+                }
+#pragma unroll
+                for (int q = 0; q < U; ++q) accumulate(acc[q], buf[q], wj);
             }
         }
+#pragma unroll
+        for (int q = 0; q < U; ++q) {
+            const int v = vb + q * 32 + lane;
+            if (v < vb_end) st_stream_v4(dst + (size_t)v * 16, to_bf16x8(acc[q]));
+        }
+        }
     }
+    if (__any_sync(kFull, bad_slot) && lane == 0) atomicOr(a.status, kDevBadSlot);
+}
+
+// ---------------------------------------------------------------------------
+// TMA combine (opt-in variant; the vector-gather kernel above is the default
+// because the combine is bound by its per-element fp32 work, which needs many
+// warps per SM, not by bytes in flight).  Persistent grid of single-warp
+// CTAs, several per SM; each CTA
+// owns a contiguous range of tokens, split into work units (token, chunk of
+// the row).  For every unit the warp's lane j issues a cp.async.bulk of slot
+// j's row chunk into the unit's shared-memory stage (completion on the
+// stage's mbarrier) and records the slot mask and gate weights beside it; up
+// to `stages` units are in flight.  The same warp then accumulates each unit
+// from shared memory in slot order (fp32, products and sums rounded
+// separately), streams the bf16 result to `out`, and refills the stage.
+// ---------------------------------------------------------------------------
+struct StageMeta {
+    uint32_t mask;  // bit j: slot j has a row in this stage
+    uint32_t pad[3];
+    float w[kMaxTopk];
+};
+
+__global__ void __launch_bounds__(32, 1) combine_tma_kernel(const CombineArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const Geometry &g = a.g;
+    const int k = g.k;
+    const int lane = threadIdx.x;
+    const int NS = a.stages, CH = a.chunk_bytes, nch = a.nchunks;
+    const size_t stage_bytes = (size_t)k * CH;
+    StageMeta *meta = reinterpret_cast<StageMeta *>(smem + (size_t)NS * stage_bytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(meta + NS);
+
+    const long long ntok = (long long)g.R * g.T;
+    const long long per = (ntok + gridDim.x - 1) / gridDim.x;
+    const long long tb = min(ntok, (long long)blockIdx.x * per);
+    const long long te = min(ntok, tb + per);
+    if (tb >= te) return;
+    const long long n = (te - tb) * nch;
+    const size_t rowb = (size_t)g.H * 2;
+    const char *y = reinterpret_cast<const char *>(a.y);
+    char *outp = reinterpret_cast<char *>(a.out);
+
+    if (lane == 0) {
+        for (int i = 0; i < NS; ++i) mbar_init(&full[i], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    grid_dependency_wait();  // slot_map and y come from the kernels before
+
+    // issue side: slots and weights of a batch of BT tokens, one per lane
+    const int BT = max(1, 32 / k);
+    const int my_b = lane / k, my_j = lane - my_b * k;
+    bool bad_slot = false;
+    auto load_batch = [&](long long tok0, int32_t &row, float &w) {
+        const long long tok = tok0 + my_b;
+        row = -1;
+        w = 0.f;
+        if (my_b < BT && tok < te) {
+            row = __ldg(a.slot_map + (size_t)tok * k + my_j);
+            w = __ldg(a.gate + (size_t)tok * k + my_j);
+        }
+    };
+    long long ib0 = tb;  // first token of the issue-side batch
+    int32_t cur_row, nxt_row;
+    float cur_w, nxt_w;
+    load_batch(ib0, cur_row, cur_w);
+    load_batch(ib0 + BT, nxt_row, nxt_w);
+
+    auto issue = [&](long long p) {
+        const long long tok = tb + p / nch;
+        if (tok >= ib0 + BT) {  // advance the issue-side batch (tokens only move forward)
+            ib0 += BT;
+            cur_row = nxt_row;
+            cur_w = nxt_w;
+            load_batch(ib0 + BT, nxt_row, nxt_w);
+        }
+        const int st = (int)(p % NS);
+        const uint32_t off = (uint32_t)(p % nch) * CH;
+        const uint32_t bytes = (uint32_t)min((size_t)CH, rowb - off);
+        const int src = ((int)(tok - ib0) * k + (lane % k)) & 31;
+        const int32_t r = __shfl_sync(kFull, cur_row, src);
+        const float w = __shfl_sync(kFull, cur_w, src);
+        const bool in_arena = r >= 0 && r < a.arena_rows;
+        bad_slot |= lane < k && r >= a.arena_rows;
+        const uint32_t mask = __ballot_sync(kFull, lane < k && in_arena);
+        if (lane < k) meta[st].w[lane] = w;
+        if (lane == 0) meta[st].mask = mask;
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)__popc(mask) * bytes);
+        __syncwarp();
+        if (lane < k && in_arena)
+            bulk_load(smem + (size_t)st * stage_bytes + (size_t)lane * CH, y + (size_t)r * rowb + off, bytes,
+                      &full[st]);
+    };
+
+    const long long pre = min(n, (long long)NS);
+    for (long long p = 0; p < pre; ++p) issue(p);
+    long long issued = pre;
+    bool timed_out = false;
+    for (long long i = 0; i < n; ++i) {
+        const int st = (int)(i % NS);
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait_bounded(&full[st], (uint32_t)((i / NS) & 1));
+        ok = __shfl_sync(kFull, ok, 0);
+        if (!ok) {
+            timed_out = true;
+            // let every copy this CTA issued land before leaving (bounded)
+            if (lane == 0)
+                for (long long p = i + 1; p < issued; ++p) mbar_wait_bounded(&full[p % NS], (uint32_t)((p / NS) & 1));
+            break;
+        }
+        const long long tok = tb + i / nch;
+        const uint32_t off = (uint32_t)(i % nch) * CH;
+        const int nvec = (int)(min((size_t)CH, rowb - off) >> 4);
+        const uint32_t mask = meta[st].mask;
+        const unsigned char *stage = smem + (size_t)st * stage_bytes;
+        char *dst = outp + (size_t)tok * rowb + off;
+        for (int v = lane; v < nvec; v += 32) {
+            float acc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+            for (int j = 0; j < k; ++j) {
+                if (!((mask >> j) & 1u)) continue;
+                const uint4 val = *reinterpret_cast<const uint4 *>(stage + (size_t)j * CH + (size_t)v * 16);
+                accumulate(acc, val, meta[st].w[j]);
+            }
+            st_stream_v4(dst + (size_t)v * 16, to_bf16x8(acc));
+        }
+        __syncwarp();
+        if (i + NS < n) {
+            fence_proxy_async_smem();  // our generic reads of the stage precede the async refill
+            issue(i + NS);
+            issued = i + NS + 1;
+        }
+    }
+    if (lane == 0 && timed_out) atomicOr(a.status, kDevWaitTimeout);
     if (__any_sync(kFull, bad_slot) && lane == 0) atomicOr(a.status, kDevBadSlot);
 }
 
@@ -162,19 +317,68 @@ __global__ void __launch_bounds__(256) expert_scale_kernel(const ScaleArgs a) {
 }
 
 template <int KT, int U>
-cudaError_t occupancy_grid(const a2av_plan_s &p, int &grid) {
+cudaError_t occupancy_grid(a2av_plan_s &p, int &grid) {
     int per_sm = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<KT, U>, 256, 0);
     grid = p.num_sms * (per_sm > 0 ? per_sm : 1);
+    // split rows so that every warp gets at least ~4 units
+    const long long warps = (long long)grid * 8;
+    const long long ntok = (long long)p.g.R * p.g.T;
+    const int steps_per_row = ((p.g.H >> 3) + 32 * U - 1) / (32 * U);
+    long long ns = (4 * warps + ntok - 1) / ntok;
+    if (ns < 1) ns = 1;
+    if (ns > steps_per_row) ns = steps_per_row;
+    p.comb_nsplit = (int32_t)ns;
     return e;
 }
 
 }  // namespace
 
+constexpr int kCombStagesMax = 16;
+constexpr int kCombDefaultCtasPerSm = 4;
+constexpr int kCombDefaultStageBytes = 16384;
+
+cudaError_t configure_combine_tma(a2av_plan_s &p) {
+    const size_t rowb = (size_t)p.g.H * 2;
+    const int cps = p.cfg.combine_ctas_per_sm > 0 ? p.cfg.combine_ctas_per_sm : kCombDefaultCtasPerSm;
+    const size_t target = p.cfg.combine_stage_bytes > 0 ? (size_t)p.cfg.combine_stage_bytes : kCombDefaultStageBytes;
+    size_t chunk = (target / (size_t)p.g.k) / 16 * 16;
+    if (chunk < 256) chunk = 256;
+    if (chunk > rowb) chunk = rowb;
+    int max_optin = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p.cfg.device);
+    if (e != cudaSuccess) return e;
+    size_t budget = (size_t)max_optin / cps;
+    budget = budget > 2048 ? budget - 2048 : budget;
+    // at least two stages: shrink the chunk if the requested one does not fit
+    while (chunk > 256 && 2 * ((size_t)p.g.k * chunk + sizeof(StageMeta) + 8) > budget) chunk = (chunk / 2 + 15) / 16 * 16;
+    const size_t per_stage = (size_t)p.g.k * chunk + sizeof(StageMeta) + 8;
+    int stages = (int)(budget / per_stage);
+    if (stages > kCombStagesMax) stages = kCombStagesMax;
+    if (stages < 2) return cudaErrorInvalidConfiguration;
+    p.comb_chunk_bytes = (int32_t)chunk;
+    p.comb_nchunks = (int32_t)((rowb + chunk - 1) / chunk);
+    p.comb_stages = stages;
+    p.combine.block = 32;
+    p.combine.grid = p.num_sms * cps;
+    p.combine.smem = (size_t)stages * per_stage;
+    return cudaFuncSetAttribute(combine_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
+}
+
 cudaError_t configure_combine(a2av_plan_s &p) {
     p.combine.block = 256;
     p.scale.block = 256;
     cudaError_t e;
+    if (p.cfg.flags & A2AV_FLAG_COMBINE_TMA) {
+        p.combine_tma = 1;
+        e = configure_combine_tma(p);
+        if (e != cudaSuccess) return e;
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, expert_scale_kernel, 256, 0);
+        p.scale.grid = p.num_sms * (per_sm > 0 ? per_sm : 1);
+        return e;
+    }
+    p.combine_tma = 0;
     switch (p.g.k) {
         case 1: e = occupancy_grid<1, 4>(p, p.combine.grid); break;
         case 2: e = occupancy_grid<2, 4>(p, p.combine.grid); break;
@@ -190,14 +394,24 @@ cudaError_t configure_combine(a2av_plan_s &p) {
 }
 
 cudaError_t launch_combine(const a2av_plan_s &p, const CombineArgs &a, cudaStream_t s) {
-    switch (p.g.k) {
-        case 1: combine_kernel<1, 4><<<p.combine.grid, 256, 0, s>>>(a); break;
-        case 2: combine_kernel<2, 4><<<p.combine.grid, 256, 0, s>>>(a); break;
-        case 4: combine_kernel<4, 2><<<p.combine.grid, 256, 0, s>>>(a); break;
-        case 8: combine_kernel<8, 2><<<p.combine.grid, 256, 0, s>>>(a); break;
-        default: combine_kernel<0, 2><<<p.combine.grid, 256, 0, s>>>(a); break;
+    cudaError_t e;
+    CombineArgs b = a;
+    if (p.combine_tma) {
+        b.chunk_bytes = p.comb_chunk_bytes;
+        b.nchunks = p.comb_nchunks;
+        b.stages = p.comb_stages;
+        e = launch_pdl(combine_tma_kernel, p.combine.grid, p.combine.block, p.combine.smem, s, b);
+        return e != cudaSuccess ? e : cudaGetLastError();
     }
-    return cudaGetLastError();
+    b.nsplit = p.comb_nsplit;
+    switch (p.g.k) {
+        case 1: e = launch_pdl(combine_kernel<1, 4>, p.combine.grid, 256, 0, s, b); break;
+        case 2: e = launch_pdl(combine_kernel<2, 4>, p.combine.grid, 256, 0, s, b); break;
+        case 4: e = launch_pdl(combine_kernel<4, 2>, p.combine.grid, 256, 0, s, b); break;
+        case 8: e = launch_pdl(combine_kernel<8, 2>, p.combine.grid, 256, 0, s, b); break;
+        default: e = launch_pdl(combine_kernel<0, 2>, p.combine.grid, 256, 0, s, b); break;
+    }
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_scale(const a2av_plan_s &p, const ScaleArgs &a, cudaStream_t s) {

@@ -25,61 +25,24 @@ namespace a2av {
 namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
-constexpr long long kWaitLimit = 1ll << 22;  // bounded spin on our own copies
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
-    for (long long it = 0; it < kWaitLimit; ++it)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst_smem)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-__device__ __forceinline__ void bulk_store(void *dst, const void *src_smem, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src_smem)),
-                 "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+__device__ __forceinline__ long long arena_rows_of(const Geometry &g) {
+    return g.window_mode == A2AV_WINDOW_FIXED ? (long long)g.R * g.window_rows : (long long)g.R * g.T * g.k;
 }
 
-// Final arena row of assignment j of flat token `tok` (reads the rank inside
-// its histogram tile from slot_map), or -1 if dropped.
+// Final arena row of assignment j of flat token `tok`, or -1 if dropped.  With
+// the tiled splits kernel slot_map holds the rank inside the histogram tile
+// and the row is assembled here; with the one-CTA kernel it is already final.
 __device__ __forceinline__ int32_t final_row(const PackArgs &a, long long tok, int j, uint32_t &ovf) {
     const Geometry &g = a.g;
     const size_t ga = (size_t)tok * g.k + j;
+    if (a.rows_final) {
+        const int32_t row = a.slot_map[ga];
+        if (row >= arena_rows_of(g)) {
+            ovf = 1;
+            return -1;
+        }
+        return row;
+    }
     const int e = __ldg(a.idx + ga);
     const int r = a.slot_map[ga];
     if (e < 0 || e >= g.E || r < 0) return -1;
@@ -95,9 +58,7 @@ __device__ __forceinline__ int32_t final_row(const PackArgs &a, long long tok, i
         return -1;
     }
     const long long row = (long long)__ldg(a.window_base + d) + rel;
-    const long long arena = g.window_mode == A2AV_WINDOW_FIXED ? (long long)g.R * g.window_rows
-                                                               : (long long)g.R * g.T * g.k;
-    if (row < 0 || row >= arena) {
+    if (row < 0 || row >= arena_rows_of(g)) {
         ovf = 1;
         return -1;
     }
@@ -113,7 +74,7 @@ __device__ __forceinline__ int32_t batch_rows(const PackArgs &a, long long tok0,
     const long long tok = tok0 + b;
     if (b >= bt || tok >= tok_end) return -1;
     const int32_t row = final_row(a, tok, j, ovf);
-    a.slot_map[(size_t)tok * k + j] = row;
+    if (!a.rows_final) a.slot_map[(size_t)tok * k + j] = row;
     return row;
 }
 
@@ -149,10 +110,16 @@ __global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
         mbar_arrive_expect_tx(bar, bytes);
         bulk_load(smem + (size_t)(p % NS) * CH, x + (size_t)tok * rowb + off, bytes, bar);
     };
+    // Loads may run NS - LAG units ahead; up to LAG store groups may still be
+    // reading their stage when the next load is issued.
+    const int LAG = a.lag;
     const long long pre = min(n, (long long)NS);
     if (lane == 0)
         for (long long p = 0; p < pre; ++p) issue_load(p);
     long long issued = pre;  // loads issued so far (units 0..issued-1)
+
+    // x does not depend on the splits kernel; everything below does.
+    grid_dependency_wait();
 
     uint32_t ovf = 0;
     long long batch_tok0 = tb;
@@ -186,13 +153,13 @@ __global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
         }
         if (lane == 0) {
             bulk_commit();
-            const long long p = i - 1 + NS;
-            if (i >= 1 && p < n) {
-                bulk_wait_read_1();
-                issue_load(p);
+            const long long jdone = i - (LAG - 1);  // its stores have finished reading once <= LAG-1 groups pend
+            if (jdone >= 0 && jdone + NS < n) {
+                bulk_wait_read_upto(LAG - 1);
+                issue_load(jdone + NS);
+                issued = jdone + NS + 1;
             }
         }
-        issued = min(n, max(issued, i - 1 + NS + 1));
         __syncwarp();
     }
     if (lane == 0) {
@@ -215,11 +182,12 @@ __global__ void __launch_bounds__(256) pack_lsu_kernel(const PackArgs a) {
     const size_t rowb = (size_t)g.H * 2;
     const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
     uint32_t ovf = 0;
+    grid_dependency_wait();
     for (long long u = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < ntok; u += nw) {
         int32_t row = -1;
         if (lane < g.k) {
             row = final_row(a, u, lane, ovf);
-            a.slot_map[(size_t)u * g.k + lane] = row;
+            if (!a.rows_final) a.slot_map[(size_t)u * g.k + lane] = row;
         }
         const char *src = reinterpret_cast<const char *>(a.x) + (size_t)u * rowb;
         for (int vb = 0; vb < nv; vb += 32 * U) {
@@ -246,6 +214,8 @@ __global__ void __launch_bounds__(256) pack_lsu_kernel(const PackArgs a) {
 
 constexpr int kLsuUnroll = 4;
 constexpr size_t kTmaChunkMax = 16384;
+constexpr int kDefaultCtasPerSm = 4;
+constexpr int kDefaultLag = 2;
 
 }  // namespace
 
@@ -260,21 +230,26 @@ cudaError_t configure_pack(a2av_plan_s &p) {
         p.pack.smem = 0;
         return cudaSuccess;
     }
-    const int ctas_per_sm = p.cfg.pack_ctas_per_sm > 0 ? p.cfg.pack_ctas_per_sm : 1;
+    const int ctas_per_sm = p.cfg.pack_ctas_per_sm > 0 ? p.cfg.pack_ctas_per_sm : kDefaultCtasPerSm;
     size_t chunk = p.cfg.pack_stage_bytes > 0 ? (size_t)p.cfg.pack_stage_bytes : kTmaChunkMax;
     chunk = (chunk + 15) / 16 * 16;
     if (chunk > rowb) chunk = rowb;
-    const int nch = (int)((rowb + chunk - 1) / chunk);
     int max_optin = 0;
     cudaError_t e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p.cfg.device);
     if (e != cudaSuccess) return e;
     size_t budget = (size_t)max_optin / ctas_per_sm;
     budget = budget > 2048 ? budget - 2048 : budget;  // leave room for the static/runtime reservation
+    // at least two stages: shrink the chunk if the requested one does not fit
+    while (chunk > 256 && 2 * (chunk + 8) > budget) chunk = (chunk / 2 + 15) / 16 * 16;
+    const int nch2 = (int)((rowb + chunk - 1) / chunk);
     int stages = (int)((budget) / (chunk + 8));
     if (stages > 32) stages = 32;
-    if (stages < 2) return cudaErrorInvalidConfiguration;
+    int lag = p.cfg.pack_store_lag > 0 ? p.cfg.pack_store_lag : kDefaultLag;
+    if (lag > stages - 1) lag = stages - 1;
+    if (lag < 1) return cudaErrorInvalidConfiguration;
+    p.pack_lag = lag;
     p.pack_chunk_bytes = (int32_t)chunk;
-    p.pack_nchunks = nch;
+    p.pack_nchunks = nch2;
     p.pack_stages = stages;
     p.pack.block = 32;
     p.pack.smem = (size_t)stages * chunk + (size_t)stages * 8;
@@ -285,16 +260,19 @@ cudaError_t configure_pack(a2av_plan_s &p) {
 }
 
 cudaError_t launch_pack(const a2av_plan_s &p, const PackArgs &a, cudaStream_t s) {
+    PackArgs b = a;
+    b.rows_final = p.splits_small;
+    cudaError_t e;
     if (p.pack_tma) {
-        PackArgs b = a;
         b.chunk_bytes = p.pack_chunk_bytes;
         b.nchunks = p.pack_nchunks;
         b.stages = p.pack_stages;
-        pack_tma_kernel<<<p.pack.grid, p.pack.block, p.pack.smem, s>>>(b);
+        b.lag = p.pack_lag;
+        e = launch_pdl(pack_tma_kernel, p.pack.grid, p.pack.block, p.pack.smem, s, b);
     } else {
-        pack_lsu_kernel<kLsuUnroll><<<p.pack.grid, p.pack.block, 0, s>>>(a);
+        e = launch_pdl(pack_lsu_kernel<kLsuUnroll>, p.pack.grid, p.pack.block, 0, s, b);
     }
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace a2av

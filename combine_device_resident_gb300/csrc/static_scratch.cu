@@ -76,6 +76,8 @@ extern "C" a2av_status_t a2av_dispatch_static(const a2av_config_t *cfg, const vo
     g.H = cfg->hidden;
     g.k = cfg->topk;
     g.epr = g.E / g.R;
+    g.key_bits = 1;
+    while ((1 << g.key_bits) <= g.E) ++g.key_bits;
     g.tiles = (int32_t)(((long long)g.T * g.k + a2av::kHistTile - 1) / a2av::kHistTile);
     g.window_mode = cfg->window_mode;
     g.window_rows = cfg->window_mode == A2AV_WINDOW_FIXED ? cfg->window_rows : 0;

@@ -97,7 +97,9 @@ enum {
 
 /* Variant flags (a2av_config_t.flags). */
 enum {
-    A2AV_FLAG_PACK_LSU = 1u << 0, /* pack+exchange with 16-byte vector loads/stores instead of TMA bulk copies */
+    A2AV_FLAG_PACK_LSU = 1u << 0,     /* pack+exchange with 16-byte vector loads/stores instead of TMA bulk copies */
+    A2AV_FLAG_SPLITS_TILED = 1u << 1, /* always use the multi-CTA tiled splits kernel (else one CTA when it fits) */
+    A2AV_FLAG_COMBINE_TMA = 1u << 2,  /* combine through TMA bulk copies into shared memory (default: vector gathers) */
 };
 
 typedef struct {
@@ -110,8 +112,11 @@ typedef struct {
     int64_t window_rows;     /* fixed mode: rows per window (R*window_rows < 2^31); ignored when packed */
     int32_t device;          /* CUDA device ordinal the plan and all its tensors live on */
     uint32_t flags;          /* A2AV_FLAG_* */
-    int32_t pack_ctas_per_sm; /* TMA pack: resident CTAs per SM, 1..4 (0 = 1) */
+    int32_t pack_ctas_per_sm; /* TMA pack: resident CTAs per SM, 1..4 (0 = 4) */
     int32_t pack_stage_bytes; /* TMA pack: bytes per shared-memory stage, multiple of 16 (0 = min(row, 16 KiB)) */
+    int32_t pack_store_lag;   /* TMA pack: row stores that may still read a stage before its refill, 1..8 (0 = 2) */
+    int32_t combine_ctas_per_sm;  /* TMA combine: resident CTAs per SM, 1..8 (0 = 4) */
+    int32_t combine_stage_bytes;  /* TMA combine: bytes of the k row chunks per stage, multiple of 16 (0 = 16 KiB) */
 } a2av_config_t;
 
 /* Caller-owned device arrays the split counts and offsets are written to

@@ -59,7 +59,7 @@ def test_config_check_host_only(lib):
           _cfg(window_mode="fixed", window_rows=100)]
     bad = [_cfg(R=0), _cfg(R=65, E=130), _cfg(E=12, R=8), _cfg(E=4096, R=8), _cfg(H=12), _cfg(H=0), _cfg(k=0),
            _cfg(k=33), _cfg(T=0), _cfg(window_mode=2), _cfg(window_mode="fixed", window_rows=-1),
-           _cfg(R=64, E=64, T=1 << 20, k=32), _cfg(flags=1 << 7), _cfg(pack_stage_bytes=24),
+           _cfg(R=64, E=64, T=1 << 20, k=32), _cfg(flags=1 << 7), _cfg(flags=1 << 3), _cfg(pack_stage_bytes=24),
            _cfg(pack_ctas_per_sm=9)]
     for c in ok:
         assert lib.a2av_config_check(ctypes.byref(c)) == 0

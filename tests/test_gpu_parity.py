@@ -39,24 +39,44 @@ def test_workload_parity_full_hidden(wid):
     P.full_parity(W.WORKLOADS[wid].scaled(T=300))
 
 
-def test_combine_is_bit_exact_against_oracle():
-    # The kernel rounds each product and sum separately in slot order, exactly
+@pytest.mark.parametrize("flags", [0, 4], ids=["lsu", "tma"])
+def test_combine_is_bit_exact_against_oracle(flags):
+    # The kernels round each product and sum separately in slot order, exactly
     # as the oracle does, so the result is the oracle's bit for bit (the
     # stated bar, 1 ulp, is looser).
-    for wid, T, H in [(4, 700, 200), (5, 300, 64)]:
-        g = P.full_parity(W.WORKLOADS[wid].scaled(T=T, H=H))
+    for wid, T, H in [(4, 700, 200), (5, 300, 64), (5, 90, 7176)]:
+        g = P.full_parity(W.WORKLOADS[wid].scaled(T=T, H=H), flags=flags)
         np.testing.assert_array_equal(g["out"], g["ref"]["out"])
 
 
 @pytest.mark.parametrize("variant", [
     dict(flags=1),                              # LSU pack
-    dict(pack_ctas_per_sm=2),                   # two TMA CTAs per SM
+    dict(pack_ctas_per_sm=1),                   # one TMA CTA per SM, deep ring
+    dict(pack_ctas_per_sm=2, pack_store_lag=1),  # stores must finish reading before each refill
     dict(pack_stage_bytes=1024),                # rows split into several stage chunks
-    dict(pack_stage_bytes=4096, pack_ctas_per_sm=3),
-], ids=["lsu", "tma2", "chunked", "chunked3"])
+    dict(pack_stage_bytes=4096, pack_ctas_per_sm=3, pack_store_lag=6),
+    dict(flags=2),                              # tiled splits kernel forced
+    dict(flags=3),                              # tiled splits + LSU pack
+    dict(flags=4),                              # TMA combine
+    dict(flags=7),                              # LSU pack, tiled splits, TMA combine
+    dict(flags=4, combine_ctas_per_sm=1, combine_stage_bytes=2048),   # TMA combine: deep ring, small chunks
+    dict(flags=4, combine_ctas_per_sm=8, combine_stage_bytes=65536),  # TMA combine: whole rows, 2 stages
+], ids=["lsu", "tma1", "lag1", "chunked", "chunked3-lag6", "tiled", "tiled-lsu", "tma-combine", "mixed",
+        "comb-deep", "comb-wide"])
 def test_pack_variants(variant):
     P.full_parity(W.WORKLOADS[5].scaled(T=500, H=1032), **variant)
     P.full_parity(W.WORKLOADS[2].scaled(T=900, H=2056), **variant)
+    P.full_parity(W.WORKLOADS[2].scaled(T=200, H=520), **variant)  # one-CTA splits unless forced
+
+
+@pytest.mark.parametrize("wid,T,H", [(1, None, None), (2, 1024, 264), (3, 256, 136), (3, 130, 40)])
+def test_one_cta_and_tiled_splits_agree(wid, T, H):
+    # workloads small enough for the one-CTA splits kernel, run both ways
+    w = W.WORKLOADS[wid] if T is None else W.WORKLOADS[wid].scaled(T=T, H=H)
+    a = P.full_parity(w)
+    b = P.full_parity(w, flags=2)
+    assert a["plan"].cfg.flags == 0 and b["plan"].cfg.flags == 2
+    np.testing.assert_array_equal(a["slot_map"], b["slot_map"])
 
 
 def _uniform(R, E, T, H, k, **kw):
