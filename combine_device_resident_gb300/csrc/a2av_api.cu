@@ -132,11 +132,10 @@ a2av_status_t a2av_plan_create(const a2av_config_t *cfg, a2av_plan_t *out_plan) 
         return cuda_fail(e, "cudaDeviceGetAttribute");
     }
 
-    // Workspace: tile bases [R][tiles][E], dest bases [R][E], counters [R+1], status.
+    // Workspace: tile bases [R][tiles][E], per-rank totals [R], counters [R+1], status.
     const size_t n_tile = (size_t)g.R * g.tiles * g.E;
-    const size_t n_dest = (size_t)g.R * g.E;
-    const size_t off_dest = ((n_tile * 4) + 255) / 256 * 256;
-    const size_t off_cnt = off_dest + ((n_dest * 4) + 255) / 256 * 256;
+    const size_t off_tot = ((n_tile * 4) + 255) / 256 * 256;
+    const size_t off_cnt = off_tot + (((size_t)g.R * 4) + 255) / 256 * 256;
     const size_t off_status = off_cnt + (((size_t)g.R + 1) * 4 + 255) / 256 * 256;
     p->workspace_bytes = off_status + 256;
     e = cudaMalloc(&p->workspace, p->workspace_bytes);
@@ -147,7 +146,7 @@ a2av_status_t a2av_plan_create(const a2av_config_t *cfg, a2av_plan_t *out_plan) 
     }
     char *base = static_cast<char *>(p->workspace);
     p->tile_base = reinterpret_cast<int32_t *>(base);
-    p->dest_base = reinterpret_cast<int32_t *>(base + off_dest);
+    p->rank_total = reinterpret_cast<int32_t *>(base + off_tot);
     p->counters = reinterpret_cast<uint32_t *>(base + off_cnt);
     p->status = reinterpret_cast<uint32_t *>(base + off_status);
     e = cudaMemset(p->workspace, 0, p->workspace_bytes);
@@ -182,7 +181,7 @@ a2av_status_t a2av_splits(a2av_plan_t p, const int32_t *topk_idx, const a2av_spl
     a.idx = topk_idx;
     a.slot_map = slot_map;
     a.tile_base = p->tile_base;
-    a.dest_base = p->dest_base;
+    a.rank_total = p->rank_total;
     a.counters = p->counters;
     a.status = p->status;
     a.sp = to_internal(splits);
@@ -208,7 +207,8 @@ a2av_status_t a2av_pack(a2av_plan_t p, const void *x, const int32_t *topk_idx, c
     a.idx = topk_idx;
     a.slot_map = slot_map;
     a.tile_base = p->tile_base;
-    a.dest_base = p->dest_base;
+    a.send_offsets = splits->send_offsets;
+    a.recv_offsets = splits->recv_offsets;
     a.window_base = splits->window_base;
     a.recv = static_cast<uint16_t *>(recv);
     a.status = p->status;

@@ -41,9 +41,9 @@ struct HistArgs {
     Geometry g;
     const int32_t *idx;
     int32_t *slot_map;   // receives the rank of each assignment inside its tile
-    int32_t *tile_base;  // [R][tiles][E] counts, turned into exclusive bases
-    int32_t *dest_base;  // [R][E] window-relative first row of (source, expert)
-    uint32_t *counters;  // [R + 1] last-block-done counters (left at 0)
+    int32_t *tile_base;   // [R][tiles][E] counts, turned into exclusive bases
+    int32_t *rank_total;  // [R] valid assignments of each source rank
+    uint32_t *counters;   // [R + 1] last-block-done counters (left at 0)
     uint32_t *status;
     Splits sp;
 };
@@ -54,7 +54,8 @@ struct PackArgs {
     const int32_t *idx;
     int32_t *slot_map;
     const int32_t *tile_base;
-    const int32_t *dest_base;
+    const int32_t *send_offsets;  // splits arrays written by the splits kernel
+    const int32_t *recv_offsets;
     const int32_t *window_base;
     uint16_t *recv;
     uint32_t *status;
@@ -111,7 +112,7 @@ struct a2av_plan_s {
     void *workspace = nullptr;  // one device allocation
     size_t workspace_bytes = 0;
     int32_t *tile_base = nullptr;
-    int32_t *dest_base = nullptr;
+    int32_t *rank_total = nullptr;
     uint32_t *counters = nullptr;
     uint32_t *status = nullptr;
     a2av::LaunchShape hist, pack, combine, scale;

@@ -6,10 +6,11 @@
 // inference; the hungchun0201 digest, 3.3 AllToAllvDynamic).
 //
 // Row of assignment (s, t, j) with expert e on rank d = e / (E/R):
-//   rel = dest_base[s][e] + tile_base[s][tile(t*k+j)][e] + rank_in_tile
+//   rel = recv_offsets[d][s] + send_offsets[s][e] - send_offsets[s][d*E/R]
+//         + tile_base[s][tile(t*k+j)][e] + rank_in_tile
 //   row = window_base[d] + rel        (dropped if rel >= window_rows, fixed mode)
-// where dest_base = recv_offsets[d][s] + send_offsets[s][e] - send_offsets[s][d*E/R]
-// (all produced on the device by the splits kernel).
+// (all produced on the device by the splits kernel; with the cluster splits
+// kernel slot_map already holds the row).
 //
 // Two variants:
 //   * TMA bulk (default): persistent grid, one warp per CTA.  Row chunks are
@@ -50,7 +51,9 @@ __device__ __forceinline__ int32_t final_row(const PackArgs &a, long long tok, i
     const int t = (int)(tok - (long long)s * g.T);
     const int tl = (t * g.k + j) / kHistTile;
     const int d = e / g.epr;
-    const long long rel = (long long)__ldg(a.dest_base + (size_t)s * g.E + e) +
+    const long long rel = (long long)__ldg(a.recv_offsets + (size_t)d * g.R + s) +
+                          __ldg(a.send_offsets + (size_t)s * g.E + e) -
+                          __ldg(a.send_offsets + (size_t)s * g.E + (size_t)d * g.epr) +
                           __ldg(a.tile_base + ((size_t)s * g.tiles + tl) * g.E + e) + r;
     const long long cap = g.window_mode == A2AV_WINDOW_FIXED ? g.window_rows : (long long)g.R * g.T * g.k;
     if (rel < 0 || rel >= cap) {

@@ -5,8 +5,8 @@
 // whose caching allocator owns all device memory and must not be bypassed,
 // or processes with a fixed device-memory budget that is exhausted by the
 // time this library runs.  For them this entry point keeps its scratch (the
-// per-tile histogram bases, the per-(source, expert) window bases and the
-// completion counters the splits kernel needs) in one file-scope __device__
+// per-tile histogram bases, the per-rank totals and the completion counters
+// the splits kernel needs) in one file-scope __device__
 // array, so the only device memory it touches besides the caller's buffers
 // is memory the library already owns from the moment it is loaded.
 //
@@ -23,7 +23,7 @@
 namespace {
 
 // 1 MiB of scratch per GPU (262144 int32).  Enough for, e.g., R=32 ranks,
-// E=256 experts and 16384 assignments per rank (about 74k entries).
+// E=256 experts and 16384 assignments per rank (about 66k entries).
 constexpr size_t kStaticScratchInts = 262144;
 static __device__ __align__(256) int32_t g_dispatch_scratch[kStaticScratchInts];
 
@@ -93,14 +93,14 @@ extern "C" a2av_status_t a2av_dispatch_static(const a2av_config_t *cfg, const vo
     }
 
     const size_t n_tile = round64((size_t)g.R * g.tiles * g.E);
-    const size_t n_dest = round64((size_t)g.R * g.E);
+    const size_t n_tot = round64((size_t)g.R);
     const size_t n_cnt = round64((size_t)g.R + 1);
-    if (n_tile + n_dest + n_cnt > kStaticScratchInts) {
+    if (n_tile + n_tot + n_cnt > kStaticScratchInts) {
         char msg[256];
         snprintf(msg, sizeof msg,
                  "a2av_dispatch_static: this shape needs %zu int32 of scratch, the static array holds %zu "
                  "(use a plan and a2av_dispatch instead)",
-                 n_tile + n_dest + n_cnt, kStaticScratchInts);
+                 n_tile + n_tot + n_cnt, kStaticScratchInts);
         a2av::set_last_error(msg);
         return A2AV_ERR_INVALID_ARG;
     }
@@ -113,8 +113,8 @@ extern "C" a2av_status_t a2av_dispatch_static(const a2av_config_t *cfg, const vo
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p.num_sms, cudaDevAttrMultiProcessorCount, cfg->device);
     if (e == cudaSuccess) {
         p.tile_base = scratch;
-        p.dest_base = scratch + n_tile;
-        p.counters = reinterpret_cast<uint32_t *>(scratch + n_tile + n_dest);
+        p.rank_total = scratch + n_tile;
+        p.counters = reinterpret_cast<uint32_t *>(scratch + n_tile + n_tot);
         p.status = dev_status;
         e = a2av::configure_hist(p);
     }
@@ -129,7 +129,7 @@ extern "C" a2av_status_t a2av_dispatch_static(const a2av_config_t *cfg, const vo
         h.idx = topk_idx;
         h.slot_map = slot_map;
         h.tile_base = p.tile_base;
-        h.dest_base = p.dest_base;
+        h.rank_total = p.rank_total;
         h.counters = p.counters;
         h.status = dev_status;
         h.sp = a2av::Splits{splits->send_counts, splits->send_offsets, splits->recv_counts, splits->recv_offsets,
@@ -143,7 +143,8 @@ extern "C" a2av_status_t a2av_dispatch_static(const a2av_config_t *cfg, const vo
         a.idx = topk_idx;
         a.slot_map = slot_map;
         a.tile_base = p.tile_base;
-        a.dest_base = p.dest_base;
+        a.send_offsets = splits->send_offsets;
+        a.recv_offsets = splits->recv_offsets;
         a.window_base = splits->window_base;
         a.recv = static_cast<uint16_t *>(recv);
         a.status = dev_status;

@@ -200,7 +200,7 @@ a2av_status_t a2av_expert_scale(a2av_plan_t plan, const void *recv, const int32_
  * and results as a2av_dispatch on a plan made from `cfg`; the scratch the
  * splits and pack kernels need lives in one static device array of the
  * library (1 MiB per GPU that loads the library, held until process exit),
- * which bounds the shapes it accepts: R*ceil(T*k/2048)*E + R*E + R + 1 int32
+ * which bounds the shapes it accepts: R*ceil(T*k/2048)*E + R + (R + 1) int32
  * (each term rounded up to 64) must fit in 262144, else A2AV_ERR_INVALID_ARG
  * with the sizes in a2av_last_error().  `dev_status` is a caller-owned device
  * uint32 that the kernels OR the A2AV_DEV_* bits into (the caller clears it).
