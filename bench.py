@@ -57,6 +57,7 @@ def parse():
     ap.add_argument("--pack-store-lag", type=int, default=0)
     ap.add_argument("--combine-ctas-per-sm", type=int, default=0)
     ap.add_argument("--combine-stage-bytes", type=int, default=0)
+    ap.add_argument("--combine-unroll", type=int, default=0)
     ap.add_argument("--kernel-steps", type=int, default=300, help="steps of the per-kernel timing pass")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline sample budget")
@@ -282,7 +283,7 @@ def main():
     plan = A.Plan(w.R, w.E, w.T, w.H, w.k, w.window_mode, w.window_rows, device=dev, flags=args.flags,
                   pack_ctas_per_sm=args.pack_ctas_per_sm, pack_stage_bytes=args.pack_stage_bytes,
                   pack_store_lag=args.pack_store_lag, combine_ctas_per_sm=args.combine_ctas_per_sm,
-                  combine_stage_bytes=args.combine_stage_bytes)
+                  combine_stage_bytes=args.combine_stage_bytes, combine_unroll=args.combine_unroll)
     recv, slot_map, out = plan.new_buffers()
     sp = plan.new_splits()
     # L2 flush by READING a buffer larger than L2: it evicts our lines and leaves
@@ -468,7 +469,8 @@ def main():
                                           "pack_stage_bytes": args.pack_stage_bytes,
                                           "pack_store_lag": args.pack_store_lag,
                                           "combine_ctas_per_sm": args.combine_ctas_per_sm,
-                                          "combine_stage_bytes": args.combine_stage_bytes},
+                                          "combine_stage_bytes": args.combine_stage_bytes,
+                                          "combine_unroll": args.combine_unroll},
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -54,6 +54,7 @@ class Config(ctypes.Structure):
         ("pack_store_lag", ctypes.c_int32),
         ("combine_ctas_per_sm", ctypes.c_int32),
         ("combine_stage_bytes", ctypes.c_int32),
+        ("combine_unroll", ctypes.c_int32),
     ]
 
 
@@ -130,11 +131,11 @@ def _check(L, rc: int, what: str):
 
 def make_config(R, E, T, H, k, window_mode="packed", window_rows=0, device=0, flags=0,
                 pack_ctas_per_sm=0, pack_stage_bytes=0, pack_store_lag=0, combine_ctas_per_sm=0,
-                combine_stage_bytes=0) -> Config:
+                combine_stage_bytes=0, combine_unroll=0) -> Config:
     mode = {"packed": WINDOW_PACKED, "fixed": WINDOW_FIXED}.get(window_mode, window_mode)
     return Config(int(R), int(E), int(T), int(H), int(k), int(mode), int(window_rows), int(device),
                   int(flags), int(pack_ctas_per_sm), int(pack_stage_bytes), int(pack_store_lag),
-                  int(combine_ctas_per_sm), int(combine_stage_bytes))
+                  int(combine_ctas_per_sm), int(combine_stage_bytes), int(combine_unroll))
 
 
 class Splits:
@@ -175,7 +176,7 @@ class Plan:
 
     def __init__(self, R, E, T, H, k, window_mode="packed", window_rows=0, device=None, flags=0,
                  pack_ctas_per_sm=0, pack_stage_bytes=0, pack_store_lag=0, combine_ctas_per_sm=0,
-                 combine_stage_bytes=0):
+                 combine_stage_bytes=0, combine_unroll=0):
         import torch
 
         self.lib = load_library()
@@ -188,7 +189,7 @@ class Plan:
         self.window_rows = int(window_rows)
         self.cfg = make_config(R, E, T, H, k, window_mode, window_rows, dev.index, flags,
                                pack_ctas_per_sm, pack_stage_bytes, pack_store_lag, combine_ctas_per_sm,
-                               combine_stage_bytes)
+                               combine_stage_bytes, combine_unroll)
         handle = ctypes.c_void_p()
         _check(self.lib, self.lib.a2av_plan_create(ctypes.byref(self.cfg), ctypes.byref(handle)), "a2av_plan_create")
         self.handle = handle

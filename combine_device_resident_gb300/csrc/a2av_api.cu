@@ -86,6 +86,7 @@ a2av_status_t a2av_config_check(const a2av_config_t *c) {
     if (c->combine_ctas_per_sm < 0 || c->combine_ctas_per_sm > 8) return A2AV_ERR_INVALID_ARG;
     if (c->combine_stage_bytes < 0 || c->combine_stage_bytes % 16 != 0 || c->combine_stage_bytes > 131072)
         return A2AV_ERR_INVALID_ARG;
+    if (c->combine_unroll < 0 || c->combine_unroll > 8) return A2AV_ERR_INVALID_ARG;
     if (c->pack_ctas_per_sm < 0 || c->pack_ctas_per_sm > 4) return A2AV_ERR_INVALID_ARG;
     if (c->pack_stage_bytes < 0 || c->pack_stage_bytes % 16 != 0 || c->pack_stage_bytes > 65536)
         return A2AV_ERR_INVALID_ARG;

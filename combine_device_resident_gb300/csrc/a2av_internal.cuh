@@ -118,7 +118,7 @@ struct a2av_plan_s {
     a2av::LaunchShape hist, pack, combine, scale;
     int splits_small = 0;  // 1: one-CTA splits kernel that writes final rows
     int combine_tma = 1;
-    int32_t comb_chunk_bytes = 0, comb_nchunks = 0, comb_stages = 0, comb_nsplit = 1;
+    int32_t comb_chunk_bytes = 0, comb_nchunks = 0, comb_stages = 0, comb_nsplit = 1, comb_unroll = 2;
     int pack_tma = 1;
     int32_t pack_chunk_bytes = 0, pack_nchunks = 0, pack_stages = 0, pack_lag = 1;
     int64_t launches = 0;

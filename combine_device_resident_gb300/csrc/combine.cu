@@ -316,19 +316,59 @@ __global__ void __launch_bounds__(256) expert_scale_kernel(const ScaleArgs a) {
     }
 }
 
-template <int KT, int U>
-cudaError_t occupancy_grid(a2av_plan_s &p, int &grid) {
+using CombineKernel = void (*)(const CombineArgs);
+
+// The instantiated (k, U) pairs; U = 16-byte vectors per lane and step.
+struct CombineVariant {
+    int k, u;
+    CombineKernel fn;
+};
+const CombineVariant kCombineVariants[] = {
+    {1, 2, combine_kernel<1, 2>}, {1, 4, combine_kernel<1, 4>}, {1, 8, combine_kernel<1, 8>},
+    {2, 1, combine_kernel<2, 1>}, {2, 2, combine_kernel<2, 2>}, {2, 4, combine_kernel<2, 4>},
+    {4, 1, combine_kernel<4, 1>}, {4, 2, combine_kernel<4, 2>},
+    {8, 1, combine_kernel<8, 1>}, {8, 2, combine_kernel<8, 2>},
+    {0, 1, combine_kernel<0, 1>}, {0, 2, combine_kernel<0, 2>},
+};
+
+// Measured on GB300: fewer loads per lane and more resident warps win
+// (k*U of 2 to 8 vectors in flight per lane).
+int default_unroll(int k) {
+    switch (k) {
+        case 1: return 2;
+        case 2: return 2;
+        case 4: return 1;
+        case 8: return 1;
+        default: return 1;
+    }
+}
+
+// Kernel for this plan's k and requested unroll (nearest instantiated one).
+const CombineVariant *pick_variant(int k, int want_u) {
+    const int kk = (k == 1 || k == 2 || k == 4 || k == 8) ? k : 0;
+    const int u = want_u > 0 ? want_u : (kk ? default_unroll(kk) : 2);
+    const CombineVariant *best = nullptr;
+    for (const auto &v : kCombineVariants) {
+        if (v.k != kk) continue;
+        if (!best || abs(v.u - u) < abs(best->u - u) || (abs(v.u - u) == abs(best->u - u) && v.u < best->u))
+            best = &v;
+    }
+    return best;
+}
+
+cudaError_t occupancy_grid(a2av_plan_s &p, const CombineVariant *v) {
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<KT, U>, 256, 0);
-    grid = p.num_sms * (per_sm > 0 ? per_sm : 1);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, v->fn, 256, 0);
+    p.combine.grid = p.num_sms * (per_sm > 0 ? per_sm : 1);
     // split rows so that every warp gets at least ~4 units
-    const long long warps = (long long)grid * 8;
+    const long long warps = (long long)p.combine.grid * 8;
     const long long ntok = (long long)p.g.R * p.g.T;
-    const int steps_per_row = ((p.g.H >> 3) + 32 * U - 1) / (32 * U);
+    const int steps_per_row = ((p.g.H >> 3) + 32 * v->u - 1) / (32 * v->u);
     long long ns = (4 * warps + ntok - 1) / ntok;
     if (ns < 1) ns = 1;
     if (ns > steps_per_row) ns = steps_per_row;
     p.comb_nsplit = (int32_t)ns;
+    p.comb_unroll = v->u;
     return e;
 }
 
@@ -379,13 +419,7 @@ cudaError_t configure_combine(a2av_plan_s &p) {
         return e;
     }
     p.combine_tma = 0;
-    switch (p.g.k) {
-        case 1: e = occupancy_grid<1, 4>(p, p.combine.grid); break;
-        case 2: e = occupancy_grid<2, 4>(p, p.combine.grid); break;
-        case 4: e = occupancy_grid<4, 2>(p, p.combine.grid); break;
-        case 8: e = occupancy_grid<8, 2>(p, p.combine.grid); break;
-        default: e = occupancy_grid<0, 2>(p, p.combine.grid); break;
-    }
+    e = occupancy_grid(p, pick_variant(p.g.k, p.cfg.combine_unroll));
     if (e != cudaSuccess) return e;
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, expert_scale_kernel, 256, 0);
@@ -404,13 +438,7 @@ cudaError_t launch_combine(const a2av_plan_s &p, const CombineArgs &a, cudaStrea
         return e != cudaSuccess ? e : cudaGetLastError();
     }
     b.nsplit = p.comb_nsplit;
-    switch (p.g.k) {
-        case 1: e = launch_pdl(combine_kernel<1, 4>, p.combine.grid, 256, 0, s, b); break;
-        case 2: e = launch_pdl(combine_kernel<2, 4>, p.combine.grid, 256, 0, s, b); break;
-        case 4: e = launch_pdl(combine_kernel<4, 2>, p.combine.grid, 256, 0, s, b); break;
-        case 8: e = launch_pdl(combine_kernel<8, 2>, p.combine.grid, 256, 0, s, b); break;
-        default: e = launch_pdl(combine_kernel<0, 2>, p.combine.grid, 256, 0, s, b); break;
-    }
+    e = launch_pdl(pick_variant(p.g.k, p.comb_unroll)->fn, p.combine.grid, 256, 0, s, b);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

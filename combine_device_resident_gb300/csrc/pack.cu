@@ -234,7 +234,10 @@ cudaError_t configure_pack(a2av_plan_s &p) {
         return cudaSuccess;
     }
     const int ctas_per_sm = p.cfg.pack_ctas_per_sm > 0 ? p.cfg.pack_ctas_per_sm : kDefaultCtasPerSm;
-    size_t chunk = p.cfg.pack_stage_bytes > 0 ? (size_t)p.cfg.pack_stage_bytes : kTmaChunkMax;
+    // Defaults measured on GB300: for k >= 4 small stages (many loads ahead)
+    // and a deep store lag; for k <= 2 whole-row stages (big stores per unit).
+    const bool wide = p.g.k >= 4;
+    size_t chunk = p.cfg.pack_stage_bytes > 0 ? (size_t)p.cfg.pack_stage_bytes : (wide ? 2048 : kTmaChunkMax);
     chunk = (chunk + 15) / 16 * 16;
     if (chunk > rowb) chunk = rowb;
     int max_optin = 0;
@@ -247,7 +250,7 @@ cudaError_t configure_pack(a2av_plan_s &p) {
     const int nch2 = (int)((rowb + chunk - 1) / chunk);
     int stages = (int)((budget) / (chunk + 8));
     if (stages > 32) stages = 32;
-    int lag = p.cfg.pack_store_lag > 0 ? p.cfg.pack_store_lag : kDefaultLag;
+    int lag = p.cfg.pack_store_lag > 0 ? p.cfg.pack_store_lag : (wide ? 6 : kDefaultLag);
     if (lag > stages - 1) lag = stages - 1;
     if (lag < 1) return cudaErrorInvalidConfiguration;
     p.pack_lag = lag;

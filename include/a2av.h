@@ -113,10 +113,14 @@ typedef struct {
     int32_t device;          /* CUDA device ordinal the plan and all its tensors live on */
     uint32_t flags;          /* A2AV_FLAG_* */
     int32_t pack_ctas_per_sm; /* TMA pack: resident CTAs per SM, 1..4 (0 = 4) */
-    int32_t pack_stage_bytes; /* TMA pack: bytes per shared-memory stage, multiple of 16 (0 = min(row, 16 KiB)) */
-    int32_t pack_store_lag;   /* TMA pack: row stores that may still read a stage before its refill, 1..8 (0 = 2) */
+    int32_t pack_stage_bytes; /* TMA pack: bytes per shared-memory stage, multiple of 16
+                                 (0 = 2 KiB for k >= 4, else min(row, 16 KiB)) */
+    int32_t pack_store_lag;   /* TMA pack: row stores that may still read a stage before its refill, 1..8
+                                 (0 = 6 for k >= 4, else 2) */
     int32_t combine_ctas_per_sm;  /* TMA combine: resident CTAs per SM, 1..8 (0 = 4) */
     int32_t combine_stage_bytes;  /* TMA combine: bytes of the k row chunks per stage, multiple of 16 (0 = 16 KiB) */
+    int32_t combine_unroll;       /* vector combine: 16-byte loads per lane and slot per step, 1..8
+                                     (0 = 2 for k <= 2, else 1) */
 } a2av_config_t;
 
 /* Caller-owned device arrays the split counts and offsets are written to

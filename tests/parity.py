@@ -27,7 +27,7 @@ def device():
 
 def gpu_run(w: W.Workload, x, idx: np.ndarray, gate: np.ndarray, flags=0, pack_ctas_per_sm=0,
             pack_stage_bytes=0, pack_store_lag=0, combine_ctas_per_sm=0, combine_stage_bytes=0,
-            guard_rows=4, expert=None, plan=None):
+            combine_unroll=0, guard_rows=4, expert=None, plan=None):
     """Run dispatch (+ expert stand-in) + combine on the GPU through the C ABI.
     Returns host copies and the plan.  x is a torch bf16 tensor on the GPU."""
     import torch
@@ -38,7 +38,7 @@ def gpu_run(w: W.Workload, x, idx: np.ndarray, gate: np.ndarray, flags=0, pack_c
         plan = Plan(w.R, w.E, w.T, w.H, w.k, w.window_mode, w.window_rows, device=dev, flags=flags,
                     pack_ctas_per_sm=pack_ctas_per_sm, pack_stage_bytes=pack_stage_bytes,
                     pack_store_lag=pack_store_lag, combine_ctas_per_sm=combine_ctas_per_sm,
-                    combine_stage_bytes=combine_stage_bytes)
+                    combine_stage_bytes=combine_stage_bytes, combine_unroll=combine_unroll)
     rows = plan.arena_rows
     canary = torch.full((rows + guard_rows, w.H), -7.0, dtype=torch.bfloat16, device=dev)
     recv = canary[:rows]

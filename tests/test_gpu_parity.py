@@ -39,6 +39,15 @@ def test_workload_parity_full_hidden(wid):
     P.full_parity(W.WORKLOADS[wid].scaled(T=300))
 
 
+@pytest.mark.parametrize("unroll", [1, 2, 4, 8])
+def test_combine_unroll_variants(unroll):
+    for wid, T, H in [(1, None, None), (4, 300, 1032), (5, 60, 7176)]:
+        w = W.WORKLOADS[wid] if T is None else W.WORKLOADS[wid].scaled(T=T, H=H)
+        g = P.full_parity(w, combine_unroll=unroll)
+        np.testing.assert_array_equal(g["out"], g["ref"]["out"])
+    P.full_parity(_uniform(4, 64, 200, 48, 3), combine_unroll=unroll)
+
+
 @pytest.mark.parametrize("flags", [0, 4], ids=["lsu", "tma"])
 def test_combine_is_bit_exact_against_oracle(flags):
     # The kernels round each product and sum separately in slot order, exactly
