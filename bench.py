@@ -71,6 +71,26 @@ def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(x: float) -> float:
+    """Max of a per-rank float over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job(per_rank_bytes: int, per_rank_tokens: int, ms_max: float, world: int) -> dict:
+    """Whole-job throughput of N independent replicas timed by the slowest rank."""
+    sec = ms_max * 1e-3
+    return {"gbs": per_rank_bytes * world / sec / 1e9, "tokens_per_s": per_rank_tokens * world / sec,
+            "us_per_call": ms_max * 1e3}
+
+
 def read_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -363,11 +383,7 @@ def main():
     t_wall1 = time.time()
     sampler.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = sum(step_ms) / K
-    if world > 1:
-        tt = torch.tensor([ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(sum(step_ms) / K)
     status = plan.read_status()
     if status != 0:
         raise RuntimeError(f"device status word set during the timed region: {status:#x}")
@@ -394,7 +410,8 @@ def main():
 
     # ---- results -------------------------------------------------------------------
     bytes_step = w.algorithmic_bytes()
-    gbs = bytes_step / (ms * 1e-3) / 1e9 * world
+    job = whole_job(bytes_step, w.R * w.T, ms, world)
+    gbs = job["gbs"]
     peak, peak_kind = read_peaks()
     A_ = w.R * w.T * w.k
     # algorithmic bytes per launch: pack reads x once and writes k copies (+ idx
@@ -440,12 +457,8 @@ def main():
             b.synchronize()
             if i >= 3:
                 e2e_ms.append(a.elapsed_time(b))
-    e2e_t = sum(e2e_ms) / len(e2e_ms)
-    if world > 1:
-        tt = torch.tensor([e2e_t], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_t = float(tt.item())
-    e2e = {"value": round(bytes_step / (e2e_t * 1e-3) / 1e9 * world, 2), "unit": "GB/s",
+    e2e_t = max_over_ranks(sum(e2e_ms) / len(e2e_ms))
+    e2e = {"value": round(whole_job(bytes_step, w.R * w.T, e2e_t, world)["gbs"], 2), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_t, 4),
            "path": "pinned host x/idx/gate -> HBM, graph replay, out -> pinned host"}
 
@@ -462,7 +475,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_block(w, f"flushed between steps (read of a {FLUSH_BYTES >> 20} MiB buffer)"),
             "pct_of_peak": round(100 * gbs / world / peak, 2), "peak_gbs": peak,
-            "tokens_per_s": round(w.R * w.T * world / (ms * 1e-3), 1), "us_per_call": round(ms * 1e3, 3),
+            "tokens_per_s": round(job["tokens_per_s"], 1), "us_per_call": round(job["us_per_call"], 3),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(kernels_per_step * K), "kernels_per_step": int(kernels_per_step),
             "clocks": clocks, "variant": {"flags": args.flags, "pack_ctas_per_sm": args.pack_ctas_per_sm,
