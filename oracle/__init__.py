@@ -103,6 +103,8 @@ def _mode(window_mode) -> int:
         return 0
     if window_mode in (1, "fixed"):
         return 1
+    if window_mode in (2, "padded"):
+        return 2
     raise ValueError(window_mode)
 
 
@@ -141,7 +143,8 @@ def slot_map(R: int, E: int, idx: np.ndarray, sp: dict, window_mode="packed", wi
 
 
 def arena_rows(R: int, T: int, k: int, window_mode="packed", window_rows: int = 0) -> int:
-    return R * T * k if _mode(window_mode) == 0 else R * int(window_rows)
+    m = _mode(window_mode)
+    return R * T * k if m == 0 else (R * int(window_rows) if m == 1 else R * R * T * k)
 
 
 def dispatch(R: int, E: int, x: np.ndarray, idx: np.ndarray, sp: dict, window_mode="packed",

@@ -31,6 +31,10 @@
  *       0..R-1 back to back, in source order, with no gaps;
  *   R4  windows: "packed" mode places window d right after window d-1 in one
  *       arena; "fixed" mode gives window d the rows [d*W, (d+1)*W);
+ *       "padded" mode is the worst-case layout a host-side AllToAllv must
+ *       use under graph capture [P1 Inference; P2 3.3]: every (source,
+ *       destination) pair gets T*k rows, so window d starts at d*R*T*k and
+ *       source s's segment inside it at s*T*k;
  *   R5  combine: out = bf16_rne( sum_j w_j * y[slot(t,j)] ), accumulated in
  *       fp32 from 0.0f in slot order j = 0..k-1, each product and each sum
  *       rounded on its own (this file must be built with -ffp-contract=off);
@@ -90,6 +94,8 @@ uint16_t oracle_f32_to_bf16(float f)
  * recv_expert_counts[d][s][le] = send_counts[s][d*(E/R) + le].
  * recv_total[d] = sum over s of recv_counts[d][s].
  * window_base[d] = sum over d' < d of recv_total[d'] (packed) or d*W (fixed).
+ * Padded mode (R4): recv_offsets[d][s] = s*T*k and window_base[d] = d*R*T*k,
+ * the fixed places of the worst-case segments.
  * Returns the status bits.
  */
 uint32_t oracle_splits(int R, int E, int T, int k, int window_mode, int64_t window_rows,
@@ -141,10 +147,16 @@ uint32_t oracle_splits(int R, int E, int T, int k, int window_mode, int64_t wind
     for (int d = 0; d < R; ++d) {
         if (window_mode == 1)
             window_base[d] = (int32_t)((int64_t)d * window_rows);
+        else if (window_mode == 2)
+            window_base[d] = (int32_t)((int64_t)d * R * T * k);
         else
             window_base[d] = (int32_t)base;
         base += recv_total[d];
     }
+    if (window_mode == 2)
+        for (int d = 0; d < R; ++d)
+            for (int s = 0; s < R; ++s)
+                recv_offsets[(size_t)d * R + s] = (int32_t)((int64_t)s * T * k);
     return status;
 }
 

@@ -55,12 +55,21 @@ def brute_force(R, E, idx, window_mode="packed", window_rows=0):
         out["window_base"] = np.array([d * window_rows for d in range(R)])
         if any(len(w) > window_rows for w in windows):
             status |= oracle.WINDOW_OVERFLOW
+    elif window_mode == "padded":
+        # worst case: every (source, destination) pair owns T*k rows
+        out["window_base"] = np.array([d * R * T * k for d in range(R)])
+        out["recv_offsets"] = np.array([[src * T * k for src in range(R)] for _ in range(R)])
     else:
         out["window_base"] = np.array([sum(len(w) for w in windows[:d]) for d in range(R)])
     slot = -np.ones((R, T, k), dtype=np.int64)
     for d, w in enumerate(windows):
         for pos, (s, e, t, j) in enumerate(w):
             if window_mode == "fixed" and pos >= window_rows:
+                continue
+            if window_mode == "padded":
+                # place inside source s's own segment of window d
+                pos = sum(1 for it in w[:pos] if it[0] == s)
+                slot[s, t, j] = d * R * T * k + s * T * k + pos
                 continue
             slot[s, t, j] = out["window_base"][d] + pos
     out["slot_map"] = slot
@@ -156,6 +165,37 @@ def test_fixed_windows_and_overflow_against_brute():
     sm, st = oracle.slot_map(R, E, idx, sp, "fixed", T * k)
     assert st & oracle.WINDOW_OVERFLOW
     assert (sm[0] >= 0).all() and (sm[1:] == -1).all()
+
+
+def test_padded_layout_against_brute():
+    rng = np.random.default_rng(13)
+    for R, E, T, k in [(2, 4, 3, 1), (3, 6, 5, 2), (4, 8, 7, 3)]:
+        for _ in range(15):
+            idx = rng.integers(0, E, size=(R, T, k), dtype=np.int32)
+            check_against_brute(R, E, idx, "padded")
+    # exhaustive on the tiny case
+    for combo in itertools.product(range(4), repeat=4):
+        check_against_brute(2, 4, np.array(combo, np.int32).reshape(2, 2, 1), "padded")
+
+
+def test_padded_and_packed_place_the_same_rows_in_the_same_order():
+    # the two layouts differ only by where each (source, destination) segment
+    # starts; inside a segment the order is the same
+    rng = np.random.default_rng(5)
+    R, E, T, k = 4, 8, 9, 2
+    idx = rng.integers(0, E, size=(R, T, k), dtype=np.int32)
+    a = oracle.splits(R, E, idx)
+    b = oracle.splits(R, E, idx, "padded")
+    sa, _ = oracle.slot_map(R, E, idx, a)
+    sb, _ = oracle.slot_map(R, E, idx, b, "padded")
+    d = idx // (E // R)
+    src = np.arange(R)[:, None, None]
+    rel_a = sa - a["window_base"][d] - a["recv_offsets"][d, src]
+    rel_b = sb - b["window_base"][d] - b["recv_offsets"][d, src]
+    np.testing.assert_array_equal(rel_a, rel_b)
+    assert (rel_b >= 0).all() and (rel_b < T * k).all()
+    for key in ("send_counts", "send_offsets", "recv_counts", "recv_expert_counts", "recv_total"):
+        np.testing.assert_array_equal(a[key], b[key])
 
 
 def test_bad_expert_ids_are_dropped():
@@ -358,6 +398,8 @@ MUTANTS = {
                                       "        base += recv_total[d];\n            window_base[d] = (int32_t)base;"),
     "wrong expert-to-rank map": ("            int d = e / epr;\n            int64_t rel", "            int d = e % R;\n            int64_t rel"),
     "expert scale sign": ("float scale = 1.0f + q;", "float scale = 1.0f - q;"),
+    "padded segments by destination": ("recv_offsets[(size_t)d * R + s] = (int32_t)((int64_t)s * T * k);",
+                                       "recv_offsets[(size_t)d * R + s] = (int32_t)((int64_t)d * T * k);"),
 }
 
 
@@ -372,6 +414,7 @@ def _pin_suite():
     test_scaled_experts_closed_form_numpy_f32()
     test_expert_scale_closed_form_torch()
     test_bf16_rounding_matches_torch()
+    test_padded_layout_against_brute()
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
