@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--mode", choices=["dynamic", "padded"], default="dynamic",
+                    help="padded: the worst-case baseline (every pair sends T*k rows)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="run the workload with this many tokens per rank (small cases for profiling)")
     ap.add_argument("--flags", type=int, default=0,
@@ -294,6 +296,17 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
+    padded = args.mode == "padded"
+    if padded:
+        import dataclasses
+
+        w = dataclasses.replace(w, window_mode="padded", window_rows=0)
+        need = 2 * w.R * w.R * w.T * w.k * w.H * 2 * (2 if args.e2e_steps else 1)
+        free = torch.cuda.mem_get_info(local)[0]
+        if need > 0.9 * free:
+            raise SystemExit(f"padded mode needs {need / 1e9:.0f} GB for its worst-case buffers, "
+                             f"{free / 1e9:.0f} GB free")
+
     # ---- inputs (seeded, synthetic) ----------------------------------------------
     rg = W.make_routing_gate(w, 0)
     idx_h, gate_h = rg["topk_idx"], rg["gate_w"]
@@ -306,6 +319,7 @@ def main():
                   combine_stage_bytes=args.combine_stage_bytes, combine_unroll=args.combine_unroll)
     recv, slot_map, out = plan.new_buffers()
     sp = plan.new_splits()
+    sendbuf = plan.new_send_buffer() if padded else None
     # L2 flush by READING a buffer larger than L2: it evicts our lines and leaves
     # clean ones behind (a write flush would leave ~L2-size dirty lines whose
     # write-back would land inside the next timed step).
@@ -313,36 +327,45 @@ def main():
     flush_out = torch.zeros((), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(dev)
 
-    def path(s):
-        plan.splits(idx, sp, slot_map, stream=s)
-        plan.pack(x, idx, sp, recv, slot_map, stream=s)
-        plan.combine(recv, gate, slot_map, out, stream=s)
+    def make_stages(x_, idx_, gate_, sp_, recv_, slot_, out_, send_):
+        """The path as (name, launch(stream)) stages, in order."""
+        if padded:
+            return [("splits", lambda s: plan.splits(idx_, sp_, slot_, stream=s)),
+                    ("pack", lambda s: plan.pack_padded(x_, idx_, sp_, send_, slot_, stream=s)),
+                    ("exchange", lambda s: plan.exchange_padded(send_, recv_, stream=s)),
+                    ("combine", lambda s: plan.combine(recv_, gate_, slot_, out_, stream=s))]
+        return [("splits", lambda s: plan.splits(idx_, sp_, slot_, stream=s)),
+                ("pack", lambda s: plan.pack(x_, idx_, sp_, recv_, slot_, stream=s)),
+                ("combine", lambda s: plan.combine(recv_, gate_, slot_, out_, stream=s))]
+
+    stages = make_stages(x, idx, gate, sp, recv, slot_map, out, sendbuf)
+
+    def capture(stage_list):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            s_ = torch.cuda.current_stream(dev)
+            for _, fn in stage_list:
+                fn(s_)
+        return g
 
     # warm-up outside capture, then capture the path once
     with torch.cuda.stream(stream):
-        path(stream)
+        for _, fn in stages:
+            fn(stream)
     torch.cuda.synchronize(dev)
     if plan.read_status() != 0:
         raise RuntimeError("device status set during warm-up")
 
-    # The timed graph: the three kernels back to back (pack and combine are
-    # programmatic dependents of their predecessor).
-    graph = torch.cuda.CUDAGraph()
+    # The timed graph: the kernels back to back (each one after the first is a
+    # programmatic dependent of its predecessor).
     launches0 = plan.launches
-    with torch.cuda.graph(graph, stream=stream):
-        path(torch.cuda.current_stream(dev))
+    graph = capture(stages)
     kernels_per_step = plan.launches - launches0
 
-    # Per-kernel timing: nested graphs [splits], [splits, pack] and the full
-    # path; the difference of consecutive ones is the time a kernel adds to the
-    # step (programmatic-launch overlap included).
-    g_splits, g_dispatch = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_splits, stream=stream):
-        plan.splits(idx, sp, slot_map, stream=torch.cuda.current_stream(dev))
-    with torch.cuda.graph(g_dispatch, stream=stream):
-        s_ = torch.cuda.current_stream(dev)
-        plan.splits(idx, sp, slot_map, stream=s_)
-        plan.pack(x, idx, sp, recv, slot_map, stream=s_)
+    # Per-kernel timing: nested graphs holding the first 1, 2, ... stages; the
+    # difference of consecutive ones is the time a kernel adds to the step
+    # (programmatic-launch overlap included).
+    prefixes = [capture(stages[:n]) for n in range(1, len(stages))] + [graph]
 
     def flush_l2():
         torch.sum(flush, dim=0, out=flush_out)
@@ -356,7 +379,7 @@ def main():
     # ---- warm-up -----------------------------------------------------------------
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
-            for gr in (g_splits, g_dispatch, graph):
+            for gr in prefixes:
                 flush_l2()
                 gr.replay()
     torch.cuda.synchronize(dev)
@@ -390,23 +413,23 @@ def main():
 
     # ---- per-kernel durations (same stream, same flush) ------------------------------
     KK = max(1, min(K, args.kernel_steps))
-    nested = {"splits": [], "dispatch": [], "path": []}
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(KK)]
+    timed = prefixes + [g_null]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(timed))] for _ in range(KK)]
     with torch.cuda.stream(stream):
         for i in range(KK):
-            for j, gr in enumerate((g_splits, g_dispatch, graph, g_null)):
+            for j, gr in enumerate(timed):
                 flush_l2()
                 ev[i][2 * j].record(stream)
                 gr.replay()
                 ev[i][2 * j + 1].record(stream)
     torch.cuda.synchronize(dev)
-    nested["null"] = []
-    for i in range(KK):
-        for j, name in enumerate(("splits", "dispatch", "path", "null")):
-            nested[name].append(ev[i][2 * j].elapsed_time(ev[i][2 * j + 1]))
-    mean = {n: sum(v) / len(v) for n, v in nested.items()}
-    kt = {"splits": [mean["splits"]], "pack": [mean["dispatch"] - mean["splits"]],
-          "combine": [mean["path"] - mean["dispatch"]]}
+    prefix_ms = [sum(ev[i][2 * j].elapsed_time(ev[i][2 * j + 1]) for i in range(KK)) / KK for j in range(len(timed))]
+    names = [n for n, _ in stages]
+    mean = {"+".join(names[:j + 1]): prefix_ms[j] for j in range(len(stages))}
+    mean["null"] = prefix_ms[-1]
+    kt = {names[0]: [prefix_ms[0]]}
+    for j in range(1, len(stages)):
+        kt[names[j]] = [prefix_ms[j] - prefix_ms[j - 1]]
 
     # ---- results -------------------------------------------------------------------
     bytes_step = w.algorithmic_bytes()
@@ -416,21 +439,24 @@ def main():
     A_ = w.R * w.T * w.k
     # algorithmic bytes per launch: pack reads x once and writes k copies (+ idx
     # read, slot_map write); combine reads k rows and writes out (+ slot_map and
-    # gate reads).  pack + combine = Workload.algorithmic_bytes().
+    # gate reads).  pack + combine = Workload.algorithmic_bytes().  The padded
+    # baseline's exchange moves every worst-case segment: R*R*T*k rows read and
+    # written.
     kbytes = {
         "splits": 8 * A_,
         "pack": w.R * w.T * w.H * 2 * (1 + w.k) + 8 * A_,
+        "exchange": 2 * w.R * A_ * w.H * 2,
         "combine": w.R * w.T * w.H * 2 * (1 + w.k) + 8 * A_,
     }
     kus = {n: 1e3 * sum(v) / len(v) for n, v in kt.items() if v}
-    dom = max(("pack", "combine"), key=lambda n: kus.get(n, 0.0))
+    dom = max((n for n in names if n != "splits"), key=lambda n: kus.get(n, 0.0))
     ach = kbytes[dom] / (kus[dom] * 1e-6) / 1e9
-    traffic = ncu_traffic(dom, w.name)
+    traffic = None if padded else ncu_traffic(dom, w.name)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
                 "kernel_us": {n: round(v, 3) for n, v in kus.items()},
                 "kernel_gbs": {n: round(kbytes[n] / (kus[n] * 1e-6) / 1e9, 1) for n in kus},
-                "timing": (f"marginal: nested graphs [splits], [splits,pack], [splits,pack,combine], "
+                "timing": (f"marginal: nested graphs of the first 1..{len(stages)} kernels, "
                            f"{KK} steps each, L2 flushed before each replay"),
                 "nested_us": {n: round(1e3 * v, 3) for n, v in mean.items()}}
 
@@ -469,13 +495,9 @@ def main():
     idx2, gate2 = torch.empty_like(idx), torch.empty_like(gate)
     recv2, slot_map2, out2 = plan.new_buffers()
     sp2 = plan.new_splits()
+    send2 = plan.new_send_buffer() if padded else None
     sets = [(x, idx, gate, recv, slot_map, out, sp, graph)]
-    g2 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g2, stream=stream):
-        s_ = torch.cuda.current_stream(dev)
-        plan.splits(idx2, sp2, slot_map2, stream=s_)
-        plan.pack(x2, idx2, sp2, recv2, slot_map2, stream=s_)
-        plan.combine(recv2, gate2, slot_map2, out2, stream=s_)
+    g2 = capture(make_stages(x2, idx2, gate2, sp2, recv2, slot_map2, out2, send2))
     sets.append((x2, idx2, gate2, recv2, slot_map2, out2, sp2, g2))
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]
@@ -529,7 +551,7 @@ def main():
     clocks = sampler.summary(t_wall0, t_wall1)
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not padded:
         cpu = cpu_baseline(w, W.bf16_bits(x), idx_h, gate_h, args.cpu_seconds)
 
     if rank == 0:
@@ -538,6 +560,7 @@ def main():
             "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_block(w, f"flushed between steps (read of a {FLUSH_BYTES >> 20} MiB buffer)"),
+            "mode": args.mode,
             "pct_of_peak": round(100 * gbs / world / peak, 2), "peak_gbs": peak,
             "tokens_per_s": round(job["tokens_per_s"], 1), "us_per_call": round(job["us_per_call"], 3),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,

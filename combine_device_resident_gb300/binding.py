@@ -25,6 +25,7 @@ DEV_WAIT_TIMEOUT = 1 << 31
 
 WINDOW_PACKED = 0
 WINDOW_FIXED = 1
+WINDOW_PADDED = 2
 FLAG_PACK_LSU = 1 << 0
 FLAG_SPLITS_TILED = 1 << 1
 FLAG_COMBINE_TMA = 1 << 2
@@ -35,6 +36,7 @@ EXPORTED = [
     "a2av_dispatch", "a2av_splits", "a2av_pack", "a2av_combine", "a2av_expert_scale",
     "a2av_read_device_status", "a2av_device_status_ptr", "a2av_plan_launches",
     "a2av_status_string", "a2av_last_error", "a2av_dispatch_static",
+    "a2av_dispatch_padded", "a2av_pack_padded", "a2av_exchange_padded",
 ]
 
 
@@ -117,6 +119,12 @@ def load_library(path: Optional[str] = None):
     L.a2av_last_error.restype = ctypes.c_char_p
     L.a2av_dispatch_static.argtypes = [cfgp, vp, vp, spp, vp, vp, vp, vp]
     L.a2av_dispatch_static.restype = i32
+    L.a2av_dispatch_padded.argtypes = [vp, vp, vp, spp, vp, vp, vp, vp]
+    L.a2av_dispatch_padded.restype = i32
+    L.a2av_pack_padded.argtypes = [vp, vp, vp, spp, vp, vp, vp]
+    L.a2av_pack_padded.restype = i32
+    L.a2av_exchange_padded.argtypes = [vp, vp, vp, vp]
+    L.a2av_exchange_padded.restype = i32
     if path is None:
         _lib = L
     return L
@@ -132,7 +140,7 @@ def _check(L, rc: int, what: str):
 def make_config(R, E, T, H, k, window_mode="packed", window_rows=0, device=0, flags=0,
                 pack_ctas_per_sm=0, pack_stage_bytes=0, pack_store_lag=0, combine_ctas_per_sm=0,
                 combine_stage_bytes=0, combine_unroll=0) -> Config:
-    mode = {"packed": WINDOW_PACKED, "fixed": WINDOW_FIXED}.get(window_mode, window_mode)
+    mode = {"packed": WINDOW_PACKED, "fixed": WINDOW_FIXED, "padded": WINDOW_PADDED}.get(window_mode, window_mode)
     return Config(int(R), int(E), int(T), int(H), int(k), int(mode), int(window_rows), int(device),
                   int(flags), int(pack_ctas_per_sm), int(pack_stage_bytes), int(pack_store_lag),
                   int(combine_ctas_per_sm), int(combine_stage_bytes), int(combine_unroll))
@@ -265,6 +273,36 @@ class Plan:
             self._t(topk_idx, torch.int32, (self.R, self.T, self.k), "topk_idx"), ctypes.byref(splits.ptrs),
             self._rows(recv, "recv"), self._t(slot_map, torch.int32, (self.R, self.T, self.k), "slot_map"),
             _stream_ptr(stream, self.device)), "a2av_pack")
+
+    def new_send_buffer(self):
+        """Padded plans: the worst-case send buffer, bf16 [R*R*T*k][H] (uninitialised)."""
+        import torch
+
+        return torch.empty((self.arena_rows, self.H), dtype=torch.bfloat16, device=self.device)
+
+    def dispatch_padded(self, x, topk_idx, splits: Splits, sendbuf, recv, slot_map, stream=None):
+        import torch
+
+        _check(self.lib, self.lib.a2av_dispatch_padded(
+            self.handle, self._t(x, torch.bfloat16, (self.R, self.T, self.H), "x"),
+            self._t(topk_idx, torch.int32, (self.R, self.T, self.k), "topk_idx"), ctypes.byref(splits.ptrs),
+            self._rows(sendbuf, "sendbuf"), self._rows(recv, "recv"),
+            self._t(slot_map, torch.int32, (self.R, self.T, self.k), "slot_map"),
+            _stream_ptr(stream, self.device)), "a2av_dispatch_padded")
+
+    def pack_padded(self, x, topk_idx, splits: Splits, sendbuf, slot_map, stream=None):
+        import torch
+
+        _check(self.lib, self.lib.a2av_pack_padded(
+            self.handle, self._t(x, torch.bfloat16, (self.R, self.T, self.H), "x"),
+            self._t(topk_idx, torch.int32, (self.R, self.T, self.k), "topk_idx"), ctypes.byref(splits.ptrs),
+            self._rows(sendbuf, "sendbuf"), self._t(slot_map, torch.int32, (self.R, self.T, self.k), "slot_map"),
+            _stream_ptr(stream, self.device)), "a2av_pack_padded")
+
+    def exchange_padded(self, sendbuf, recv, stream=None):
+        _check(self.lib, self.lib.a2av_exchange_padded(
+            self.handle, self._rows(sendbuf, "sendbuf"), self._rows(recv, "recv"),
+            _stream_ptr(stream, self.device)), "a2av_exchange_padded")
 
     def combine(self, y, gate_w, slot_map, out, stream=None):
         import torch

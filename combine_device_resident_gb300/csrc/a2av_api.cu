@@ -76,6 +76,8 @@ a2av_status_t a2av_config_check(const a2av_config_t *c) {
     if ((long long)c->tokens_per_rank * c->topk >= (1ll << 31) - a2av::kHistTile) return A2AV_ERR_INVALID_ARG;
     if (c->window_mode == A2AV_WINDOW_FIXED) {
         if (c->window_rows < 0 || (long long)c->num_ranks * c->window_rows >= (1ll << 31)) return A2AV_ERR_INVALID_ARG;
+    } else if (c->window_mode == A2AV_WINDOW_PADDED) {
+        if (assignments * c->num_ranks >= (1ll << 31)) return A2AV_ERR_INVALID_ARG;
     } else if (c->window_mode != A2AV_WINDOW_PACKED) {
         return A2AV_ERR_INVALID_ARG;
     }
@@ -96,6 +98,8 @@ a2av_status_t a2av_config_check(const a2av_config_t *c) {
 int64_t a2av_recv_arena_rows(const a2av_config_t *c) {
     if (a2av_config_check(c) != A2AV_OK) return -1;
     if (c->window_mode == A2AV_WINDOW_FIXED) return (int64_t)c->num_ranks * c->window_rows;
+    if (c->window_mode == A2AV_WINDOW_PADDED)
+        return (int64_t)c->num_ranks * c->num_ranks * c->tokens_per_rank * c->topk;
     return (int64_t)c->num_ranks * c->tokens_per_rank * c->topk;
 }
 
@@ -192,9 +196,30 @@ a2av_status_t a2av_splits(a2av_plan_t p, const int32_t *topk_idx, const a2av_spl
     return A2AV_OK;
 }
 
+static a2av_status_t pack_into(a2av_plan_t p, const void *x, const int32_t *topk_idx, const a2av_splits_t *splits,
+                               void *dst, int32_t *slot_map, void *stream, bool padded);
+
 a2av_status_t a2av_pack(a2av_plan_t p, const void *x, const int32_t *topk_idx, const a2av_splits_t *splits,
                         void *recv, int32_t *slot_map, void *stream) {
-    if (!p || !aligned(x, 16) || !aligned(recv, 16) || !aligned(topk_idx, 4) || !aligned(slot_map, 4) ||
+    if (!p || p->cfg.window_mode == A2AV_WINDOW_PADDED) {
+        a2av::set_last_error("a2av_pack: padded plans use a2av_pack_padded");
+        return A2AV_ERR_INVALID_ARG;
+    }
+    return pack_into(p, x, topk_idx, splits, recv, slot_map, stream, false);
+}
+
+a2av_status_t a2av_pack_padded(a2av_plan_t p, const void *x, const int32_t *topk_idx, const a2av_splits_t *splits,
+                               void *sendbuf, int32_t *slot_map, void *stream) {
+    if (!p || p->cfg.window_mode != A2AV_WINDOW_PADDED) {
+        a2av::set_last_error("a2av_pack_padded: the plan is not padded");
+        return A2AV_ERR_INVALID_ARG;
+    }
+    return pack_into(p, x, topk_idx, splits, sendbuf, slot_map, stream, true);
+}
+
+static a2av_status_t pack_into(a2av_plan_t p, const void *x, const int32_t *topk_idx, const a2av_splits_t *splits,
+                               void *recv, int32_t *slot_map, void *stream, bool padded) {
+    if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(topk_idx, 4) || !aligned(slot_map, 4) ||
         !splits_ok(splits))
         return A2AV_ERR_INVALID_ARG;
     const int64_t rows = a2av_recv_arena_rows(&p->cfg);
@@ -213,14 +238,51 @@ a2av_status_t a2av_pack(a2av_plan_t p, const void *x, const int32_t *topk_idx, c
     a.window_base = splits->window_base;
     a.recv = static_cast<uint16_t *>(recv);
     a.status = p->status;
+    a.padded_tk = padded ? (int64_t)p->g.T * p->g.k : 0;
     cudaError_t e = a2av::launch_pack(*p, a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "pack kernel launch");
     p->launches += 1;
     return A2AV_OK;
 }
 
+a2av_status_t a2av_exchange_padded(a2av_plan_t p, const void *sendbuf, void *recv, void *stream) {
+    if (!p || p->cfg.window_mode != A2AV_WINDOW_PADDED || !aligned(sendbuf, 16) || !aligned(recv, 16))
+        return A2AV_ERR_INVALID_ARG;
+    const size_t bytes = (size_t)a2av_recv_arena_rows(&p->cfg) * row_bytes(p);
+    if (overlap(sendbuf, bytes, recv, bytes)) return A2AV_ERR_INVALID_ARG;
+    DeviceGuard guard(p->cfg.device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    a2av::ExchangeArgs a;
+    a.sendbuf = static_cast<const uint16_t *>(sendbuf);
+    a.recv = static_cast<uint16_t *>(recv);
+    a.R = p->g.R;
+    a.block_vecs = (int64_t)p->g.T * p->g.k * (p->g.H / 8);
+    cudaError_t e = a2av::launch_exchange_padded(*p, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "padded exchange kernel launch");
+    p->launches += 1;
+    return A2AV_OK;
+}
+
+a2av_status_t a2av_dispatch_padded(a2av_plan_t p, const void *x, const int32_t *topk_idx,
+                                   const a2av_splits_t *splits, void *sendbuf, void *recv, int32_t *slot_map,
+                                   void *stream) {
+    if (!p || p->cfg.window_mode != A2AV_WINDOW_PADDED || !aligned(sendbuf, 16) || !aligned(recv, 16))
+        return A2AV_ERR_INVALID_ARG;
+    const size_t bytes = (size_t)a2av_recv_arena_rows(&p->cfg) * row_bytes(p);
+    if (overlap(x, tokens(p) * row_bytes(p), recv, bytes) || overlap(sendbuf, bytes, recv, bytes))
+        return A2AV_ERR_INVALID_ARG;
+    a2av_status_t st = a2av_splits(p, topk_idx, splits, slot_map, stream);
+    if (st == A2AV_OK) st = a2av_pack_padded(p, x, topk_idx, splits, sendbuf, slot_map, stream);
+    if (st == A2AV_OK) st = a2av_exchange_padded(p, sendbuf, recv, stream);
+    return st;
+}
+
 a2av_status_t a2av_dispatch(a2av_plan_t p, const void *x, const int32_t *topk_idx, const a2av_splits_t *splits,
                             void *recv, int32_t *slot_map, void *stream) {
+    if (p && p->cfg.window_mode == A2AV_WINDOW_PADDED) {
+        a2av::set_last_error("a2av_dispatch: padded plans use a2av_dispatch_padded");
+        return A2AV_ERR_INVALID_ARG;
+    }
     if (!p || !aligned(x, 16) || !aligned(recv, 16) || !aligned(topk_idx, 4) || !aligned(slot_map, 4) ||
         !splits_ok(splits))
         return A2AV_ERR_INVALID_ARG;

@@ -65,6 +65,14 @@ struct PackArgs {
     int32_t stages;
     int32_t rows_final;   // 1: slot_map already holds final rows (single-CTA splits)
     int32_t lag;          // store groups allowed to read a stage before it is refilled
+    int64_t padded_tk;    // padded plans: T*k, and `recv` is the padded send buffer
+};
+
+struct ExchangeArgs {
+    const uint16_t *sendbuf;
+    uint16_t *recv;
+    int32_t R;
+    int64_t block_vecs;  // 16-byte vectors per (source, destination) segment: T*k*H/8
 };
 
 struct CombineArgs {
@@ -115,7 +123,7 @@ struct a2av_plan_s {
     int32_t *rank_total = nullptr;
     uint32_t *counters = nullptr;
     uint32_t *status = nullptr;
-    a2av::LaunchShape hist, pack, combine, scale;
+    a2av::LaunchShape hist, pack, combine, scale, exchange;
     int splits_small = 0;  // 1: one-CTA splits kernel that writes final rows
     int combine_tma = 1;
     int32_t comb_chunk_bytes = 0, comb_nchunks = 0, comb_stages = 0, comb_nsplit = 1, comb_unroll = 2;
@@ -148,6 +156,7 @@ cudaError_t launch_hist(const a2av_plan_s &p, const HistArgs &a, cudaStream_t s)
 cudaError_t launch_pack(const a2av_plan_s &p, const PackArgs &a, cudaStream_t s);
 cudaError_t launch_combine(const a2av_plan_s &p, const CombineArgs &a, cudaStream_t s);
 cudaError_t launch_scale(const a2av_plan_s &p, const ScaleArgs &a, cudaStream_t s);
+cudaError_t launch_exchange_padded(const a2av_plan_s &p, const ExchangeArgs &a, cudaStream_t s);
 
 // Records the text a2av_last_error() returns on the calling thread.
 void set_last_error(const char *msg);

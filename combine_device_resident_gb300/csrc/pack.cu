@@ -27,7 +27,22 @@ namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
 __device__ __forceinline__ long long arena_rows_of(const Geometry &g) {
-    return g.window_mode == A2AV_WINDOW_FIXED ? (long long)g.R * g.window_rows : (long long)g.R * g.T * g.k;
+    const long long tk = (long long)g.T * g.k;
+    return g.window_mode == A2AV_WINDOW_FIXED ? (long long)g.R * g.window_rows
+           : g.window_mode == A2AV_WINDOW_PADDED ? (long long)g.R * g.R * tk
+                                                  : (long long)g.R * tk;
+}
+
+// Padded plans store into the padded send buffer: the row a receive-side
+// (window d, segment s, position p) row came from, (s*R + d)*T*k + p; -1 if
+// the row does not lie in source s's segment (never for rows the splits
+// kernel produced; the store is then skipped).
+__device__ __forceinline__ long long send_row_of(const PackArgs &a, long long row, int s) {
+    const long long tk = a.padded_tk, window = (long long)a.g.R * tk;
+    const long long d = row / window;
+    const long long p = row - d * window - (long long)s * tk;
+    if (p < 0 || p >= tk) return -1;
+    return ((long long)s * a.g.R + d) * tk + p;
 }
 
 // Final arena row of assignment j of flat token `tok`, or -1 if dropped.  With
@@ -56,6 +71,7 @@ __device__ __forceinline__ int32_t final_row(const PackArgs &a, long long tok, i
                           __ldg(a.send_offsets + (size_t)s * g.E + (size_t)d * g.epr) +
                           __ldg(a.tile_base + ((size_t)s * g.tiles + tl) * g.E + e) + r;
     const long long cap = g.window_mode == A2AV_WINDOW_FIXED ? g.window_rows : (long long)g.R * g.T * g.k;
+    // (packed: a window holds at most R*T*k rows; padded: a window is R*T*k rows)
     if (rel < 0 || rel >= cap) {
         ovf = 1;
         return -1;
@@ -150,9 +166,13 @@ __global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
         const uint32_t bytes = (uint32_t)min((size_t)CH, rowb - off);
         const int lb = (int)(tok - batch_tok0);
         if (lane == 0) fence_proxy_async_smem();
+        const int s_tok = (int)(tok / g.T);
         for (int j = 0; j < g.k; ++j) {
             const int32_t rj = __shfl_sync(kFull, cur, lb * g.k + j);
-            if (lane == 0 && rj >= 0) bulk_store(recv + (size_t)rj * rowb + off, smem + (size_t)st * CH, bytes);
+            if (lane == 0 && rj >= 0) {
+                const long long dst = a.padded_tk ? send_row_of(a, rj, s_tok) : (long long)rj;
+                if (dst >= 0) bulk_store(recv + (size_t)dst * rowb + off, smem + (size_t)st * CH, bytes);
+            }
         }
         if (lane == 0) {
             bulk_commit();
@@ -203,7 +223,9 @@ __global__ void __launch_bounds__(256) pack_lsu_kernel(const PackArgs a) {
             for (int j = 0; j < g.k; ++j) {
                 const int32_t rj = __shfl_sync(kFull, row, j);
                 if (rj < 0) continue;
-                char *dst = reinterpret_cast<char *>(a.recv) + (size_t)rj * rowb;
+                const long long drow = a.padded_tk ? send_row_of(a, rj, (int)(u / g.T)) : (long long)rj;
+                if (drow < 0) continue;
+                char *dst = reinterpret_cast<char *>(a.recv) + (size_t)drow * rowb;
 #pragma unroll
                 for (int q = 0; q < U; ++q) {
                     const int v = vb + q * 32 + lane;
@@ -222,8 +244,47 @@ constexpr int kDefaultLag = 2;
 
 }  // namespace
 
+namespace {
+// The fixed-size AllToAll of the padded baseline: every (source s,
+// destination d) segment of T*k rows, padding included, from the send buffer
+// at (s*R + d) to the receive arena at (d*R + s).  16-byte vectors, four in
+// flight per thread, grid-stride over the whole arena.
+__global__ void __launch_bounds__(256) exchange_padded_kernel(const ExchangeArgs a) {
+    grid_dependency_wait();
+    const long long total = (long long)a.R * a.R * a.block_vecs;
+    const long long nthr = (long long)gridDim.x * blockDim.x;
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.sendbuf);
+    uint4 *dst = reinterpret_cast<uint4 *>(a.recv);
+    for (long long v0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; v0 < total; v0 += 4 * nthr) {
+        uint4 buf[4];
+        long long from[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const long long v = v0 + q * nthr;
+            from[q] = -1;
+            if (v < total) {
+                const long long blk = v / a.block_vecs, in = v - blk * a.block_vecs;
+                const long long d = blk / a.R, s = blk - d * a.R;
+                from[q] = (s * a.R + d) * a.block_vecs + in;
+                buf[q] = ld_stream_v4(src + from[q]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (from[q] >= 0) st_v4(dst + v0 + q * nthr, buf[q]);
+    }
+}
+}  // namespace
+
 cudaError_t configure_pack(a2av_plan_s &p) {
     const size_t rowb = (size_t)p.g.H * 2;
+    {
+        int per_sm = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, exchange_padded_kernel, 256, 0);
+        if (e != cudaSuccess) return e;
+        p.exchange.grid = p.num_sms * (per_sm > 0 ? per_sm : 1);
+        p.exchange.block = 256;
+    }
     if (!p.pack_tma) {
         p.pack.block = 256;
         int per_sm = 0;
@@ -263,6 +324,12 @@ cudaError_t configure_pack(a2av_plan_s &p) {
     // The attribute is a per-kernel cap shared by every plan: raise it to the
     // device maximum (never lower it to this plan's size).
     return cudaFuncSetAttribute(pack_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
+}
+
+
+cudaError_t launch_exchange_padded(const a2av_plan_s &p, const ExchangeArgs &a, cudaStream_t s) {
+    cudaError_t e = launch_pdl(exchange_padded_kernel, p.exchange.grid, 256, 0, s, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_pack(const a2av_plan_s &p, const PackArgs &a, cudaStream_t s) {

@@ -228,7 +228,8 @@ __global__ void __launch_bounds__(kHistThreads) hist_scan_kernel(const HistArgs 
             const int incl = warp_inclusive_scan(v, lane);
             if (src < R) {
                 a.sp.recv_counts[d * R + src] = v;
-                a.sp.recv_offsets[d * R + src] = carry + incl - v;
+                a.sp.recv_offsets[d * R + src] =
+                    g.window_mode == A2AV_WINDOW_PADDED ? (int)((long long)src * g.T * g.k) : carry + incl - v;
             }
             carry += __shfl_sync(kFull, incl, 31);
         }
@@ -246,7 +247,10 @@ __global__ void __launch_bounds__(kHistThreads) hist_scan_kernel(const HistArgs 
             const int d = c0 + lane;
             const int v = d < R ? wt[d] : 0;
             const int incl = warp_inclusive_scan(v, lane);
-            if (d < R) a.sp.window_base[d] = fixed ? (int)((long long)d * g.window_rows) : carry + incl - v;
+            if (d < R)
+                a.sp.window_base[d] = fixed ? (int)((long long)d * g.window_rows)
+                                    : g.window_mode == A2AV_WINDOW_PADDED ? (int)((long long)d * R * g.T * g.k)
+                                                                           : carry + incl - v;
             ovf |= fixed && d < R && v > g.window_rows;
             carry += __shfl_sync(kFull, incl, 31);
         }
@@ -362,9 +366,10 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
         const int v = lane < R ? rc[d * R + lane] : 0;
         const int incl = warp_inclusive_scan(v, lane);
         if (lane == s) {
-            ro[d] = incl - v;
+            const int off = g.window_mode == A2AV_WINDOW_PADDED ? (int)((long long)s * g.T * g.k) : incl - v;
+            ro[d] = off;
             a.sp.recv_counts[d * R + s] = v;
-            a.sp.recv_offsets[d * R + s] = incl - v;
+            a.sp.recv_offsets[d * R + s] = off;
         }
         if (lane == 31) {
             wb[d] = incl;
@@ -376,7 +381,9 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
         const int v = lane < R ? wb[lane] : 0;
         const int incl = warp_inclusive_scan(v, lane);
         const bool fixed = g.window_mode == A2AV_WINDOW_FIXED;
-        const long long base = fixed ? (long long)lane * g.window_rows : (long long)(incl - v);
+        const long long base = fixed ? (long long)lane * g.window_rows
+                               : g.window_mode == A2AV_WINDOW_PADDED ? (long long)lane * R * g.T * g.k
+                                                                      : (long long)(incl - v);
         const bool ovf = fixed && lane < R && v > g.window_rows;
         if (s == 0 && __any_sync(kFull, ovf) && lane == 0) atomicOr(a.status, (uint32_t)A2AV_DEV_WINDOW_OVERFLOW);
         __syncwarp();

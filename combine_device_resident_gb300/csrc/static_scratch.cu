@@ -54,8 +54,8 @@ bool aligned(const void *p, size_t a) { return p != nullptr && (reinterpret_cast
 extern "C" a2av_status_t a2av_dispatch_static(const a2av_config_t *cfg, const void *x, const int32_t *topk_idx,
                                               const a2av_splits_t *splits, void *recv, int32_t *slot_map,
                                               uint32_t *dev_status, void *stream) {
-    if (a2av_config_check(cfg) != A2AV_OK) {
-        a2av::set_last_error("a2av_dispatch_static: invalid configuration");
+    if (a2av_config_check(cfg) != A2AV_OK || cfg->window_mode == A2AV_WINDOW_PADDED) {
+        a2av::set_last_error("a2av_dispatch_static: invalid configuration (padded plans need a send buffer)");
         return A2AV_ERR_INVALID_ARG;
     }
     if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(topk_idx, 4) || !aligned(slot_map, 4) ||

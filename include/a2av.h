@@ -93,6 +93,9 @@ enum {
 enum {
     A2AV_WINDOW_PACKED = 0, /* window d starts right after window d-1: arena of exactly R*T*k rows */
     A2AV_WINDOW_FIXED = 1,  /* window d owns rows [d*window_rows, (d+1)*window_rows) */
+    A2AV_WINDOW_PADDED = 2, /* worst-case layout of a host-side AllToAllv under graph capture: every
+                               (source s, destination d) pair owns T*k rows at (d*R + s)*T*k; the
+                               padded baseline the dynamic collective is compared with */
 };
 
 /* Variant flags (a2av_config_t.flags). */
@@ -108,7 +111,7 @@ typedef struct {
     int32_t tokens_per_rank; /* T >= 1; R*T*k < 2^31 */
     int32_t hidden;          /* H, a multiple of 8, >= 8 */
     int32_t topk;            /* k, 1..32 */
-    int32_t window_mode;     /* A2AV_WINDOW_PACKED or A2AV_WINDOW_FIXED */
+    int32_t window_mode;     /* A2AV_WINDOW_PACKED, A2AV_WINDOW_FIXED or A2AV_WINDOW_PADDED */
     int64_t window_rows;     /* fixed mode: rows per window (R*window_rows < 2^31); ignored when packed */
     int32_t device;          /* CUDA device ordinal the plan and all its tensors live on */
     uint32_t flags;          /* A2AV_FLAG_* */
@@ -139,8 +142,8 @@ typedef struct {
 /* Host-only check of a configuration against the limits above; touches no GPU. */
 a2av_status_t a2av_config_check(const a2av_config_t *cfg);
 
-/* Rows the recv arena needs: R*T*k (packed) or R*window_rows (fixed); -1 for
- * an invalid configuration.  Host-only. */
+/* Rows the recv arena needs: R*T*k (packed), R*window_rows (fixed) or
+ * R*R*T*k (padded); -1 for an invalid configuration.  Host-only. */
 int64_t a2av_recv_arena_rows(const a2av_config_t *cfg);
 
 /* Create a plan: validates `cfg`, allocates the plan's small device
@@ -217,6 +220,30 @@ a2av_status_t a2av_expert_scale(a2av_plan_t plan, const void *recv, const int32_
 a2av_status_t a2av_dispatch_static(const a2av_config_t *cfg, const void *x, const int32_t *topk_idx,
                                    const a2av_splits_t *splits, void *recv, int32_t *slot_map,
                                    uint32_t *dev_status, void *stream);
+
+/* The padded baseline (plans with window_mode A2AV_WINDOW_PADDED): what an
+ * AllToAllv whose counts are frozen at graph capture has to do.  The counts
+ * cannot be trusted when the collective runs, so every source sends the
+ * worst case -- every token to one expert, T*k rows -- to every destination
+ * and most of what moves is padding [Inference section; digest 3.3; the
+ * deep dive, Figure 15].  Three steps on `stream`:
+ *   a2av_splits          counts and scans as usual; recv_offsets[d][s] = s*T*k,
+ *                        window_base[d] = d*R*T*k; slot_map gets the padded rows
+ *   a2av_pack_padded     the sort into the send buffer: sendbuf[(s*R + d)*T*k + p]
+ *                        = the p-th row rank s sends to d (expert order); rows past
+ *                        the real count are left as they are (padding)
+ *   a2av_exchange_padded the fixed-size AllToAll: for every (s, d) all T*k rows of
+ *                        sendbuf's segment (s, d) go to recv's segment (d, s),
+ *                        padding included
+ * sendbuf and recv are bf16 [R*R*T*k][H] (a2av_recv_arena_rows), distinct and
+ * disjoint from x.  a2av_combine then works unchanged.  a2av_dispatch and
+ * a2av_pack reject padded plans. */
+a2av_status_t a2av_dispatch_padded(a2av_plan_t plan, const void *x, const int32_t *topk_idx,
+                                   const a2av_splits_t *splits, void *sendbuf, void *recv, int32_t *slot_map,
+                                   void *stream);
+a2av_status_t a2av_pack_padded(a2av_plan_t plan, const void *x, const int32_t *topk_idx,
+                               const a2av_splits_t *splits, void *sendbuf, int32_t *slot_map, void *stream);
+a2av_status_t a2av_exchange_padded(a2av_plan_t plan, const void *sendbuf, void *recv, void *stream);
 
 /* Copy the device status word to *bits (synchronises `stream`); if `clear`,
  * reset it to 0 afterwards.  Not capturable. */

@@ -48,7 +48,11 @@ def gpu_run(w: W.Workload, x, idx: np.ndarray, gate: np.ndarray, flags=0, pack_c
     idx_t = torch.from_numpy(idx).to(dev)
     gate_t = torch.from_numpy(gate).to(dev)
     plan.read_status(clear=True)
-    plan.dispatch(x, idx_t, sp, recv, slot_map)
+    if w.window_mode == "padded":
+        sendbuf = plan.new_send_buffer()
+        plan.dispatch_padded(x, idx_t, sp, sendbuf, recv, slot_map)
+    else:
+        plan.dispatch(x, idx_t, sp, recv, slot_map)
     expert = expert or w.expert
     if expert == "scale":
         y = torch.empty_like(recv)

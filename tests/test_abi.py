@@ -56,9 +56,10 @@ def _cfg(**kw):
 
 def test_config_check_host_only(lib):
     ok = [_cfg(), _cfg(R=1, E=1, T=1, H=8, k=1), _cfg(R=64, E=2048, T=3, H=8, k=32),
-          _cfg(window_mode="fixed", window_rows=100)]
+          _cfg(window_mode="fixed", window_rows=100), _cfg(window_mode="padded")]
     bad = [_cfg(R=0), _cfg(R=65, E=130), _cfg(E=12, R=8), _cfg(E=4096, R=8), _cfg(H=12), _cfg(H=0), _cfg(k=0),
-           _cfg(k=33), _cfg(T=0), _cfg(window_mode=2), _cfg(window_mode="fixed", window_rows=-1),
+           _cfg(k=33), _cfg(T=0), _cfg(window_mode=3), _cfg(window_mode="fixed", window_rows=-1),
+           _cfg(R=64, E=64, T=65536, k=8, window_mode="padded"),
            _cfg(R=64, E=64, T=1 << 20, k=32), _cfg(flags=1 << 7), _cfg(flags=1 << 3), _cfg(pack_stage_bytes=24),
            _cfg(pack_ctas_per_sm=9)]
     for c in ok:
@@ -72,6 +73,7 @@ def test_arena_rows(lib):
     assert lib.a2av_recv_arena_rows(ctypes.byref(_cfg(R=32, E=256, T=2048, k=8))) == 32 * 2048 * 8
     assert lib.a2av_recv_arena_rows(ctypes.byref(_cfg(window_mode="fixed", window_rows=2048))) == 8 * 2048
     assert lib.a2av_recv_arena_rows(ctypes.byref(_cfg(H=7))) == -1
+    assert lib.a2av_recv_arena_rows(ctypes.byref(_cfg(window_mode="padded"))) == 8 * 8 * 1024
 
 
 def test_plan_create_rejects_bad_config_without_touching_a_gpu(lib):

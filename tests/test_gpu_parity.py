@@ -238,3 +238,62 @@ def test_plans_with_different_shapes_coexist():
     P.full_parity(small)
     P.full_parity(big, x=xb, idx=rgb["topk_idx"], gate=rgb["gate_w"])
     P.gpu_run(big, xb, rgb["topk_idx"], rgb["gate_w"], plan=gbig["plan"])
+
+
+# ---------------------------------------------------------------------------
+# padded baseline (worst-case segments, fixed-size exchange)
+# ---------------------------------------------------------------------------
+def _padded(w):
+    import dataclasses
+
+    return dataclasses.replace(w, window_mode="padded", window_rows=0, name=w.name + "-padded")
+
+
+@pytest.mark.parametrize("wid,T,H", [(1, None, None), (2, 1100, 264), (3, 300, 136), (4, 700, 72), (5, 40, 64)])
+def test_padded_parity_and_same_output_as_dynamic(wid, T, H):
+    w = W.WORKLOADS[wid] if T is None else W.WORKLOADS[wid].scaled(T=T, H=H)
+    import dataclasses
+
+    w = dataclasses.replace(w, window_mode="packed", window_rows=0)
+    x = W.make_x(w, 0, device=P.device())
+    rg = W.make_routing_gate(w, 0)
+    dyn = P.full_parity(w, x=x, idx=rg["topk_idx"], gate=rg["gate_w"])
+    pad = P.full_parity(_padded(w), x=x, idx=rg["topk_idx"], gate=rg["gate_w"])
+    np.testing.assert_array_equal(pad["out"], dyn["out"])
+    # same counts; padded offsets are the fixed segment starts
+    for key in ("send_counts", "send_offsets", "recv_counts", "recv_expert_counts", "recv_total"):
+        np.testing.assert_array_equal(pad["splits"][key], dyn["splits"][key])
+    assert pad["splits"]["window_base"].tolist() == [d * w.R * w.T * w.k for d in range(w.R)]
+
+
+@pytest.mark.parametrize("flags", [1, 2, 3], ids=["lsu", "tiled", "tiled-lsu"])
+def test_padded_variants(flags):
+    P.full_parity(_padded(W.WORKLOADS[4].scaled(T=1500, H=136)), flags=flags)
+    P.full_parity(_padded(W.WORKLOADS[2].scaled(T=300, H=520)), flags=flags)
+
+
+def test_padded_edge_cases():
+    import combine_device_resident_gb300 as A
+
+    w = _padded(_uniform(4, 8, 900, 24, 1))
+    idx = np.full((w.R, w.T, 1), 3, np.int32)  # the worst case itself: every token to one expert
+    g = P.full_parity(w, idx=idx, gate=np.ones_like(idx, np.float32))
+    assert g["splits"]["recv_total"].tolist() == [0, w.R * w.T, 0, 0]
+    rg = W.make_routing_gate(w, 1)
+    bad = rg["topk_idx"].copy()
+    bad[1, 5, 0] = -1
+    g = P.full_parity(w, idx=bad, gate=rg["gate_w"])
+    assert g["status"] & A.DEV_BAD_EXPERT
+
+
+def test_padded_plan_rejects_dynamic_calls():
+    import torch
+    import combine_device_resident_gb300 as A
+
+    w = _padded(_uniform(2, 4, 16, 8, 1))
+    plan = A.Plan(w.R, w.E, w.T, w.H, w.k, "padded", device=P.device())
+    x = W.make_x(w, 0, device=P.device())
+    idx = torch.zeros((w.R, w.T, 1), dtype=torch.int32, device=P.device())
+    recv, sm, out = plan.new_buffers()
+    with pytest.raises(A.A2avError, match="padded"):
+        plan.dispatch(x, idx, plan.new_splits(), recv, sm)
