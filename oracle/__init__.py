@@ -62,11 +62,12 @@ def bind(L):
     i64p = np.ctypeslib.ndpointer(np.int64, flags="C_CONTIGUOUS")
     ci, ci64 = ctypes.c_int, ctypes.c_int64
     L.oracle_splits.restype = ctypes.c_uint32
-    L.oracle_splits.argtypes = [ci, ci, ci, ci, ci, ci64, i32p] + [i32p] * 7
+    vp = ctypes.c_void_p  # optional int32 array (NULL = every token takes part)
+    L.oracle_splits.argtypes = [ci, ci, ci, ci, ci, ci64, vp, i32p] + [i32p] * 7
     L.oracle_slot_map.restype = ctypes.c_uint32
-    L.oracle_slot_map.argtypes = [ci, ci, ci, ci, ci, ci64, i32p, i32p, i32p, i32p, i32p]
+    L.oracle_slot_map.argtypes = [ci, ci, ci, ci, ci, ci64, vp, i32p, i32p, i32p, i32p, i32p]
     L.oracle_dispatch.restype = ctypes.c_uint32
-    L.oracle_dispatch.argtypes = [ci, ci, ci, ci, ci, ci, ci64, u16p, i32p, i32p, i32p, i32p, i32p,
+    L.oracle_dispatch.argtypes = [ci, ci, ci, ci, ci, ci, ci64, vp, u16p, i32p, i32p, i32p, i32p, i32p,
                                   u16p, i32p]
     L.oracle_expert_scale.restype = None
     L.oracle_expert_scale.argtypes = [ci, ci, ci64, u16p, i32p, i32p, u16p]
@@ -98,6 +99,14 @@ def lib():
     return _lib
 
 
+def _counts_ptr(num_tokens):
+    """(ctypes pointer or None, keep-alive array) for an optional per-rank token count."""
+    if num_tokens is None:
+        return None, None
+    arr = np.ascontiguousarray(num_tokens, dtype=np.int32)
+    return arr.ctypes.data_as(ctypes.c_void_p), arr
+
+
 def _mode(window_mode) -> int:
     if window_mode in (0, "packed"):
         return 0
@@ -108,8 +117,9 @@ def _mode(window_mode) -> int:
     raise ValueError(window_mode)
 
 
-def splits(R: int, E: int, idx: np.ndarray, window_mode="packed", window_rows: int = 0) -> dict:
-    """Counts and offsets of one dispatch.  idx int32 [R][T][k]."""
+def splits(R: int, E: int, idx: np.ndarray, window_mode="packed", window_rows: int = 0, num_tokens=None) -> dict:
+    """Counts and offsets of one dispatch.  idx int32 [R][T][k]; num_tokens
+    int32 [R] (optional): only tokens t < num_tokens[s] take part."""
     idx = np.ascontiguousarray(idx, dtype=np.int32)
     _, T, k = idx.shape
     if E % R:
@@ -124,7 +134,8 @@ def splits(R: int, E: int, idx: np.ndarray, window_mode="packed", window_rows: i
         "recv_total": np.zeros((R,), np.int32),
         "window_base": np.zeros((R,), np.int32),
     }
-    st = lib().oracle_splits(R, E, T, k, _mode(window_mode), int(window_rows), idx,
+    nt, _keep = _counts_ptr(num_tokens)
+    st = lib().oracle_splits(R, E, T, k, _mode(window_mode), int(window_rows), nt, idx,
                              out["send_counts"], out["send_offsets"], out["recv_counts"],
                              out["recv_offsets"], out["recv_expert_counts"], out["recv_total"],
                              out["window_base"])
@@ -132,12 +143,14 @@ def splits(R: int, E: int, idx: np.ndarray, window_mode="packed", window_rows: i
     return out
 
 
-def slot_map(R: int, E: int, idx: np.ndarray, sp: dict, window_mode="packed", window_rows: int = 0):
+def slot_map(R: int, E: int, idx: np.ndarray, sp: dict, window_mode="packed", window_rows: int = 0,
+             num_tokens=None):
     """(slot_map int32 [R][T][k], status) without moving any payload."""
     idx = np.ascontiguousarray(idx, dtype=np.int32)
     _, T, k = idx.shape
     sm = np.empty((R, T, k), np.int32)
-    st = lib().oracle_slot_map(R, E, T, k, _mode(window_mode), int(window_rows), idx,
+    nt, _keep = _counts_ptr(num_tokens)
+    st = lib().oracle_slot_map(R, E, T, k, _mode(window_mode), int(window_rows), nt, idx,
                                sp["send_offsets"], sp["recv_offsets"], sp["window_base"], sm)
     return sm, int(st)
 
@@ -148,7 +161,7 @@ def arena_rows(R: int, T: int, k: int, window_mode="packed", window_rows: int = 
 
 
 def dispatch(R: int, E: int, x: np.ndarray, idx: np.ndarray, sp: dict, window_mode="packed",
-             window_rows: int = 0, recv: Optional[np.ndarray] = None):
+             window_rows: int = 0, recv: Optional[np.ndarray] = None, num_tokens=None):
     """(recv uint16 [rows][H], slot_map, status).  x uint16 bf16 bits [R][T][H].
     Rows no assignment reaches keep their prior contents (zeros if recv is None)."""
     x = np.ascontiguousarray(x, dtype=np.uint16)
@@ -159,7 +172,8 @@ def dispatch(R: int, E: int, x: np.ndarray, idx: np.ndarray, sp: dict, window_mo
     if recv is None:
         recv = np.zeros((rows, H), np.uint16)
     sm = np.empty((R, T, k), np.int32)
-    st = lib().oracle_dispatch(R, E, T, H, k, _mode(window_mode), int(window_rows), x, idx,
+    nt, _keep = _counts_ptr(num_tokens)
+    st = lib().oracle_dispatch(R, E, T, H, k, _mode(window_mode), int(window_rows), nt, x, idx,
                                sp["send_counts"], sp["send_offsets"], sp["recv_offsets"],
                                sp["window_base"], recv, sm)
     return recv, sm, int(st)
@@ -213,11 +227,21 @@ def f32_to_bf16(v: float) -> int:
     return int(lib().oracle_f32_to_bf16(float(v)))
 
 
-def run_all(R, E, x, idx, gate, window_mode="packed", window_rows=0, expert="identity"):
-    """The whole path on the CPU: splits, dispatch, expert stand-in, combine."""
-    sp = splits(R, E, idx, window_mode, window_rows)
-    recv, sm, st = dispatch(R, E, x, idx, sp, window_mode, window_rows)
+def run_all(R, E, x, idx, gate, window_mode="packed", window_rows=0, expert="identity", num_tokens=None):
+    """The whole path on the CPU: splits, dispatch, expert stand-in, combine.
+    With num_tokens, out rows of tokens that do not take part are zero here
+    (the combine produces nothing for them)."""
+    sp = splits(R, E, idx, window_mode, window_rows, num_tokens)
+    recv, sm, st = dispatch(R, E, x, idx, sp, window_mode, window_rows, num_tokens=num_tokens)
     y = expert_scale(E, recv, idx, sm) if expert == "scale" else recv
-    out = combine(y, gate, sm).reshape(x.shape)
+    T = idx.shape[1]
+    if num_tokens is None:
+        out = combine(y, gate, sm).reshape(x.shape)
+    else:
+        act = [s * T + t for s in range(R) for t in range(min(max(int(num_tokens[s]), 0), T))]
+        out = np.zeros((R * T, x.shape[2]), np.uint16)
+        if act:
+            out[act] = combine(y, gate, sm, np.array(act, np.int64))
+        out = out.reshape(x.shape)
     return {"splits": sp, "recv": recv, "slot_map": sm, "y": y, "out": out,
             "status": sp["status"] | st}

@@ -38,6 +38,11 @@
  *   R5  combine: out = bf16_rne( sum_j w_j * y[slot(t,j)] ), accumulated in
  *       fp32 from 0.0f in slot order j = 0..k-1, each product and each sum
  *       rounded on its own (this file must be built with -ffp-contract=off);
+ *   R7  variable batches: when a per-rank count num_tokens[s] is given, only
+ *       tokens t < num_tokens[s] of rank s take part (the others are not
+ *       counted, get slot -1 and no combine output) -- the counts change from
+ *       step to step while the buffers stay sized for T [P1 Inference;
+ *       P3 section 7, double buffering];
  *   R6  error handling: an expert id outside [0, E) is dropped (not counted,
  *       slot -1, status bit 0); in fixed mode a row whose window-relative
  *       position is >= W is dropped (slot -1, status bit 1) while the counts
@@ -83,6 +88,16 @@ uint16_t oracle_f32_to_bf16(float f)
     return (uint16_t)(u >> 16);
 }
 
+/* Number of tokens of rank s that take part (R7): all T when no counts are
+ * given, else num_tokens[s] clamped to [0, T]. */
+static int active_tokens(const int32_t *num_tokens, int s, int T)
+{
+    if (!num_tokens)
+        return T;
+    int n = num_tokens[s];
+    return n < 0 ? 0 : (n > T ? T : n);
+}
+
 /* ---- step 1: the split counts (what the router's counts are) ---------------
  * send_counts[s][e] = number of (t, j) on rank s with idx = e.
  * send_offsets[s][e] = sum over e' < e of send_counts[s][e']: the start of
@@ -99,7 +114,7 @@ uint16_t oracle_f32_to_bf16(float f)
  * Returns the status bits.
  */
 uint32_t oracle_splits(int R, int E, int T, int k, int window_mode, int64_t window_rows,
-                       const int32_t *idx,
+                       const int32_t *num_tokens, const int32_t *idx,
                        int32_t *send_counts, int32_t *send_offsets,
                        int32_t *recv_counts, int32_t *recv_offsets,
                        int32_t *recv_expert_counts, int32_t *recv_total,
@@ -111,7 +126,8 @@ uint32_t oracle_splits(int R, int E, int T, int k, int window_mode, int64_t wind
         int32_t *cnt = send_counts + (size_t)s * E;
         for (int e = 0; e < E; ++e)
             cnt[e] = 0;
-        for (int t = 0; t < T; ++t)
+        int Ts = active_tokens(num_tokens, s, T);
+        for (int t = 0; t < Ts; ++t)
             for (int j = 0; j < k; ++j) {
                 int32_t e = idx[((size_t)s * T + t) * k + j];
                 if (e < 0 || e >= E) {
@@ -167,7 +183,7 @@ uint32_t oracle_splits(int R, int E, int T, int k, int window_mode, int64_t wind
  * counting sort by expert key) [P1 Inference, Figure 13: the send buffer is
  * ordered by expert].  Dropped ids get -1.
  */
-static void send_positions(int E, int T, int k, const int32_t *idx_s, const int32_t *send_offsets_s,
+static void send_positions(int E, int T, int Ts, int k, const int32_t *idx_s, const int32_t *send_offsets_s,
                            int32_t *running, int32_t *send_pos)
 {
     for (int e = 0; e < E; ++e)
@@ -175,6 +191,10 @@ static void send_positions(int E, int T, int k, const int32_t *idx_s, const int3
     for (int t = 0; t < T; ++t)
         for (int j = 0; j < k; ++j) {
             int32_t e = idx_s[(size_t)t * k + j];
+            if (t >= Ts) {
+                send_pos[(size_t)t * k + j] = -2; /* not taking part (R7) */
+                continue;
+            }
             if (e < 0 || e >= E) {
                 send_pos[(size_t)t * k + j] = -1;
                 continue;
@@ -195,7 +215,7 @@ static void send_positions(int E, int T, int k, const int32_t *idx_s, const int3
  * Returns the status bits.
  */
 uint32_t oracle_slot_map(int R, int E, int T, int k, int window_mode, int64_t window_rows,
-                         const int32_t *idx, const int32_t *send_offsets,
+                         const int32_t *num_tokens, const int32_t *idx, const int32_t *send_offsets,
                          const int32_t *recv_offsets, const int32_t *window_base,
                          int32_t *slot_map)
 {
@@ -206,13 +226,14 @@ uint32_t oracle_slot_map(int R, int E, int T, int k, int window_mode, int64_t wi
     for (int s = 0; s < R; ++s) {
         const int32_t *idx_s = idx + (size_t)s * T * k;
         const int32_t *so = send_offsets + (size_t)s * E;
-        send_positions(E, T, k, idx_s, so, running, pos);
+        send_positions(E, T, active_tokens(num_tokens, s, T), k, idx_s, so, running, pos);
         for (size_t a = 0; a < (size_t)T * k; ++a) {
             int32_t e = idx_s[a];
             int32_t *slot = slot_map + (size_t)s * T * k + a;
             if (pos[a] < 0) {
                 *slot = -1;
-                status |= ORACLE_BAD_EXPERT;
+                if (pos[a] == -1)
+                    status |= ORACLE_BAD_EXPERT;
                 continue;
             }
             int d = e / epr;
@@ -238,7 +259,7 @@ uint32_t oracle_slot_map(int R, int E, int T, int k, int window_mode, int64_t wi
  * written (R6).  Also fills slot_map (as oracle_slot_map).  Returns status.
  */
 uint32_t oracle_dispatch(int R, int E, int T, int H, int k, int window_mode, int64_t window_rows,
-                         const uint16_t *x, const int32_t *idx,
+                         const int32_t *num_tokens, const uint16_t *x, const int32_t *idx,
                          const int32_t *send_counts, const int32_t *send_offsets,
                          const int32_t *recv_offsets, const int32_t *window_base,
                          uint16_t *recv, int32_t *slot_map)
@@ -253,13 +274,14 @@ uint32_t oracle_dispatch(int R, int E, int T, int H, int k, int window_mode, int
         const int32_t *idx_s = idx + (size_t)s * T * k;
         const int32_t *so = send_offsets + (size_t)s * E;
         const int32_t *sc = send_counts + (size_t)s * E;
-        send_positions(E, T, k, idx_s, so, running, pos);
+        send_positions(E, T, active_tokens(num_tokens, s, T), k, idx_s, so, running, pos);
         /* the sort: rows into the send buffer in expert order */
         for (int t = 0; t < T; ++t)
             for (int j = 0; j < k; ++j) {
                 int32_t p = pos[(size_t)t * k + j];
                 if (p < 0) {
-                    status |= ORACLE_BAD_EXPERT;
+                    if (p == -1)
+                        status |= ORACLE_BAD_EXPERT;
                     continue;
                 }
                 memcpy(sendbuf + (size_t)p * H, x + ((size_t)s * T + t) * H, row_bytes);

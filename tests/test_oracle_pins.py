@@ -198,6 +198,48 @@ def test_padded_and_packed_place_the_same_rows_in_the_same_order():
         np.testing.assert_array_equal(a[key], b[key])
 
 
+def test_active_token_counts_equal_truncated_routing():
+    # Tokens past num_tokens[s] take no part: the counts and rows equal those
+    # of the same routing with those tokens' expert ids removed, and their
+    # slots are -1 without a bad-expert status.
+    rng = np.random.default_rng(21)
+    for R, E, T, k in [(2, 4, 6, 1), (3, 6, 7, 2), (4, 16, 12, 3)]:
+        for _ in range(10):
+            idx = rng.integers(0, E, size=(R, T, k), dtype=np.int32)
+            nt = rng.integers(0, T + 1, size=R).astype(np.int32)
+            masked = idx.copy()
+            for s_ in range(R):
+                masked[s_, nt[s_]:] = -1
+            for mode in ("packed", "padded"):
+                bf = brute_force(R, E, masked, mode)
+                sp = oracle.splits(R, E, idx, mode, num_tokens=nt)
+                for key in SPLIT_KEYS:
+                    np.testing.assert_array_equal(sp[key], bf[key].reshape(sp[key].shape), err_msg=key)
+                sm, st = oracle.slot_map(R, E, idx, sp, mode, num_tokens=nt)
+                np.testing.assert_array_equal(sm, bf["slot_map"])
+                assert sp["status"] == 0 and st == 0
+    # clamping: negative counts take nothing, counts past T take everything
+    idx = rng.integers(0, 4, size=(2, 5, 1), dtype=np.int32)
+    a = oracle.splits(2, 4, idx, num_tokens=np.array([-3, 99], np.int32))
+    assert a["send_counts"][0].sum() == 0 and a["send_counts"][1].sum() == 5
+
+
+def test_active_token_counts_combine_only_active_tokens():
+    import workloads as W
+
+    w = W.Workload("t", R=3, E=6, T=9, H=16, k=2, routing="zipf_distinct", zipf_s=1.0, gate="softmax")
+    x = W.bf16_bits(W.make_x(w, 2))
+    rg = W.make_routing_gate(w, 2)
+    nt = np.array([9, 4, 0], np.int32)
+    full = oracle.run_all(w.R, w.E, x, rg["topk_idx"], rg["gate_w"])
+    part = oracle.run_all(w.R, w.E, x, rg["topk_idx"], rg["gate_w"], num_tokens=nt)
+    for s_ in range(w.R):
+        np.testing.assert_array_equal(part["out"][s_, :nt[s_]], full["out"][s_, :nt[s_]])
+        assert (part["out"][s_, nt[s_]:] == 0).all()
+        assert (part["slot_map"][s_, nt[s_]:] == -1).all()
+    assert part["splits"]["recv_total"].sum() == nt.sum() * w.k
+
+
 def test_bad_expert_ids_are_dropped():
     R, E, T, k = 2, 4, 4, 2
     rng = np.random.default_rng(3)
@@ -390,8 +432,8 @@ MUTANTS = {
                                 "(int64_t)recv_offsets[(size_t)s * R + d] + (pos[a] - so[d * epr]);\n            if (window_mode == 1 && rel >= window_rows) {\n                *slot = -1;\n                status"),
     "inclusive send_offsets": ("            send_offsets[(size_t)s * E + e] = run;\n            run += cnt[e];",
                                "            run += cnt[e];\n            send_offsets[(size_t)s * E + e] = run;"),
-    "unstable sort": ("    for (int t = 0; t < T; ++t)\n        for (int j = 0; j < k; ++j) {\n            int32_t e = idx_s[(size_t)t * k + j];\n            if (e < 0 || e >= E) {\n                send_pos",
-                      "    for (int t = T - 1; t >= 0; --t)\n        for (int j = 0; j < k; ++j) {\n            int32_t e = idx_s[(size_t)t * k + j];\n            if (e < 0 || e >= E) {\n                send_pos"),
+    "unstable sort": ("    for (int t = 0; t < T; ++t)\n        for (int j = 0; j < k; ++j) {\n            int32_t e = idx_s[(size_t)t * k + j];\n            if (t >= Ts) {",
+                      "    for (int t = T - 1; t >= 0; --t)\n        for (int j = 0; j < k; ++j) {\n            int32_t e = idx_s[(size_t)t * k + j];\n            if (t >= Ts) {"),
     "dropped gate weight": ("float prod = w[j] * oracle_bf16_to_f32(", "float prod = 1.0f * oracle_bf16_to_f32("),
     "truncating bf16 rounding": ("u += 0x7fffu + keep_lsb;", "u += 0u * keep_lsb;"),
     "window base off by one window": ("            window_base[d] = (int32_t)base;\n        base += recv_total[d];",
