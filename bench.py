@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
     ap.add_argument("--mode", choices=["dynamic", "padded"], default="dynamic",
                     help="padded: the worst-case baseline (every pair sends T*k rows)")
+    ap.add_argument("--active-frac", type=float, default=1.0,
+                    help="tokens taking part per rank, as a fraction of T (read from device memory)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="run the workload with this many tokens per rank (small cases for profiling)")
     ap.add_argument("--flags", type=int, default=0,
@@ -320,6 +322,12 @@ def main():
     recv, slot_map, out = plan.new_buffers()
     sp = plan.new_splits()
     sendbuf = plan.new_send_buffer() if padded else None
+    t_active = w.T
+    if args.active_frac < 1.0:
+        # variable batch: per-rank counts live in device memory, read at run time
+        t_active = max(0, min(w.T, int(round(args.active_frac * w.T))))
+        num_tokens = torch.full((w.R,), t_active, dtype=torch.int32, device=dev)
+        plan.set_active_tokens(num_tokens)
     # L2 flush by READING a buffer larger than L2: it evicts our lines and leaves
     # clean ones behind (a write flush would leave ~L2-size dirty lines whose
     # write-back would land inside the next timed step).
@@ -432,11 +440,12 @@ def main():
         kt[names[j]] = [prefix_ms[j] - prefix_ms[j - 1]]
 
     # ---- results -------------------------------------------------------------------
-    bytes_step = w.algorithmic_bytes()
-    job = whole_job(bytes_step, w.R * w.T, ms, world)
+    w_act = w.scaled(T=t_active) if t_active != w.T else w  # the bytes and tokens that take part
+    bytes_step = w_act.algorithmic_bytes()
+    job = whole_job(bytes_step, w.R * t_active, ms, world)
     gbs = job["gbs"]
     peak, peak_kind = read_peaks()
-    A_ = w.R * w.T * w.k
+    A_ = w.R * t_active * w.k
     # algorithmic bytes per launch: pack reads x once and writes k copies (+ idx
     # read, slot_map write); combine reads k rows and writes out (+ slot_map and
     # gate reads).  pack + combine = Workload.algorithmic_bytes().  The padded
@@ -444,14 +453,14 @@ def main():
     # written.
     kbytes = {
         "splits": 8 * A_,
-        "pack": w.R * w.T * w.H * 2 * (1 + w.k) + 8 * A_,
-        "exchange": 2 * w.R * A_ * w.H * 2,
-        "combine": w.R * w.T * w.H * 2 * (1 + w.k) + 8 * A_,
+        "pack": w.R * t_active * w.H * 2 * (1 + w.k) + 8 * A_,
+        "exchange": 2 * w.R * w.R * w.T * w.k * w.H * 2,
+        "combine": w.R * t_active * w.H * 2 * (1 + w.k) + 8 * A_,
     }
     kus = {n: 1e3 * sum(v) / len(v) for n, v in kt.items() if v}
     dom = max((n for n in names if n != "splits"), key=lambda n: kus.get(n, 0.0))
     ach = kbytes[dom] / (kus[dom] * 1e-6) / 1e9
-    traffic = None if padded else ncu_traffic(dom, w.name)
+    traffic = None if (padded or t_active != w.T) else ncu_traffic(dom, w.name)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
                 "kernel_us": {n: round(v, 3) for n, v in kus.items()},
@@ -539,19 +548,19 @@ def main():
     pipelined(4)  # warm-up
     pipe_ms = max_over_ranks(pipelined(n_pipe))
     serial_t = max_over_ranks(sum(serial_ms) / len(serial_ms))
-    e2e = {"value": round(whole_job(bytes_step, w.R * w.T, pipe_ms, world)["gbs"], 2), "unit": "GB/s",
+    e2e = {"value": round(whole_job(bytes_step, w.R * t_active, pipe_ms, world)["gbs"], 2), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(pipe_ms, 4),
            "steps": n_pipe,
            "path": ("double-buffered loop: pinned host x/idx/gate -> HBM (copy stream), graph replay "
                     "(compute stream), out -> pinned host (copy stream); every step copies its own "
                     "inputs and result"),
-           "serial": {"value": round(whole_job(bytes_step, w.R * w.T, serial_t, world)["gbs"], 2),
+           "serial": {"value": round(whole_job(bytes_step, w.R * t_active, serial_t, world)["gbs"], 2),
                       "ms_per_step": round(serial_t, 4), "path": "one step at a time on one stream"}}
 
     clocks = sampler.summary(t_wall0, t_wall1)
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline and not padded:
+    if rank == 0 and not args.no_cpu_baseline and not padded and t_active == w.T:
         cpu = cpu_baseline(w, W.bf16_bits(x), idx_h, gate_h, args.cpu_seconds)
 
     if rank == 0:
@@ -560,7 +569,7 @@ def main():
             "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_block(w, f"flushed between steps (read of a {FLUSH_BYTES >> 20} MiB buffer)"),
-            "mode": args.mode,
+            "mode": args.mode, "active_tokens_per_rank": t_active,
             "pct_of_peak": round(100 * gbs / world / peak, 2), "peak_gbs": peak,
             "tokens_per_s": round(job["tokens_per_s"], 1), "us_per_call": round(job["us_per_call"], 3),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,

@@ -36,7 +36,7 @@ EXPORTED = [
     "a2av_dispatch", "a2av_splits", "a2av_pack", "a2av_combine", "a2av_expert_scale",
     "a2av_read_device_status", "a2av_device_status_ptr", "a2av_plan_launches",
     "a2av_status_string", "a2av_last_error", "a2av_dispatch_static",
-    "a2av_dispatch_padded", "a2av_pack_padded", "a2av_exchange_padded",
+    "a2av_dispatch_padded", "a2av_pack_padded", "a2av_exchange_padded", "a2av_set_active_tokens",
 ]
 
 
@@ -125,6 +125,8 @@ def load_library(path: Optional[str] = None):
     L.a2av_pack_padded.restype = i32
     L.a2av_exchange_padded.argtypes = [vp, vp, vp, vp]
     L.a2av_exchange_padded.restype = i32
+    L.a2av_set_active_tokens.argtypes = [vp, vp]
+    L.a2av_set_active_tokens.restype = i32
     if path is None:
         _lib = L
     return L
@@ -273,6 +275,20 @@ class Plan:
             self._t(topk_idx, torch.int32, (self.R, self.T, self.k), "topk_idx"), ctypes.byref(splits.ptrs),
             self._rows(recv, "recv"), self._t(slot_map, torch.int32, (self.R, self.T, self.k), "slot_map"),
             _stream_ptr(stream, self.device)), "a2av_pack")
+
+    def set_active_tokens(self, num_tokens=None):
+        """Read per-rank token counts from the int32 device tensor `num_tokens`
+        [R] in every later call (None: every token takes part)."""
+        import torch
+
+        if num_tokens is None:
+            self._num_tokens = None
+            ptr = None
+        else:
+            self._t(num_tokens, torch.int32, (self.R,), "num_tokens")
+            self._num_tokens = num_tokens  # keep it alive while the plan may read it
+            ptr = ctypes.c_void_p(num_tokens.data_ptr())
+        _check(self.lib, self.lib.a2av_set_active_tokens(self.handle, ptr), "a2av_set_active_tokens")
 
     def new_send_buffer(self):
         """Padded plans: the worst-case send buffer, bf16 [R*R*T*k][H] (uninitialised)."""

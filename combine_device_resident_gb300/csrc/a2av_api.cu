@@ -183,6 +183,7 @@ a2av_status_t a2av_splits(a2av_plan_t p, const int32_t *topk_idx, const a2av_spl
     if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
     a2av::HistArgs a;
     a.g = p->g;
+    a.num_tokens = p->num_tokens;
     a.idx = topk_idx;
     a.slot_map = slot_map;
     a.tile_base = p->tile_base;
@@ -229,6 +230,7 @@ static a2av_status_t pack_into(a2av_plan_t p, const void *x, const int32_t *topk
     a2av::PackArgs a;
     memset(&a, 0, sizeof a);
     a.g = p->g;
+    a.num_tokens = p->num_tokens;
     a.x = static_cast<const uint16_t *>(x);
     a.idx = topk_idx;
     a.slot_map = slot_map;
@@ -303,6 +305,7 @@ a2av_status_t a2av_combine(a2av_plan_t p, const void *y, const float *gate_w, co
     if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
     a2av::CombineArgs a;
     a.g = p->g;
+    a.num_tokens = p->num_tokens;
     a.y = static_cast<const uint16_t *>(y);
     a.gate = gate_w;
     a.slot_map = slot_map;
@@ -347,6 +350,12 @@ a2av_status_t a2av_read_device_status(a2av_plan_t p, uint32_t *bits, int clear, 
         if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     }
     return e == cudaSuccess ? A2AV_OK : cuda_fail(e, "read device status");
+}
+
+a2av_status_t a2av_set_active_tokens(a2av_plan_t p, const int32_t *num_tokens) {
+    if (!p || (num_tokens && (reinterpret_cast<uintptr_t>(num_tokens) % 4) != 0)) return A2AV_ERR_INVALID_ARG;
+    p->num_tokens = num_tokens;
+    return A2AV_OK;
 }
 
 const void *a2av_device_status_ptr(a2av_plan_t p) { return p ? p->status : nullptr; }

@@ -39,6 +39,7 @@ struct Geometry {
 
 struct HistArgs {
     Geometry g;
+    const int32_t *num_tokens;  // [R] tokens taking part per rank, or null (all T)
     const int32_t *idx;
     int32_t *slot_map;   // receives the rank of each assignment inside its tile
     int32_t *tile_base;   // [R][tiles][E] counts, turned into exclusive bases
@@ -50,6 +51,7 @@ struct HistArgs {
 
 struct PackArgs {
     Geometry g;
+    const int32_t *num_tokens;
     const uint16_t *x;
     const int32_t *idx;
     int32_t *slot_map;
@@ -77,6 +79,7 @@ struct ExchangeArgs {
 
 struct CombineArgs {
     Geometry g;
+    const int32_t *num_tokens;
     const uint16_t *y;
     const float *gate;
     const int32_t *slot_map;
@@ -125,6 +128,7 @@ struct a2av_plan_s {
     uint32_t *status = nullptr;
     a2av::LaunchShape hist, pack, combine, scale, exchange;
     int splits_small = 0;  // 1: one-CTA splits kernel that writes final rows
+    const int32_t *num_tokens = nullptr;  // a2av_set_active_tokens
     int combine_tma = 1;
     int32_t comb_chunk_bytes = 0, comb_nchunks = 0, comb_stages = 0, comb_nsplit = 1, comb_unroll = 2;
     int pack_tma = 1;
@@ -200,6 +204,14 @@ __device__ __forceinline__ uint32_t peers_by_ballot(uint32_t key, int nbits) {
         peers &= bit ? set : ~set;
     }
     return peers;
+}
+
+// Tokens of rank s that take part in this call: all T, or the caller's
+// device-resident count clamped to [0, T] (read when the kernel runs).
+__device__ __forceinline__ int active_tokens(const int32_t *num_tokens, int s, int T) {
+    if (!num_tokens) return T;
+    const int n = __ldg(num_tokens + s);
+    return n < 0 ? 0 : (n > T ? T : n);
 }
 
 // Programmatic dependent launch: a kernel launched with the programmatic

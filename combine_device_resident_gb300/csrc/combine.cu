@@ -76,6 +76,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
     long long cur = -1;
     int32_t row = -1;
     float w = 0.f;
+    bool active = true;
     // token-major grid stride: the warps active at one time cover a compact
     // stretch of `out` (and of each token's gathered rows)
     for (long long un = gw; un < units; un += nw) {
@@ -83,6 +84,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
         const int piece = (int)(un - u * nsplit);
         if (u != cur) {
             cur = u;
+            const int s_tok = (int)(u / g.T);
+            active = u - (long long)s_tok * g.T < active_tokens(a.num_tokens, s_tok, g.T);
             row = -1;
             w = 0.f;
             if (lane < k) {
@@ -94,6 +97,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
                 }
             }
         }
+        if (!active) continue;  // warp-uniform: the token takes no part, its out row is left alone
         char *dst = reinterpret_cast<char *>(a.out) + (size_t)u * rowb;
         const int vb_end = min(nv, (piece + 1) * steps_per_unit * step);
         for (int vb = piece * steps_per_unit * step; vb < vb_end; vb += step) {
@@ -163,7 +167,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
 // ---------------------------------------------------------------------------
 struct StageMeta {
     uint32_t mask;  // bit j: slot j has a row in this stage
-    uint32_t pad[3];
+    uint32_t skip;  // 1: the unit's token takes no part (nothing loaded, nothing written)
+    uint32_t pad[2];
     float w[kMaxTopk];
 };
 
@@ -227,11 +232,16 @@ __global__ void __launch_bounds__(32, 1) combine_tma_kernel(const CombineArgs a)
         const int src = ((int)(tok - ib0) * k + (lane % k)) & 31;
         const int32_t r = __shfl_sync(kFull, cur_row, src);
         const float w = __shfl_sync(kFull, cur_w, src);
-        const bool in_arena = r >= 0 && r < a.arena_rows;
+        const int s_tok = (int)(tok / g.T);
+        const bool tok_active = tok - (long long)s_tok * g.T < active_tokens(a.num_tokens, s_tok, g.T);
+        const bool in_arena = tok_active && r >= 0 && r < a.arena_rows;
         bad_slot |= lane < k && r >= a.arena_rows;
         const uint32_t mask = __ballot_sync(kFull, lane < k && in_arena);
         if (lane < k) meta[st].w[lane] = w;
-        if (lane == 0) meta[st].mask = mask;
+        if (lane == 0) {
+            meta[st].mask = mask;
+            meta[st].skip = tok_active ? 0u : 1u;
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)__popc(mask) * bytes);
         __syncwarp();
@@ -260,9 +270,10 @@ __global__ void __launch_bounds__(32, 1) combine_tma_kernel(const CombineArgs a)
         const uint32_t off = (uint32_t)(i % nch) * CH;
         const int nvec = (int)(min((size_t)CH, rowb - off) >> 4);
         const uint32_t mask = meta[st].mask;
+        const bool skip = meta[st].skip != 0u;
         const unsigned char *stage = smem + (size_t)st * stage_bytes;
         char *dst = outp + (size_t)tok * rowb + off;
-        for (int v = lane; v < nvec; v += 32) {
+        for (int v = lane; v < nvec && !skip; v += 32) {
             float acc[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) acc[q] = 0.f;

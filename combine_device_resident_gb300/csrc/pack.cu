@@ -18,7 +18,8 @@
 //     (completion on an mbarrier) and written out by k cp.async.bulk stores,
 //     one per destination row; the ring keeps many KB in flight per SM with a
 //     single issuing thread.  Lanes compute the destination rows of the next
-//     batch of tokens while the copies run.
+//     batch of tokens while the copies run.  The CTAs split the tokens that
+//     take part (per-rank active counts), so variable batches stay balanced.
 //   * LSU: warp per token, 16-byte vector loads (no L1 allocation) and stores.
 #include "a2av_internal.cuh"
 
@@ -84,32 +85,54 @@ __device__ __forceinline__ int32_t final_row(const PackArgs &a, long long tok, i
     return (int32_t)row;
 }
 
-// Rows of a batch of `bt` tokens starting at tok0: lane l holds assignment
-// (tok0 + l / k, l % k); also writes them to slot_map.
-__device__ __forceinline__ int32_t batch_rows(const PackArgs &a, long long tok0, long long tok_end, int bt,
-                                              int lane, uint32_t &ovf) {
-    const int k = a.g.k;
-    const int b = lane / k, j = lane - b * k;
-    const long long tok = tok0 + b;
-    if (b >= bt || tok >= tok_end) return -1;
-    const int32_t row = final_row(a, tok, j, ovf);
-    if (!a.rows_final) a.slot_map[(size_t)tok * k + j] = row;
-    return row;
-}
-
 __global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const Geometry &g = a.g;
     const int lane = threadIdx.x;
     const int NS = a.stages, CH = a.chunk_bytes, nch = a.nchunks;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)NS * CH);
+    int *prefix = reinterpret_cast<int *>(bars + NS);  // [R + 1] tokens taking part before rank s
 
-    const long long ntok = (long long)g.R * g.T;
-    const long long per = (ntok + gridDim.x - 1) / gridDim.x;
-    const long long tb = min(ntok, (long long)blockIdx.x * per);
-    const long long te = min(ntok, tb + per);
-    if (tb >= te) return;
-    const long long n = (te - tb) * nch;
+    // The CTAs split the tokens that take part, not all R*T: with per-rank
+    // counts the active tokens are the first num_tokens[s] of every rank, and
+    // contiguous ranges of all tokens would leave most CTAs idle.  Active
+    // index ia maps to rank s (prefix[s] <= ia < prefix[s+1]) and token
+    // ia - prefix[s]; without counts the map is the identity.
+    const bool counted = a.num_tokens != nullptr;
+    if (counted) {
+        int carry = 0;
+        for (int c0 = 0; c0 < g.R; c0 += 32) {
+            const int s = c0 + lane;
+            const int v = s < g.R ? active_tokens(a.num_tokens, s, g.T) : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += t;
+            }
+            if (s < g.R) prefix[s] = carry + incl - v;
+            carry += __shfl_sync(kFull, incl, 31);
+        }
+        if (lane == 0) prefix[g.R] = carry;
+        __syncwarp();
+    }
+    const long long nact = counted ? (long long)prefix[g.R] : (long long)g.R * g.T;
+    auto token_of = [&](long long ia) -> long long {
+        if (!counted) return ia;
+        int lo = 0, hi = g.R - 1;  // the last rank whose prefix is <= ia (skips empty ranks)
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (prefix[mid] <= ia) lo = mid;
+            else hi = mid - 1;
+        }
+        return (long long)lo * g.T + (ia - prefix[lo]);
+    };
+
+    const long long per = (nact + gridDim.x - 1) / gridDim.x;
+    const long long ia_b = min(nact, (long long)blockIdx.x * per);
+    const long long ia_e = min(nact, ia_b + per);
+    if (ia_b >= ia_e) return;
+    const long long n = (ia_e - ia_b) * nch;
     const size_t rowb = (size_t)g.H * 2;
     const int BT = max(1, 32 / g.k);
     const char *x = reinterpret_cast<const char *>(a.x);
@@ -122,12 +145,22 @@ __global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
     __syncwarp();
 
     auto issue_load = [&](long long p) {
-        const long long tok = tb + p / nch;
+        const long long tok = token_of(ia_b + p / nch);
         const uint32_t off = (uint32_t)(p % nch) * CH;
         const uint32_t bytes = (uint32_t)min((size_t)CH, rowb - off);
         uint64_t *bar = &bars[p % NS];
         mbar_arrive_expect_tx(bar, bytes);
         bulk_load(smem + (size_t)(p % NS) * CH, x + (size_t)tok * rowb + off, bytes, bar);
+    };
+    // Destination rows of the batch of BT active tokens starting at ib0:
+    // lane l holds assignment (token of ib0 + l / k, slot l % k).
+    auto rows_of_batch = [&](long long ib0, uint32_t &ovf) -> int32_t {
+        const int b = lane / g.k, j = lane - b * g.k;
+        if (b >= BT || ib0 + b >= ia_e) return -1;
+        const long long tok = token_of(ib0 + b);
+        const int32_t row = final_row(a, tok, j, ovf);
+        if (!a.rows_final) a.slot_map[(size_t)tok * g.k + j] = row;
+        return row;
     };
     // Loads may run NS - LAG units ahead; up to LAG store groups may still be
     // reading their stage when the next load is issued.
@@ -141,18 +174,18 @@ __global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
     grid_dependency_wait();
 
     uint32_t ovf = 0;
-    long long batch_tok0 = tb;
-    int32_t cur = batch_rows(a, batch_tok0, te, BT, lane, ovf);
-    int32_t nxt = batch_rows(a, batch_tok0 + BT, te, BT, lane, ovf);
+    long long ib0 = ia_b;
+    int32_t cur = rows_of_batch(ib0, ovf);
+    int32_t nxt = rows_of_batch(ib0 + BT, ovf);
     bool timed_out = false;
     long long i = 0;
     for (; i < n; ++i) {
-        const long long tok = tb + i / nch;
+        const long long ia = ia_b + i / nch;
         const int c = (int)(i % nch);
-        if (tok >= batch_tok0 + BT) {
-            batch_tok0 += BT;
+        if (ia >= ib0 + BT) {
+            ib0 += BT;
             cur = nxt;
-            nxt = batch_rows(a, batch_tok0 + BT, te, BT, lane, ovf);
+            nxt = rows_of_batch(ib0 + BT, ovf);
         }
         const int st = (int)(i % NS);
         int ok = 1;
@@ -164,9 +197,9 @@ __global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
         }
         const uint32_t off = (uint32_t)c * CH;
         const uint32_t bytes = (uint32_t)min((size_t)CH, rowb - off);
-        const int lb = (int)(tok - batch_tok0);
+        const int lb = (int)(ia - ib0);
         if (lane == 0) fence_proxy_async_smem();
-        const int s_tok = (int)(tok / g.T);
+        const int s_tok = a.padded_tk ? (int)(token_of(ia) / g.T) : 0;
         for (int j = 0; j < g.k; ++j) {
             const int32_t rj = __shfl_sync(kFull, cur, lb * g.k + j);
             if (lane == 0 && rj >= 0) {
@@ -207,6 +240,8 @@ __global__ void __launch_bounds__(256) pack_lsu_kernel(const PackArgs a) {
     uint32_t ovf = 0;
     grid_dependency_wait();
     for (long long u = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < ntok; u += nw) {
+        const int s_tok = (int)(u / g.T);
+        if (u - (long long)s_tok * g.T >= active_tokens(a.num_tokens, s_tok, g.T)) continue;  // warp-uniform
         int32_t row = -1;
         if (lane < g.k) {
             row = final_row(a, u, lane, ovf);
@@ -306,6 +341,8 @@ cudaError_t configure_pack(a2av_plan_s &p) {
     if (e != cudaSuccess) return e;
     size_t budget = (size_t)max_optin / ctas_per_sm;
     budget = budget > 2048 ? budget - 2048 : budget;  // leave room for the static/runtime reservation
+    const size_t prefix_bytes = 4 * (size_t)(kMaxRanks + 1);
+    budget = budget > prefix_bytes ? budget - prefix_bytes : budget;
     // at least two stages: shrink the chunk if the requested one does not fit
     while (chunk > 256 && 2 * (chunk + 8) > budget) chunk = (chunk / 2 + 15) / 16 * 16;
     const int nch2 = (int)((rowb + chunk - 1) / chunk);
@@ -319,7 +356,7 @@ cudaError_t configure_pack(a2av_plan_s &p) {
     p.pack_nchunks = nch2;
     p.pack_stages = stages;
     p.pack.block = 32;
-    p.pack.smem = (size_t)stages * chunk + (size_t)stages * 8;
+    p.pack.smem = (size_t)stages * chunk + (size_t)stages * 8 + prefix_bytes;
     p.pack.grid = p.num_sms * ctas_per_sm;
     // The attribute is a per-kernel cap shared by every plan: raise it to the
     // device maximum (never lower it to this plan's size).

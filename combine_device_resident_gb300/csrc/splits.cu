@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(kHistThreads) hist_scan_kernel(const HistArgs 
     const int s = blockIdx.y, tile = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int A = g.T * g.k;  // assignments of one rank
+    const int As = active_tokens(a.num_tokens, s, g.T) * g.k;  // of them taking part
 
     // ---- per-warp counts of this tile --------------------------------------
     int *cnt = smem + warp * ES;
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(kHistThreads) hist_scan_kernel(const HistArgs 
         if (w0 + r * 32 >= A) break;  // warp-uniform
         const int ai = w0 + r * 32 + lane;
         const int e = vals[r];
-        const bool inr = ai < A;
+        const bool inr = ai < As;
         const bool good = inr && e >= 0 && e < E;
         bad |= inr && !good;
         rank[r] = count_round(cnt, e, good, E, g.key_bits);
@@ -296,6 +297,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
     const int R = g.R, E = g.E, epr = g.epr, ES = E + 1;
     const int A = g.T * g.k;
     const int s = blockIdx.x;  // == rank of this CTA in the cluster
+    const int As = active_tokens(a.num_tokens, s, g.T) * g.k;  // assignments taking part
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chunk = ((A + kClusterWarps - 1) / kClusterWarps + 31) / 32 * 32;
     const int a0 = warp * chunk;
@@ -322,7 +324,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
         for (int r = 0; r < kClusterRounds; ++r) {
             if (r * 32 >= chunk || a0 + r * 32 >= A) break;  // warp-uniform
             const int ai = a0 + r * 32 + lane;
-            const bool inr = ai < A;
+            const bool inr = ai < As;
             const int e = vals[r];
             const bool good = inr && e >= 0 && e < E;
             bad |= inr && !good;

@@ -124,8 +124,9 @@ extern "C" a2av_status_t a2av_dispatch_static(const a2av_config_t *cfg, const vo
     // at zero, but clear them anyway so that nothing depends on earlier calls.
     if (e == cudaSuccess) e = cudaMemsetAsync(p.counters, 0, ((size_t)g.R + 1) * sizeof(uint32_t), s);
     if (e == cudaSuccess) {
-        a2av::HistArgs h;
+        a2av::HistArgs h{};
         h.g = g;
+        h.num_tokens = nullptr;
         h.idx = topk_idx;
         h.slot_map = slot_map;
         h.tile_base = p.tile_base;

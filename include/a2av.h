@@ -245,6 +245,19 @@ a2av_status_t a2av_pack_padded(a2av_plan_t plan, const void *x, const int32_t *t
                                const a2av_splits_t *splits, void *sendbuf, int32_t *slot_map, void *stream);
 a2av_status_t a2av_exchange_padded(a2av_plan_t plan, const void *sendbuf, void *recv, void *stream);
 
+/* Variable batches (decode): from now on every kernel this plan enqueues
+ * reads num_tokens[s] -- a caller-owned DEVICE array of R int32, read when
+ * the kernel runs, so it may change between replays of a captured graph --
+ * and only tokens t < num_tokens[s] of rank s take part (values are clamped
+ * to [0, T]).  Tokens that take no part are not counted, not copied, get
+ * slot -1 without a bad-id status, and their `out` rows are left untouched
+ * by a2av_combine.  NULL (the default) makes every token take part.  Host
+ * call, no device work; affects later enqueues only.  [Inference section:
+ * the real counts change with every routing while the captured graph stays
+ * the same; buffers keep their worst-case size and consecutive calls use
+ * alternating receive buffers (double buffering).] */
+a2av_status_t a2av_set_active_tokens(a2av_plan_t plan, const int32_t *num_tokens);
+
 /* Copy the device status word to *bits (synchronises `stream`); if `clear`,
  * reset it to 0 afterwards.  Not capturable. */
 a2av_status_t a2av_read_device_status(a2av_plan_t plan, uint32_t *bits, int clear, void *stream);

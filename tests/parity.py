@@ -27,7 +27,7 @@ def device():
 
 def gpu_run(w: W.Workload, x, idx: np.ndarray, gate: np.ndarray, flags=0, pack_ctas_per_sm=0,
             pack_stage_bytes=0, pack_store_lag=0, combine_ctas_per_sm=0, combine_stage_bytes=0,
-            combine_unroll=0, guard_rows=4, expert=None, plan=None):
+            combine_unroll=0, guard_rows=4, expert=None, plan=None, num_tokens=None):
     """Run dispatch (+ expert stand-in) + combine on the GPU through the C ABI.
     Returns host copies and the plan.  x is a torch bf16 tensor on the GPU."""
     import torch
@@ -39,10 +39,14 @@ def gpu_run(w: W.Workload, x, idx: np.ndarray, gate: np.ndarray, flags=0, pack_c
                     pack_ctas_per_sm=pack_ctas_per_sm, pack_stage_bytes=pack_stage_bytes,
                     pack_store_lag=pack_store_lag, combine_ctas_per_sm=combine_ctas_per_sm,
                     combine_stage_bytes=combine_stage_bytes, combine_unroll=combine_unroll)
+    nt_t = None
+    if num_tokens is not None:
+        nt_t = torch.from_numpy(np.ascontiguousarray(num_tokens, np.int32)).to(dev)
+    plan.set_active_tokens(nt_t)
     rows = plan.arena_rows
     canary = torch.full((rows + guard_rows, w.H), -7.0, dtype=torch.bfloat16, device=dev)
     recv = canary[:rows]
-    out = torch.empty((w.R, w.T, w.H), dtype=torch.bfloat16, device=dev)
+    out = torch.full((w.R, w.T, w.H), 3.0, dtype=torch.bfloat16, device=dev)  # untouched rows stay 3.0
     slot_map = torch.empty((w.R, w.T, w.k), dtype=torch.int32, device=dev)
     sp = plan.new_splits()
     idx_t = torch.from_numpy(idx).to(dev)
@@ -66,7 +70,7 @@ def gpu_run(w: W.Workload, x, idx: np.ndarray, gate: np.ndarray, flags=0, pack_c
     fill = int(torch.tensor(-7.0, dtype=torch.bfloat16).view(torch.int16))
     return {"plan": plan, "splits": sp.to_numpy(), "slot_map": slot_map.cpu().numpy(), "recv_t": recv,
             "y_t": y, "out_t": out, "status": status, "guard_ok": bool((guard == fill).all()),
-            "idx_t": idx_t, "gate_t": gate_t}
+            "idx_t": idx_t, "gate_t": gate_t, "nt_t": nt_t}
 
 
 def bits(t) -> np.ndarray:
@@ -96,7 +100,9 @@ def full_parity(w: W.Workload, seed=0, idx=None, gate=None, x=None, **kw):
         gate = rg["gate_w"] if gate is None else gate
     g = gpu_run(w, x, idx, gate, **kw)
     xh = bits(x)
-    ref = oracle.run_all(w.R, w.E, xh, idx, gate, w.window_mode, w.window_rows, kw.get("expert") or w.expert)
+    nt = kw.get("num_tokens")
+    ref = oracle.run_all(w.R, w.E, xh, idx, gate, w.window_mode, w.window_rows, kw.get("expert") or w.expert,
+                         num_tokens=nt)
     check_splits(g["splits"], ref["splits"])
     np.testing.assert_array_equal(g["slot_map"], ref["slot_map"], err_msg="slot_map")
     assert g["status"] == ref["status"], (g["status"], ref["status"])
@@ -104,7 +110,16 @@ def full_parity(w: W.Workload, seed=0, idx=None, gate=None, x=None, **kw):
     recv = bits(g["recv_t"])
     np.testing.assert_array_equal(recv[np.sort(rows)], ref["recv"][np.sort(rows)], err_msg="recv rows")
     out = bits(g["out_t"])
-    d = ulp_diff(out, ref["out"])
+    if nt is not None:
+        # tokens that take part: the oracle's combine; the others: untouched
+        act = np.zeros((w.R, w.T), bool)
+        for s_ in range(w.R):
+            act[s_, :min(max(int(nt[s_]), 0), w.T)] = True
+        untouched = int(np.array([3.0], np.float32).view(np.uint32)[0] >> 16)
+        assert (out[~act] == untouched).all(), "combine wrote rows of tokens that take no part"
+        d = ulp_diff(out[act], ref["out"][act])
+    else:
+        d = ulp_diff(out, ref["out"])
     assert d.max(initial=0) <= COMBINE_ULP_TOL, f"combine off by {d.max()} ulp"
     assert g["guard_ok"], "a store landed past the end of the recv arena"
     g["ref"] = ref

@@ -297,3 +297,98 @@ def test_padded_plan_rejects_dynamic_calls():
     recv, sm, out = plan.new_buffers()
     with pytest.raises(A.A2avError, match="padded"):
         plan.dispatch(x, idx, plan.new_splits(), recv, sm)
+
+
+# ---------------------------------------------------------------------------
+# variable batches: per-rank active token counts read from device memory
+# ---------------------------------------------------------------------------
+def _counts(w, seed):
+    rng = np.random.default_rng(seed)
+    nt = rng.integers(0, w.T + 1, size=w.R).astype(np.int32)
+    nt[0] = w.T      # a full rank
+    nt[-1] = 0       # an idle rank
+    return nt
+
+
+@pytest.mark.parametrize("wid,T,H", [(1, None, None), (2, 1000, 136), (3, 256, 72), (4, 2100, 40), (5, 300, 64)])
+def test_active_token_counts(wid, T, H):
+    w = W.WORKLOADS[wid] if T is None else W.WORKLOADS[wid].scaled(T=T, H=H)
+    g = P.full_parity(w, num_tokens=_counts(w, wid))
+    assert g["status"] == 0
+
+
+@pytest.mark.parametrize("variant", [dict(flags=1), dict(flags=2), dict(flags=4), dict(flags=7)],
+                         ids=["lsu", "tiled", "tma-combine", "all-variants"])
+def test_active_token_counts_variants(variant):
+    w = W.WORKLOADS[4].scaled(T=1500, H=136)
+    P.full_parity(w, num_tokens=_counts(w, 3), **variant)
+    w = W.WORKLOADS[2].scaled(T=600, H=264)
+    P.full_parity(w, num_tokens=_counts(w, 4), **variant)
+
+
+def test_active_token_counts_padded():
+    w = _padded(W.WORKLOADS[4].scaled(T=700, H=72))
+    P.full_parity(w, num_tokens=_counts(w, 5))
+
+
+def test_active_token_counts_clamped():
+    w = W.WORKLOADS[2].scaled(T=300, H=24)
+    P.full_parity(w, num_tokens=np.array([-5, 400, 0, 300, 1, 299, 150, 10**6], np.int32))
+
+
+def test_graph_replays_with_changing_counts_and_double_buffered_arenas():
+    # One graph per receive arena (double buffering: consecutive steps never
+    # share a receive buffer); between replays the routing, the gates and the
+    # per-rank token counts change in device memory.  Every replay matches the
+    # oracle.
+    import torch
+    from combine_device_resident_gb300 import Plan
+
+    w = W.WORKLOADS[4].scaled(T=1200, H=72)
+    dev = P.device()
+    plan = Plan(w.R, w.E, w.T, w.H, w.k, device=dev)
+    nt_t = torch.full((w.R,), w.T, dtype=torch.int32, device=dev)
+    plan.set_active_tokens(nt_t)
+    x = W.make_x(w, 0, device=dev)
+    idx_t = torch.zeros((w.R, w.T, w.k), dtype=torch.int32, device=dev)
+    gate_t = torch.zeros((w.R, w.T, w.k), dtype=torch.float32, device=dev)
+    arenas = []
+    for _ in range(2):
+        recv, slot_map, out = plan.new_buffers()
+        arenas.append((recv, slot_map, out, plan.new_splits()))
+    rg = W.make_routing_gate(w, 7)
+    idx_t.copy_(torch.from_numpy(rg["topk_idx"]))
+    gate_t.copy_(torch.from_numpy(rg["gate_w"]))
+    graphs = []
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        for recv, slot_map, out, sp in arenas:  # warm-up outside capture
+            plan.dispatch(x, idx_t, sp, recv, slot_map)
+            plan.combine(recv, gate_t, slot_map, out)
+    torch.cuda.current_stream(dev).wait_stream(s)
+    torch.cuda.synchronize()
+    for recv, slot_map, out, sp in arenas:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            plan.dispatch(x, idx_t, sp, recv, slot_map)
+            plan.combine(recv, gate_t, slot_map, out)
+        graphs.append(g)
+    xh = P.bits(x)
+    for step in range(6):
+        rg = W.make_routing_gate(w, 100 + step)
+        nt = _counts(w, 200 + step)
+        idx_t.copy_(torch.from_numpy(rg["topk_idx"]))
+        gate_t.copy_(torch.from_numpy(rg["gate_w"]))
+        nt_t.copy_(torch.from_numpy(nt))
+        recv, slot_map, out, sp = arenas[step % 2]
+        out.fill_(3.0)
+        graphs[step % 2].replay()
+        torch.cuda.synchronize()
+        ref = oracle.run_all(w.R, w.E, xh, rg["topk_idx"], rg["gate_w"], num_tokens=nt)
+        P.check_splits(sp.to_numpy(), ref["splits"])
+        np.testing.assert_array_equal(slot_map.cpu().numpy(), ref["slot_map"])
+        ob = P.bits(out)
+        for s_ in range(w.R):
+            assert ulp_diff(ob[s_, :nt[s_]], ref["out"][s_, :nt[s_]]).max(initial=0) <= P.COMBINE_ULP_TOL
+    assert plan.read_status() == 0
