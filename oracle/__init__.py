@@ -48,7 +48,7 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
-                               "-fPIC", "-shared", "-Wall", "-Wextra", "-o", tmp, _SRC])
+                               "-fPIC", "-shared", "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -75,6 +75,9 @@ def bind(L):
     L.oracle_combine.argtypes = [ci, ci, u16p, f32p, i32p, i64p, ci64, u16p]
     L.oracle_combine_f64.restype = None
     L.oracle_combine_f64.argtypes = [ci, ci, u16p, f32p, i32p, i64p, ci64, f64p]
+    f32p_ = f32p
+    L.oracle_route.restype = None
+    L.oracle_route.argtypes = [ci, ci, ci, ci, vp, f32p_, i32p, f64p]
     L.oracle_bf16_to_f32.restype = ctypes.c_float
     L.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
     L.oracle_f32_to_bf16.restype = ctypes.c_uint16
@@ -88,7 +91,7 @@ def compile_source(src: str, out: str) -> str:
     with open(cfile, "w") as f:
         f.write(src)
     subprocess.check_call(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
-                           "-fPIC", "-shared", "-w", "-o", out, cfile])
+                           "-fPIC", "-shared", "-w", "-o", out, cfile, "-lm"])
     return out
 
 
@@ -217,6 +220,18 @@ def combine_f64(y: np.ndarray, gate: np.ndarray, sm: np.ndarray, tokens: Optiona
     out = np.empty((len(tokens), y.shape[1]), np.float64)
     lib().oracle_combine_f64(y.shape[1], k, y, gate, sm, tokens, len(tokens), out)
     return out
+
+
+def route(logits: np.ndarray, k: int, num_tokens=None):
+    """Router: (topk_idx int32 [R][T][k], gate float64 [R][T][k]) from fp32
+    logits [R][T][E]; entries of tokens that take no part stay -1 / 0."""
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    R, T, E = logits.shape
+    idx = np.full((R, T, k), -1, np.int32)
+    gate = np.zeros((R, T, k), np.float64)
+    nt, _keep = _counts_ptr(num_tokens)
+    lib().oracle_route(R, T, E, k, nt, logits, idx, gate)
+    return idx, gate
 
 
 def bf16_to_f32(bits: int) -> float:

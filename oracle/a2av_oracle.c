@@ -43,6 +43,8 @@
  *       counted, get slot -1 and no combine output) -- the counts change from
  *       step to step while the buffers stay sized for T [P1 Inference;
  *       P3 section 7, double buffering];
+ *   R8  the router (top-k of per-token logits, softmax gates): see
+ *       oracle_route below;
  *   R6  error handling: an expert id outside [0, E) is dropped (not counted,
  *       slot -1, status bit 0); in fixed mode a row whose window-relative
  *       position is >= W is dropped (slot -1, status bit 1) while the counts
@@ -59,6 +61,7 @@
  *   recv, y    uint16 bf16 bits  [rows][H]
  *   slot_map   int32             [R][T][k]
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -389,6 +392,74 @@ void oracle_combine_f64(int H, int k, const uint16_t *y, const float *gate, cons
                 acc += (double)w[j] * (double)oracle_bf16_to_f32(y[(size_t)slots[j] * H + h]);
             }
             out[(size_t)i * H + h] = acc;
+        }
+    }
+}
+
+/* ---- the router in front of the dispatch ------------------------------------------
+ * [P1 Inference, Figure 13: a router picks the experts of each token before
+ * the tokens are sorted by expert.]  The pages do not define the router;
+ * reading R8: for each token, the k largest of its E logits in descending
+ * order, equal logits ordered by lower expert id first, a NaN logit counted
+ * as -infinity; the gate weights are the softmax of the selected logits,
+ * exp(l_j - l_0) / sum_i exp(l_i - l_0) with l_0 the largest, summed in slot
+ * order.  Here in fp64 (exp of the exact differences), as the reference the
+ * fp32 kernel is held to.  If every selected logit is -infinity the weights
+ * are 1/k each.  Tokens past num_tokens[s] (R7) are left untouched.
+ */
+static double router_key(float v)
+{
+    return v != v ? -INFINITY : (double)v;
+}
+
+/* (a, ia) comes before (b, ib) in the selection order. */
+static int router_before(double a, int ia, double b, int ib)
+{
+    return a > b || (a == b && ia < ib);
+}
+
+void oracle_route(int R, int T, int E, int k, const int32_t *num_tokens, const float *logits,
+                  int32_t *idx, double *gate)
+{
+    for (int s = 0; s < R; ++s) {
+        int Ts = active_tokens(num_tokens, s, T);
+        for (int t = 0; t < Ts; ++t) {
+            const float *l = logits + ((size_t)s * T + t) * E;
+            int32_t *out_i = idx + ((size_t)s * T + t) * k;
+            double *out_w = gate + ((size_t)s * T + t) * k;
+            double sel[32];
+            double prev_v = INFINITY;
+            int prev_i = -1;
+            for (int j = 0; j < k; ++j) {
+                /* the first element (in selection order) after the previous pick */
+                int best = -1;
+                double best_v = 0.0;
+                for (int e = 0; e < E; ++e) {
+                    double v = router_key(l[e]);
+                    if (j > 0 && !router_before(prev_v, prev_i, v, e))
+                        continue;
+                    if (best < 0 || router_before(v, e, best_v, best)) {
+                        best = e;
+                        best_v = v;
+                    }
+                }
+                out_i[j] = best;
+                sel[j] = best_v;
+                prev_v = best_v;
+                prev_i = best;
+            }
+            if (sel[0] == -INFINITY) {
+                for (int j = 0; j < k; ++j)
+                    out_w[j] = 1.0 / k;
+                continue;
+            }
+            double sum = 0.0, ex[32];
+            for (int j = 0; j < k; ++j) {
+                ex[j] = exp(sel[j] - sel[0]);
+                sum += ex[j];
+            }
+            for (int j = 0; j < k; ++j)
+                out_w[j] = ex[j] / sum;
         }
     }
 }

@@ -240,6 +240,34 @@ def test_active_token_counts_combine_only_active_tokens():
     assert part["splits"]["recv_total"].sum() == nt.sum() * w.k
 
 
+def test_router_against_numpy_sort_and_softmax():
+    # selection = a lexicographic sort by (logit descending, id ascending),
+    # gates = the float64 softmax of the selected logits
+    from scipy.special import softmax
+
+    rng = np.random.default_rng(31)
+    for R, T, E, k in [(2, 5, 4, 1), (3, 7, 16, 2), (2, 9, 256, 8), (1, 3, 64, 32)]:
+        logits = rng.standard_normal((R, T, E)).astype(np.float32)
+        logits[0, 0, :] = 0.5                      # all equal: ids in order
+        logits[-1, -1, 3 % E] = np.nan             # NaN counts as -inf
+        logits[-1, 1 % T, :2] = np.float32(-np.inf)
+        idx, gate = oracle.route(logits, k)
+        for s_ in range(R):
+            for t in range(T):
+                v = np.where(np.isnan(logits[s_, t]), -np.inf, logits[s_, t].astype(np.float64))
+                order = np.lexsort((np.arange(E), -v))[:k]
+                np.testing.assert_array_equal(idx[s_, t], order)
+                np.testing.assert_allclose(gate[s_, t], softmax(v[order]), rtol=1e-12, atol=0)
+    # every selected logit -inf: equal weights
+    logits = np.full((1, 1, 8), -np.inf, np.float32)
+    idx, gate = oracle.route(logits, 3)
+    assert idx[0, 0].tolist() == [0, 1, 2] and np.allclose(gate, 1 / 3)
+    # inactive tokens untouched
+    logits = rng.standard_normal((2, 4, 8)).astype(np.float32)
+    idx, gate = oracle.route(logits, 2, num_tokens=np.array([1, 0], np.int32))
+    assert (idx[0, 1:] == -1).all() and (idx[1] == -1).all() and (idx[0, 0] >= 0).all()
+
+
 def test_bad_expert_ids_are_dropped():
     R, E, T, k = 2, 4, 4, 2
     rng = np.random.default_rng(3)
@@ -440,6 +468,8 @@ MUTANTS = {
                                       "        base += recv_total[d];\n            window_base[d] = (int32_t)base;"),
     "wrong expert-to-rank map": ("            int d = e / epr;\n            int64_t rel", "            int d = e % R;\n            int64_t rel"),
     "expert scale sign": ("float scale = 1.0f + q;", "float scale = 1.0f - q;"),
+    "router tie order": ("return a > b || (a == b && ia < ib);", "return a > b || (a == b && ia > ib);"),
+    "router softmax shift": ("ex[j] = exp(sel[j] - sel[0]);", "ex[j] = exp(sel[j] - sel[k - 1]) * (j + 1);"),
     "padded segments by destination": ("recv_offsets[(size_t)d * R + s] = (int32_t)((int64_t)s * T * k);",
                                        "recv_offsets[(size_t)d * R + s] = (int32_t)((int64_t)d * T * k);"),
 }
@@ -457,6 +487,7 @@ def _pin_suite():
     test_expert_scale_closed_form_torch()
     test_bf16_rounding_matches_torch()
     test_padded_layout_against_brute()
+    test_router_against_numpy_sort_and_softmax()
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
