@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
     ap.add_argument("--mode", choices=["dynamic", "padded"], default="dynamic",
                     help="padded: the worst-case baseline (every pair sends T*k rows)")
+    ap.add_argument("--router", action="store_true",
+                    help="start each step from per-token logits: router kernel (top-k + softmax) first")
     ap.add_argument("--active-frac", type=float, default=1.0,
                     help="tokens taking part per rank, as a fraction of T (read from device memory)")
     ap.add_argument("--tokens", type=int, default=0,
@@ -347,6 +349,11 @@ def main():
                 ("combine", lambda s: plan.combine(recv_, gate_, slot_, out_, stream=s))]
 
     stages = make_stages(x, idx, gate, sp, recv, slot_map, out, sendbuf)
+    logits = None
+    if args.router:
+        # the router writes idx and gate in place from logits resident in HBM
+        logits = W.make_logits(w, 0, device=dev)
+        stages = [("route", lambda s: plan.route(logits, idx, gate, stream=s))] + stages
 
     def capture(stage_list):
         g = torch.cuda.CUDAGraph()
@@ -441,7 +448,8 @@ def main():
 
     # ---- results -------------------------------------------------------------------
     w_act = w.scaled(T=t_active) if t_active != w.T else w  # the bytes and tokens that take part
-    bytes_step = w_act.algorithmic_bytes()
+    bytes_step = w_act.algorithmic_bytes() + (w.R * t_active * w.E * 4 + 8 * w.R * t_active * w.k if args.router
+                                              else 0)
     job = whole_job(bytes_step, w.R * t_active, ms, world)
     gbs = job["gbs"]
     peak, peak_kind = read_peaks()
@@ -452,13 +460,14 @@ def main():
     # baseline's exchange moves every worst-case segment: R*R*T*k rows read and
     # written.
     kbytes = {
+        "route": w.R * t_active * w.E * 4 + 8 * A_,
         "splits": 8 * A_,
         "pack": w.R * t_active * w.H * 2 * (1 + w.k) + 8 * A_,
         "exchange": 2 * w.R * w.R * w.T * w.k * w.H * 2,
         "combine": w.R * t_active * w.H * 2 * (1 + w.k) + 8 * A_,
     }
     kus = {n: 1e3 * sum(v) / len(v) for n, v in kt.items() if v}
-    dom = max((n for n in names if n != "splits"), key=lambda n: kus.get(n, 0.0))
+    dom = max((n for n in names if n not in ("splits", "route")), key=lambda n: kus.get(n, 0.0))
     ach = kbytes[dom] / (kus[dom] * 1e-6) / 1e9
     traffic = None if (padded or t_active != w.T) else ncu_traffic(dom, w.name)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
@@ -506,7 +515,10 @@ def main():
     sp2 = plan.new_splits()
     send2 = plan.new_send_buffer() if padded else None
     sets = [(x, idx, gate, recv, slot_map, out, sp, graph)]
-    g2 = capture(make_stages(x2, idx2, gate2, sp2, recv2, slot_map2, out2, send2))
+    st2 = make_stages(x2, idx2, gate2, sp2, recv2, slot_map2, out2, send2)
+    if args.router:
+        st2 = [("route", lambda s: plan.route(logits, idx2, gate2, stream=s))] + st2
+    g2 = capture(st2)
     sets.append((x2, idx2, gate2, recv2, slot_map2, out2, sp2, g2))
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]
@@ -560,7 +572,7 @@ def main():
     clocks = sampler.summary(t_wall0, t_wall1)
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline and not padded and t_active == w.T:
+    if rank == 0 and not args.no_cpu_baseline and not padded and t_active == w.T and not args.router:
         cpu = cpu_baseline(w, W.bf16_bits(x), idx_h, gate_h, args.cpu_seconds)
 
     if rank == 0:
@@ -569,7 +581,7 @@ def main():
             "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_block(w, f"flushed between steps (read of a {FLUSH_BYTES >> 20} MiB buffer)"),
-            "mode": args.mode, "active_tokens_per_rank": t_active,
+            "mode": args.mode, "active_tokens_per_rank": t_active, "router": bool(args.router),
             "pct_of_peak": round(100 * gbs / world / peak, 2), "peak_gbs": peak,
             "tokens_per_s": round(job["tokens_per_s"], 1), "us_per_call": round(job["us_per_call"], 3),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,

@@ -37,6 +37,7 @@ EXPORTED = [
     "a2av_read_device_status", "a2av_device_status_ptr", "a2av_plan_launches",
     "a2av_status_string", "a2av_last_error", "a2av_dispatch_static",
     "a2av_dispatch_padded", "a2av_pack_padded", "a2av_exchange_padded", "a2av_set_active_tokens",
+    "a2av_route",
 ]
 
 
@@ -127,6 +128,8 @@ def load_library(path: Optional[str] = None):
     L.a2av_exchange_padded.restype = i32
     L.a2av_set_active_tokens.argtypes = [vp, vp]
     L.a2av_set_active_tokens.restype = i32
+    L.a2av_route.argtypes = [vp, vp, vp, vp, vp]
+    L.a2av_route.restype = i32
     if path is None:
         _lib = L
     return L
@@ -275,6 +278,16 @@ class Plan:
             self._t(topk_idx, torch.int32, (self.R, self.T, self.k), "topk_idx"), ctypes.byref(splits.ptrs),
             self._rows(recv, "recv"), self._t(slot_map, torch.int32, (self.R, self.T, self.k), "slot_map"),
             _stream_ptr(stream, self.device)), "a2av_pack")
+
+    def route(self, logits, topk_idx, gate_w, stream=None):
+        """Top-k experts and softmax gates of fp32 logits [R][T][E] (a2av_route)."""
+        import torch
+
+        _check(self.lib, self.lib.a2av_route(
+            self.handle, self._t(logits, torch.float32, (self.R, self.T, self.E), "logits"),
+            self._t(topk_idx, torch.int32, (self.R, self.T, self.k), "topk_idx"),
+            self._t(gate_w, torch.float32, (self.R, self.T, self.k), "gate_w"),
+            _stream_ptr(stream, self.device)), "a2av_route")
 
     def set_active_tokens(self, num_tokens=None):
         """Read per-rank token counts from the int32 device tensor `num_tokens`

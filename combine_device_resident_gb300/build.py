@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "liba2av.so")
-SOURCES = ["a2av_api.cu", "splits.cu", "pack.cu", "combine.cu", "static_scratch.cu"]
+SOURCES = ["a2av_api.cu", "splits.cu", "pack.cu", "combine.cu", "static_scratch.cu", "router.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-warn-spills"]

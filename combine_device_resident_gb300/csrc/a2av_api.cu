@@ -159,6 +159,7 @@ a2av_status_t a2av_plan_create(const a2av_config_t *cfg, a2av_plan_t *out_plan) 
     if (e == cudaSuccess) e = a2av::configure_hist(*p);
     if (e == cudaSuccess) e = a2av::configure_pack(*p);
     if (e == cudaSuccess) e = a2av::configure_combine(*p);
+    if (e == cudaSuccess) e = a2av::configure_route(*p);
     if (e != cudaSuccess) {
         cudaFree(p->workspace);
         delete p;
@@ -350,6 +351,26 @@ a2av_status_t a2av_read_device_status(a2av_plan_t p, uint32_t *bits, int clear, 
         if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     }
     return e == cudaSuccess ? A2AV_OK : cuda_fail(e, "read device status");
+}
+
+a2av_status_t a2av_route(a2av_plan_t p, const float *logits, int32_t *topk_idx, float *gate_w, void *stream) {
+    if (!p || !aligned(logits, 4) || !aligned(topk_idx, 4) || !aligned(gate_w, 4)) return A2AV_ERR_INVALID_ARG;
+    if (p->g.k > p->g.E) {
+        a2av::set_last_error("a2av_route: k distinct experts need k <= E");
+        return A2AV_ERR_INVALID_ARG;
+    }
+    DeviceGuard guard(p->cfg.device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    a2av::RouteArgs a;
+    a.g = p->g;
+    a.num_tokens = p->num_tokens;
+    a.logits = logits;
+    a.idx = topk_idx;
+    a.gate = gate_w;
+    cudaError_t e = a2av::launch_route(*p, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "route kernel launch");
+    p->launches += 1;
+    return A2AV_OK;
 }
 
 a2av_status_t a2av_set_active_tokens(a2av_plan_t p, const int32_t *num_tokens) {

@@ -70,6 +70,14 @@ struct PackArgs {
     int64_t padded_tk;    // padded plans: T*k, and `recv` is the padded send buffer
 };
 
+struct RouteArgs {
+    Geometry g;
+    const int32_t *num_tokens;
+    const float *logits;  // [R][T][E]
+    int32_t *idx;         // [R][T][k]
+    float *gate;          // [R][T][k]
+};
+
 struct ExchangeArgs {
     const uint16_t *sendbuf;
     uint16_t *recv;
@@ -126,7 +134,7 @@ struct a2av_plan_s {
     int32_t *rank_total = nullptr;
     uint32_t *counters = nullptr;
     uint32_t *status = nullptr;
-    a2av::LaunchShape hist, pack, combine, scale, exchange;
+    a2av::LaunchShape hist, pack, combine, scale, exchange, route;
     int splits_small = 0;  // 1: one-CTA splits kernel that writes final rows
     const int32_t *num_tokens = nullptr;  // a2av_set_active_tokens
     int combine_tma = 1;
@@ -161,6 +169,8 @@ cudaError_t launch_pack(const a2av_plan_s &p, const PackArgs &a, cudaStream_t s)
 cudaError_t launch_combine(const a2av_plan_s &p, const CombineArgs &a, cudaStream_t s);
 cudaError_t launch_scale(const a2av_plan_s &p, const ScaleArgs &a, cudaStream_t s);
 cudaError_t launch_exchange_padded(const a2av_plan_s &p, const ExchangeArgs &a, cudaStream_t s);
+cudaError_t launch_route(const a2av_plan_s &p, const RouteArgs &a, cudaStream_t s);
+cudaError_t configure_route(a2av_plan_s &p);
 
 // Records the text a2av_last_error() returns on the calling thread.
 void set_last_error(const char *msg);

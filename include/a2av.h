@@ -245,6 +245,18 @@ a2av_status_t a2av_pack_padded(a2av_plan_t plan, const void *x, const int32_t *t
                                const a2av_splits_t *splits, void *sendbuf, int32_t *slot_map, void *stream);
 a2av_status_t a2av_exchange_padded(a2av_plan_t plan, const void *sendbuf, void *recv, void *stream);
 
+/* Router (one kernel): for every token, topk_idx[s][t][0..k-1] = the k
+ * experts with the largest logits[s][t][.] (fp32 [R][T][E], device), in
+ * descending order, equal logits by lower expert id, a NaN logit counted as
+ * -infinity; gate_w[s][t][j] = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the
+ * selected logits (fp32, sum in slot order; 1/k each if every selected
+ * logit is -infinity).  Tokens that take no part (a2av_set_active_tokens)
+ * are left untouched.  Needs k <= E.  Its outputs feed a2av_dispatch /
+ * a2av_combine.
+ * [Inference section, Figure 13: a router kernel picks each token's experts
+ * before the tokens are sorted by expert; the pages do not define it.] */
+a2av_status_t a2av_route(a2av_plan_t plan, const float *logits, int32_t *topk_idx, float *gate_w, void *stream);
+
 /* Variable batches (decode): from now on every kernel this plan enqueues
  * reads num_tokens[s] -- a caller-owned DEVICE array of R int32, read when
  * the kernel runs, so it may change between replays of a captured graph --

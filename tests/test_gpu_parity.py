@@ -392,3 +392,98 @@ def test_graph_replays_with_changing_counts_and_double_buffered_arenas():
         for s_ in range(w.R):
             assert ulp_diff(ob[s_, :nt[s_]], ref["out"][s_, :nt[s_]]).max(initial=0) <= P.COMBINE_ULP_TOL
     assert plan.read_status() == 0
+
+
+# ---------------------------------------------------------------------------
+# the router in front of the dispatch
+# ---------------------------------------------------------------------------
+def _gate_bound(logits64, idx):
+    """Relative error bound of the fp32 gates against the fp64 reference:
+    (2*max|l_j - l_0| + k + 8) * 2^-24 (rounded differences, expf within 2 ulp,
+    k - 1 rounded sums, one rounded division)."""
+    sel = np.take_along_axis(logits64, idx.astype(np.int64), axis=-1)
+    dmax = np.abs(sel - sel[..., :1]).max(axis=-1, keepdims=True)
+    return (2 * dmax + idx.shape[-1] + 8) * 2.0 ** -24
+
+
+@pytest.mark.parametrize("R,T,E,k", [(2, 300, 4, 1), (8, 512, 16, 1), (16, 257, 128, 2), (4, 130, 256, 8),
+                                     (2, 40, 2048, 32), (3, 33, 37 * 3, 5)])
+def test_router_matches_oracle(R, T, E, k):
+    import torch
+    from combine_device_resident_gb300 import Plan
+
+    dev = P.device()
+    w = W.Workload("router", R=R, E=E, T=T, H=8, k=k)
+    logits = W.make_logits(w, R + E, device=dev)
+    logits[0, 0] = 0.25                       # all equal: lowest ids first
+    logits[0, 1, :3] = float("nan")           # NaN counts as -inf
+    logits[-1, -1] = float("-inf")            # every logit -inf: equal gates
+    logits[-1, 0, E // 2] = logits[-1, 0].max()  # a tie at the top
+    if T > 3:
+        logits[0, 2, :] = -1.0                     # +0 and -0 compare equal: lower id first
+        logits[0, 2, E - 1] = 0.0
+        logits[0, 2, 0] = -0.0
+    plan = Plan(R, E, T, 8, k, device=dev)
+    idx = torch.full((R, T, k), -9, dtype=torch.int32, device=dev)
+    gate = torch.zeros((R, T, k), dtype=torch.float32, device=dev)
+    plan.route(logits, idx, gate)
+    torch.cuda.synchronize()
+    lh = logits.cpu().numpy()
+    ridx, rgate = oracle.route(lh, k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+    g = gate.cpu().numpy().astype(np.float64)
+    l64 = np.where(np.isnan(lh), -np.inf, lh.astype(np.float64))
+    finite = np.isfinite(np.take_along_axis(l64, ridx[..., :1].astype(np.int64), axis=-1))
+    bound = np.where(finite, _gate_bound(np.where(np.isfinite(l64), l64, -1e30), ridx), 2.0 ** -24)
+    assert (np.abs(g - rgate) <= bound * rgate + 1e-45).all()
+
+
+@pytest.mark.parametrize("wid,T,H", [(2, 700, 136), (4, 600, 72), (5, 120, 64)])
+def test_router_then_dispatch_and_combine(wid, T, H):
+    # The whole step from logits: GPU router -> dispatch -> combine against the
+    # oracle's router (fp64 gates rounded to fp32) -> dispatch -> combine.
+    import torch
+    from combine_device_resident_gb300 import Plan
+
+    w = W.WORKLOADS[wid].scaled(T=T, H=H)
+    dev = P.device()
+    x = W.make_x(w, 0, device=dev)
+    logits = W.make_logits(w, 0, device=dev)
+    plan = Plan(w.R, w.E, w.T, w.H, w.k, device=dev)
+    idx = torch.empty((w.R, w.T, w.k), dtype=torch.int32, device=dev)
+    gate = torch.empty((w.R, w.T, w.k), dtype=torch.float32, device=dev)
+    recv, slot_map, out = plan.new_buffers()
+    sp = plan.new_splits()
+    plan.route(logits, idx, gate)
+    plan.dispatch(x, idx, sp, recv, slot_map)
+    plan.combine(recv, gate, slot_map, out)
+    torch.cuda.synchronize()
+    ridx, rgate = oracle.route(logits.cpu().numpy(), w.k)
+    ref = oracle.run_all(w.R, w.E, P.bits(x), ridx, rgate.astype(np.float32))
+    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+    P.check_splits(sp.to_numpy(), ref["splits"])
+    np.testing.assert_array_equal(slot_map.cpu().numpy(), ref["slot_map"])
+    assert ulp_diff(P.bits(out), ref["out"]).max() <= P.COMBINE_ULP_TOL
+    assert plan.read_status() == 0
+
+
+def test_router_leaves_inactive_tokens_alone():
+    import torch
+    from combine_device_resident_gb300 import Plan
+
+    w = W.WORKLOADS[4].scaled(T=100, H=8)
+    dev = P.device()
+    plan = Plan(w.R, w.E, w.T, w.H, w.k, device=dev)
+    nt = _counts(w, 9)
+    plan.set_active_tokens(torch.from_numpy(nt).to(dev))
+    logits = W.make_logits(w, 1, device=dev)
+    idx = torch.full((w.R, w.T, w.k), -9, dtype=torch.int32, device=dev)
+    gate = torch.full((w.R, w.T, w.k), -1.0, dtype=torch.float32, device=dev)
+    plan.route(logits, idx, gate)
+    torch.cuda.synchronize()
+    ridx, _ = oracle.route(logits.cpu().numpy(), w.k, num_tokens=nt)
+    got = idx.cpu().numpy()
+    for s_ in range(w.R):
+        np.testing.assert_array_equal(got[s_, :nt[s_]], ridx[s_, :nt[s_]])
+        assert (got[s_, nt[s_]:] == -9).all()
+        assert (gate.cpu().numpy()[s_, nt[s_]:] == -1.0).all()

@@ -210,6 +210,17 @@ def make_x(w: Workload, seed: int = 0, device="cpu"):
     return x.view(w.R, w.T, w.H)
 
 
+def make_logits(w: Workload, seed: int = 0, device="cpu"):
+    """Router input: torch float32 logits [R][T][E] ~ N(0, 1) on ``device``
+    (a separate generator stream from x: seed + 7919)."""
+    import torch
+
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(int(seed) + 7919)
+    return torch.randn((w.R, w.T, w.E), generator=g, device=dev, dtype=torch.float32)
+
+
 def bf16_bits(x) -> np.ndarray:
     """Host numpy uint16 view of a torch bf16 tensor's bit patterns."""
     import torch
