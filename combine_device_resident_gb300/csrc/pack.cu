@@ -85,6 +85,19 @@ __device__ __forceinline__ int32_t final_row(const PackArgs &a, long long tok, i
     return (int32_t)row;
 }
 
+// Shared memory after the NS stages: NS stage barriers, prefix [R + 1].
+__host__ __device__ constexpr size_t pack_tail_bytes(int stages) {
+    return (size_t)stages * 8 + 4 * (size_t)(kMaxRanks + 1);
+}
+
+// One warp per CTA; lane 0 keeps the chunk loads in flight and issues the k
+// stores of every chunk, the lanes compute the destination rows of the next
+// batch of BT = 32/k tokens (lane l: token l / k, slot l % k).  COUNTED:
+// per-rank active token counts (a.num_tokens); PADDED: stores go to the
+// padded send buffer.  Both are compile-time, so the plain instantiation
+// keeps the shortest issue loop (measured: the issuing lane's scalar work
+// between copy-engine waits shows up directly in the kernel's time).
+template <bool COUNTED, bool PADDED>
 __global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const Geometry &g = a.g;
@@ -98,8 +111,7 @@ __global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
     // contiguous ranges of all tokens would leave most CTAs idle.  Active
     // index ia maps to rank s (prefix[s] <= ia < prefix[s+1]) and token
     // ia - prefix[s]; without counts the map is the identity.
-    const bool counted = a.num_tokens != nullptr;
-    if (counted) {
+    if (COUNTED) {
         int carry = 0;
         for (int c0 = 0; c0 < g.R; c0 += 32) {
             const int s = c0 + lane;
@@ -116,9 +128,9 @@ __global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
         if (lane == 0) prefix[g.R] = carry;
         __syncwarp();
     }
-    const long long nact = counted ? (long long)prefix[g.R] : (long long)g.R * g.T;
+    const long long nact = COUNTED ? (long long)prefix[g.R] : (long long)g.R * g.T;
     auto token_of = [&](long long ia) -> long long {
-        if (!counted) return ia;
+        if (!COUNTED) return ia;
         int lo = 0, hi = g.R - 1;  // the last rank whose prefix is <= ia (skips empty ranks)
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
@@ -144,23 +156,41 @@ __global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
     }
     __syncwarp();
 
+    // Loads walk the active tokens in order: with counts, step to the next
+    // token inside a rank and search only when the rank changes.
+    long long l_ia = -1, l_tok = 0, l_end = 0;
+    auto load_token = [&](long long ia) -> long long {
+        if (!COUNTED) return ia;
+        if (ia == l_ia) return l_tok;
+        if (ia == l_ia + 1 && l_tok + 1 < l_end) {
+            l_ia = ia;
+            return ++l_tok;
+        }
+        l_ia = ia;
+        l_tok = token_of(ia);
+        const int s = (int)(l_tok / g.T);
+        l_end = (long long)s * g.T + (prefix[s + 1] - prefix[s]);
+        return l_tok;
+    };
+    // unit p = (active token ia_b + p / nch, chunk p % nch) into stage p % NS
     auto issue_load = [&](long long p) {
-        const long long tok = token_of(ia_b + p / nch);
+        const long long tok = load_token(ia_b + p / nch);
         const uint32_t off = (uint32_t)(p % nch) * CH;
         const uint32_t bytes = (uint32_t)min((size_t)CH, rowb - off);
         uint64_t *bar = &bars[p % NS];
         mbar_arrive_expect_tx(bar, bytes);
         bulk_load(smem + (size_t)(p % NS) * CH, x + (size_t)tok * rowb + off, bytes, bar);
     };
-    // Destination rows of the batch of BT active tokens starting at ib0:
-    // lane l holds assignment (token of ib0 + l / k, slot l % k).
+    // Store rows of the batch starting at active index ib0; slot_map gets the
+    // arena row, padded plans store into the padded send buffer instead.
     auto rows_of_batch = [&](long long ib0, uint32_t &ovf) -> int32_t {
         const int b = lane / g.k, j = lane - b * g.k;
         if (b >= BT || ib0 + b >= ia_e) return -1;
         const long long tok = token_of(ib0 + b);
         const int32_t row = final_row(a, tok, j, ovf);
         if (!a.rows_final) a.slot_map[(size_t)tok * g.k + j] = row;
-        return row;
+        if (!PADDED || row < 0) return row;
+        return (int32_t)send_row_of(a, row, (int)(tok / g.T));
     };
     // Loads may run NS - LAG units ahead; up to LAG store groups may still be
     // reading their stage when the next load is issued.
@@ -199,13 +229,9 @@ __global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
         const uint32_t bytes = (uint32_t)min((size_t)CH, rowb - off);
         const int lb = (int)(ia - ib0);
         if (lane == 0) fence_proxy_async_smem();
-        const int s_tok = a.padded_tk ? (int)(token_of(ia) / g.T) : 0;
         for (int j = 0; j < g.k; ++j) {
             const int32_t rj = __shfl_sync(kFull, cur, lb * g.k + j);
-            if (lane == 0 && rj >= 0) {
-                const long long dst = a.padded_tk ? send_row_of(a, rj, s_tok) : (long long)rj;
-                if (dst >= 0) bulk_store(recv + (size_t)dst * rowb + off, smem + (size_t)st * CH, bytes);
-            }
+            if (lane == 0 && rj >= 0) bulk_store(recv + (size_t)rj * rowb + off, smem + (size_t)st * CH, bytes);
         }
         if (lane == 0) {
             bulk_commit();
@@ -258,7 +284,7 @@ __global__ void __launch_bounds__(256) pack_lsu_kernel(const PackArgs a) {
             for (int j = 0; j < g.k; ++j) {
                 const int32_t rj = __shfl_sync(kFull, row, j);
                 if (rj < 0) continue;
-                const long long drow = a.padded_tk ? send_row_of(a, rj, (int)(u / g.T)) : (long long)rj;
+                const long long drow = a.padded_tk ? send_row_of(a, rj, s_tok) : (long long)rj;
                 if (drow < 0) continue;
                 char *dst = reinterpret_cast<char *>(a.recv) + (size_t)drow * rowb;
 #pragma unroll
@@ -336,13 +362,18 @@ cudaError_t configure_pack(a2av_plan_s &p) {
     size_t chunk = p.cfg.pack_stage_bytes > 0 ? (size_t)p.cfg.pack_stage_bytes : (wide ? 2048 : kTmaChunkMax);
     chunk = (chunk + 15) / 16 * 16;
     if (chunk > rowb) chunk = rowb;
-    int max_optin = 0;
+    int max_optin = 0, per_sm = 0, reserved = 0;
     cudaError_t e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p.cfg.device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, p.cfg.device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, p.cfg.device);
     if (e != cudaSuccess) return e;
-    size_t budget = (size_t)max_optin / ctas_per_sm;
-    budget = budget > 2048 ? budget - 2048 : budget;  // leave room for the static/runtime reservation
-    const size_t prefix_bytes = 4 * (size_t)(kMaxRanks + 1);
-    budget = budget > prefix_bytes ? budget - prefix_bytes : budget;
+    // ctas_per_sm CTAs share the SM's shared memory, each with the runtime's
+    // per-block reservation on top of its dynamic size
+    size_t budget = (size_t)per_sm / ctas_per_sm;
+    budget = budget > (size_t)reserved ? budget - reserved : 0;
+    if (budget > (size_t)max_optin) budget = max_optin;
+    const size_t tail0 = pack_tail_bytes(0);  // prefix
+    budget = budget > tail0 ? budget - tail0 : budget;
     // at least two stages: shrink the chunk if the requested one does not fit
     while (chunk > 256 && 2 * (chunk + 8) > budget) chunk = (chunk / 2 + 15) / 16 * 16;
     const int nch2 = (int)((rowb + chunk - 1) / chunk);
@@ -356,11 +387,16 @@ cudaError_t configure_pack(a2av_plan_s &p) {
     p.pack_nchunks = nch2;
     p.pack_stages = stages;
     p.pack.block = 32;
-    p.pack.smem = (size_t)stages * chunk + (size_t)stages * 8 + prefix_bytes;
+    p.pack.smem = (size_t)stages * chunk + pack_tail_bytes(stages);
     p.pack.grid = p.num_sms * ctas_per_sm;
     // The attribute is a per-kernel cap shared by every plan: raise it to the
     // device maximum (never lower it to this plan's size).
-    return cudaFuncSetAttribute(pack_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
+    for (auto kern : {pack_tma_kernel<false, false>, pack_tma_kernel<false, true>, pack_tma_kernel<true, false>,
+                      pack_tma_kernel<true, true>}) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 
@@ -378,7 +414,10 @@ cudaError_t launch_pack(const a2av_plan_s &p, const PackArgs &a, cudaStream_t s)
         b.nchunks = p.pack_nchunks;
         b.stages = p.pack_stages;
         b.lag = p.pack_lag;
-        e = launch_pdl(pack_tma_kernel, p.pack.grid, p.pack.block, p.pack.smem, s, b);
+        const bool counted = b.num_tokens != nullptr, padded = b.padded_tk != 0;
+        auto kern = counted ? (padded ? pack_tma_kernel<true, true> : pack_tma_kernel<true, false>)
+                            : (padded ? pack_tma_kernel<false, true> : pack_tma_kernel<false, false>);
+        e = launch_pdl(kern, p.pack.grid, p.pack.block, p.pack.smem, s, b);
     } else {
         e = launch_pdl(pack_lsu_kernel<kLsuUnroll>, p.pack.grid, p.pack.block, 0, s, b);
     }
