@@ -16,8 +16,14 @@ something other than itself, in ``tests/test_oracle_pins.py``):
                     offsets, window bases) and exhaustive brute force on tiny
                     routings;
 * ``slot_map`` / ``dispatch`` -- brute force (window d = a stable sort of all
-                    assignments sent to d by key (source, expert, token, slot)),
-                    bijection onto [0, R*T*k), recv[slot] == x bit for bit;
+                    assignments sent to d by key (source, expert, token, slot),
+                    or (expert, source, token, slot) in the expert-grouped
+                    receive order), bijection onto [0, R*T*k), recv[slot] == x
+                    bit for bit; the expert-order dispatch (regroup of the
+                    source-order windows) against the direct offset formula
+                    of ``slot_map``;
+* ``recv_expert_offsets`` -- every window tiled by its (source, expert) blocks
+                    in the order of the layout, against the brute-force rows;
 * ``combine``    -- closed forms independent of the layout (unit weights and
                     identity experts give bf16(k*x), k in {1, 2, 4, 8}; gate sum
                     times x), numpy float32 with separate roundings, and the fp64
@@ -65,7 +71,9 @@ def bind(L):
     vp = ctypes.c_void_p  # optional int32 array (NULL = every token takes part)
     L.oracle_splits.argtypes = [ci, ci, ci, ci, ci, ci64, vp, i32p] + [i32p] * 7
     L.oracle_slot_map.restype = ctypes.c_uint32
-    L.oracle_slot_map.argtypes = [ci, ci, ci, ci, ci, ci64, vp, i32p, i32p, i32p, i32p, i32p]
+    L.oracle_slot_map.argtypes = [ci, ci, ci, ci, ci, ci64, vp, i32p, i32p, i32p, i32p, i32p, i32p]
+    L.oracle_recv_expert_offsets.restype = None
+    L.oracle_recv_expert_offsets.argtypes = [ci, ci, ci, i32p, i32p, i32p]
     L.oracle_dispatch.restype = ctypes.c_uint32
     L.oracle_dispatch.argtypes = [ci, ci, ci, ci, ci, ci, ci64, vp, u16p, i32p, i32p, i32p, i32p, i32p,
                                   u16p, i32p]
@@ -110,7 +118,10 @@ def _counts_ptr(num_tokens):
     return arr.ctypes.data_as(ctypes.c_void_p), arr
 
 
-def _mode(window_mode) -> int:
+ORDER_EXPERT = 0x100  # receive order flag on the C side's window_mode
+
+
+def _layout(window_mode) -> int:
     if window_mode in (0, "packed"):
         return 0
     if window_mode in (1, "fixed"):
@@ -120,9 +131,23 @@ def _mode(window_mode) -> int:
     raise ValueError(window_mode)
 
 
-def splits(R: int, E: int, idx: np.ndarray, window_mode="packed", window_rows: int = 0, num_tokens=None) -> dict:
+def _mode(window_mode, recv_order="source") -> int:
+    """Layout | receive order, as the C functions take it."""
+    m = _layout(window_mode)
+    if recv_order in (1, "expert"):
+        if m == 2:
+            raise ValueError("the expert-grouped receive order is not defined for the padded layout")
+        return m | ORDER_EXPERT
+    if recv_order not in (0, "source"):
+        raise ValueError(recv_order)
+    return m
+
+
+def splits(R: int, E: int, idx: np.ndarray, window_mode="packed", window_rows: int = 0, num_tokens=None,
+           recv_order="source") -> dict:
     """Counts and offsets of one dispatch.  idx int32 [R][T][k]; num_tokens
-    int32 [R] (optional): only tokens t < num_tokens[s] take part."""
+    int32 [R] (optional): only tokens t < num_tokens[s] take part; recv_order
+    "source" (AllToAllv convention) or "expert" (expert-grouped windows)."""
     idx = np.ascontiguousarray(idx, dtype=np.int32)
     _, T, k = idx.shape
     if E % R:
@@ -142,29 +167,33 @@ def splits(R: int, E: int, idx: np.ndarray, window_mode="packed", window_rows: i
                              out["send_counts"], out["send_offsets"], out["recv_counts"],
                              out["recv_offsets"], out["recv_expert_counts"], out["recv_total"],
                              out["window_base"])
+    out["recv_expert_offsets"] = np.zeros((R, R, epr), np.int32)
+    lib().oracle_recv_expert_offsets(R, E, _mode(window_mode, recv_order), out["recv_offsets"],
+                                     out["recv_expert_counts"], out["recv_expert_offsets"])
     out["status"] = int(st)
     return out
 
 
 def slot_map(R: int, E: int, idx: np.ndarray, sp: dict, window_mode="packed", window_rows: int = 0,
-             num_tokens=None):
+             num_tokens=None, recv_order="source"):
     """(slot_map int32 [R][T][k], status) without moving any payload."""
     idx = np.ascontiguousarray(idx, dtype=np.int32)
     _, T, k = idx.shape
     sm = np.empty((R, T, k), np.int32)
     nt, _keep = _counts_ptr(num_tokens)
-    st = lib().oracle_slot_map(R, E, T, k, _mode(window_mode), int(window_rows), nt, idx,
-                               sp["send_offsets"], sp["recv_offsets"], sp["window_base"], sm)
+    st = lib().oracle_slot_map(R, E, T, k, _mode(window_mode, recv_order), int(window_rows), nt, idx,
+                               sp["send_offsets"], sp["recv_offsets"], sp["recv_expert_offsets"],
+                               sp["window_base"], sm)
     return sm, int(st)
 
 
 def arena_rows(R: int, T: int, k: int, window_mode="packed", window_rows: int = 0) -> int:
-    m = _mode(window_mode)
+    m = _layout(window_mode)
     return R * T * k if m == 0 else (R * int(window_rows) if m == 1 else R * R * T * k)
 
 
 def dispatch(R: int, E: int, x: np.ndarray, idx: np.ndarray, sp: dict, window_mode="packed",
-             window_rows: int = 0, recv: Optional[np.ndarray] = None, num_tokens=None):
+             window_rows: int = 0, recv: Optional[np.ndarray] = None, num_tokens=None, recv_order="source"):
     """(recv uint16 [rows][H], slot_map, status).  x uint16 bf16 bits [R][T][H].
     Rows no assignment reaches keep their prior contents (zeros if recv is None)."""
     x = np.ascontiguousarray(x, dtype=np.uint16)
@@ -176,7 +205,7 @@ def dispatch(R: int, E: int, x: np.ndarray, idx: np.ndarray, sp: dict, window_mo
         recv = np.zeros((rows, H), np.uint16)
     sm = np.empty((R, T, k), np.int32)
     nt, _keep = _counts_ptr(num_tokens)
-    st = lib().oracle_dispatch(R, E, T, H, k, _mode(window_mode), int(window_rows), nt, x, idx,
+    st = lib().oracle_dispatch(R, E, T, H, k, _mode(window_mode, recv_order), int(window_rows), nt, x, idx,
                                sp["send_counts"], sp["send_offsets"], sp["recv_offsets"],
                                sp["window_base"], recv, sm)
     return recv, sm, int(st)
@@ -242,12 +271,14 @@ def f32_to_bf16(v: float) -> int:
     return int(lib().oracle_f32_to_bf16(float(v)))
 
 
-def run_all(R, E, x, idx, gate, window_mode="packed", window_rows=0, expert="identity", num_tokens=None):
+def run_all(R, E, x, idx, gate, window_mode="packed", window_rows=0, expert="identity", num_tokens=None,
+            recv_order="source"):
     """The whole path on the CPU: splits, dispatch, expert stand-in, combine.
     With num_tokens, out rows of tokens that do not take part are zero here
     (the combine produces nothing for them)."""
-    sp = splits(R, E, idx, window_mode, window_rows, num_tokens)
-    recv, sm, st = dispatch(R, E, x, idx, sp, window_mode, window_rows, num_tokens=num_tokens)
+    sp = splits(R, E, idx, window_mode, window_rows, num_tokens, recv_order)
+    recv, sm, st = dispatch(R, E, x, idx, sp, window_mode, window_rows, num_tokens=num_tokens,
+                            recv_order=recv_order)
     y = expert_scale(E, recv, idx, sm) if expert == "scale" else recv
     T = idx.shape[1]
     if num_tokens is None:

@@ -45,6 +45,17 @@
  *       P3 section 7, double buffering];
  *   R8  the router (top-k of per-token logits, softmax gates): see
  *       oracle_route below;
+ *   R9  receive order: the AllToAllv convention (R3) leaves window d in
+ *       source order, and inside each source's segment the rows are sorted by
+ *       expert.  The expert-grouped view is the same window regrouped so that
+ *       each local expert's rows are contiguous, the step after the exchange
+ *       that feeds one GEMM per expert [P1 Inference, Figure 13: the received
+ *       tokens go to their experts' FFN].  Reading: window d holds local
+ *       expert 0's rows, then local expert 1's, and so on; inside an expert,
+ *       source 0's rows, then source 1's, each in the order its segment had
+ *       (token, then slot).  The counts are those of the source order; only
+ *       the places differ.  Selected by ORACLE_ORDER_EXPERT in window_mode;
+ *       not defined for the padded layout;
  *   R6  error handling: an expert id outside [0, E) is dropped (not counted,
  *       slot -1, status bit 0); in fixed mode a row whose window-relative
  *       position is >= W is dropped (slot -1, status bit 1) while the counts
@@ -57,6 +68,9 @@
  *   send_counts, send_offsets    int32 [R][E]
  *   recv_counts, recv_offsets    int32 [R][R]      (destination-major: [d][s])
  *   recv_expert_counts           int32 [R][R][E/R] ([d][s][local expert])
+ *   recv_expert_offsets          int32 [R][R][E/R] ([d][s][local expert]):
+ *                                window-relative first row of the rows
+ *                                source s sends to local expert le of rank d
  *   recv_total, window_base      int32 [R]
  *   recv, y    uint16 bf16 bits  [rows][H]
  *   slot_map   int32             [R][T][k]
@@ -68,6 +82,9 @@
 
 #define ORACLE_BAD_EXPERT 1u
 #define ORACLE_WINDOW_OVERFLOW 2u
+/* window_mode = layout (0 packed, 1 fixed, 2 padded) | receive order (R9) */
+#define ORACLE_ORDER_EXPERT 0x100
+#define ORACLE_LAYOUT(m) ((m) & 0xff)
 
 /* ---- bf16 <-> fp32 (bf16 = top 16 bits of an IEEE binary32) ---------------- */
 
@@ -125,6 +142,7 @@ uint32_t oracle_splits(int R, int E, int T, int k, int window_mode, int64_t wind
 {
     uint32_t status = 0;
     int epr = E / R;
+    window_mode = ORACLE_LAYOUT(window_mode);
     for (int s = 0; s < R; ++s) {
         int32_t *cnt = send_counts + (size_t)s * E;
         for (int e = 0; e < E; ++e)
@@ -179,6 +197,39 @@ uint32_t oracle_splits(int R, int E, int T, int k, int window_mode, int64_t wind
     return status;
 }
 
+/* ---- where each (source, local expert) block starts in its window -----------
+ * Source order (R3): source s's segment starts at recv_offsets[d][s] and is
+ * sorted by expert, so its rows for local expert le start after its rows for
+ * the lower local experts:
+ *   recv_offsets[d][s] + sum over le' < le of recv_expert_counts[d][s][le'].
+ * Expert order (R9): all rows of the lower local experts come first, then the
+ * rows of expert le from the lower sources:
+ *   sum over le' < le, all s' of recv_expert_counts[d][s'][le']
+ *     + sum over s' < s of recv_expert_counts[d][s'][le].
+ */
+void oracle_recv_expert_offsets(int R, int E, int window_mode, const int32_t *recv_offsets,
+                                const int32_t *recv_expert_counts, int32_t *recv_expert_offsets)
+{
+    int epr = E / R;
+    for (int d = 0; d < R; ++d)
+        for (int s = 0; s < R; ++s)
+            for (int le = 0; le < epr; ++le) {
+                int64_t v = 0;
+                if (window_mode & ORACLE_ORDER_EXPERT) {
+                    for (int l2 = 0; l2 < le; ++l2)
+                        for (int s2 = 0; s2 < R; ++s2)
+                            v += recv_expert_counts[((size_t)d * R + s2) * epr + l2];
+                    for (int s2 = 0; s2 < s; ++s2)
+                        v += recv_expert_counts[((size_t)d * R + s2) * epr + le];
+                } else {
+                    v = recv_offsets[(size_t)d * R + s];
+                    for (int l2 = 0; l2 < le; ++l2)
+                        v += recv_expert_counts[((size_t)d * R + s) * epr + l2];
+                }
+                recv_expert_offsets[((size_t)d * R + s) * epr + le] = (int32_t)v;
+            }
+}
+
 /* ---- step 2: the expert sort of one rank's send buffer ---------------------
  * send_pos[t][j] = position of assignment (t, j) of rank s in its
  * expert-sorted send buffer: send_offsets[s][e] + the number of earlier
@@ -219,11 +270,13 @@ static void send_positions(int E, int T, int Ts, int k, const int32_t *idx_s, co
  */
 uint32_t oracle_slot_map(int R, int E, int T, int k, int window_mode, int64_t window_rows,
                          const int32_t *num_tokens, const int32_t *idx, const int32_t *send_offsets,
-                         const int32_t *recv_offsets, const int32_t *window_base,
-                         int32_t *slot_map)
+                         const int32_t *recv_offsets, const int32_t *recv_expert_offsets,
+                         const int32_t *window_base, int32_t *slot_map)
 {
     uint32_t status = 0;
     int epr = E / R;
+    int expert_order = (window_mode & ORACLE_ORDER_EXPERT) != 0;
+    window_mode = ORACLE_LAYOUT(window_mode);
     int32_t *running = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
     int32_t *pos = (int32_t *)malloc(sizeof(int32_t) * (size_t)T * k + 4);
     for (int s = 0; s < R; ++s) {
@@ -241,6 +294,8 @@ uint32_t oracle_slot_map(int R, int E, int T, int k, int window_mode, int64_t wi
             }
             int d = e / epr;
             int64_t rel = (int64_t)recv_offsets[(size_t)d * R + s] + (pos[a] - so[d * epr]);
+            if (expert_order) /* R9: the block of (s, e), then the rank inside it */
+                rel = (int64_t)recv_expert_offsets[((size_t)d * R + s) * epr + (e - d * epr)] + (pos[a] - so[e]);
             if (window_mode == 1 && rel >= window_rows) {
                 *slot = -1;
                 status |= ORACLE_WINDOW_OVERFLOW;
@@ -261,12 +316,21 @@ uint32_t oracle_slot_map(int R, int E, int T, int k, int window_mode, int64_t wi
  * destination's window, rows in order.  Rows whose slot is -1 are not
  * written (R6).  Also fills slot_map (as oracle_slot_map).  Returns status.
  */
+static uint32_t dispatch_expert_order(int R, int E, int T, int H, int k, int layout, int64_t window_rows,
+                                      const int32_t *num_tokens, const uint16_t *x, const int32_t *idx,
+                                      const int32_t *send_counts, const int32_t *send_offsets,
+                                      const int32_t *recv_offsets, const int32_t *window_base,
+                                      uint16_t *recv, int32_t *slot_map);
+
 uint32_t oracle_dispatch(int R, int E, int T, int H, int k, int window_mode, int64_t window_rows,
                          const int32_t *num_tokens, const uint16_t *x, const int32_t *idx,
                          const int32_t *send_counts, const int32_t *send_offsets,
                          const int32_t *recv_offsets, const int32_t *window_base,
                          uint16_t *recv, int32_t *slot_map)
 {
+    if (window_mode & ORACLE_ORDER_EXPERT)
+        return dispatch_expert_order(R, E, T, H, k, ORACLE_LAYOUT(window_mode), window_rows, num_tokens, x, idx,
+                                     send_counts, send_offsets, recv_offsets, window_base, recv, slot_map);
     uint32_t status = 0;
     int epr = E / R;
     size_t row_bytes = sizeof(uint16_t) * (size_t)H;
@@ -321,6 +385,73 @@ uint32_t oracle_dispatch(int R, int E, int T, int H, int k, int window_mode, int
     free(sendbuf);
     free(pos);
     free(running);
+    return status;
+}
+
+/* ---- the expert-grouped receive order (R9) ------------------------------------
+ * Literally: perform the source-order dispatch above into windows with no
+ * capacity limit (packed, back to back), then regroup every window: for local
+ * expert le = 0.. and, inside it, source s = 0.., take source s's rows for
+ * expert le -- in the source-order window they are the block starting at
+ * recv_offsets[d][s] + (s's rows for the lower local experts), because each
+ * segment is sorted by expert -- and append them to window d.  In fixed mode
+ * rows appended at position >= W are dropped (R6).  slot_map follows each
+ * row to its new place.
+ */
+static uint32_t dispatch_expert_order(int R, int E, int T, int H, int k, int layout, int64_t window_rows,
+                                      const int32_t *num_tokens, const uint16_t *x, const int32_t *idx,
+                                      const int32_t *send_counts, const int32_t *send_offsets,
+                                      const int32_t *recv_offsets, const int32_t *window_base,
+                                      uint16_t *recv, int32_t *slot_map)
+{
+    int epr = E / R;
+    size_t row_bytes = sizeof(uint16_t) * (size_t)H;
+    int32_t *tbase = (int32_t *)calloc((size_t)R + 1, sizeof(int32_t));
+    int64_t rows = 0;
+    for (int d = 0; d < R; ++d) {
+        tbase[d] = (int32_t)rows;
+        for (int s = 0; s < R; ++s)
+            for (int le = 0; le < epr; ++le)
+                rows += send_counts[(size_t)s * E + d * epr + le];
+    }
+    uint16_t *tmp = (uint16_t *)malloc(row_bytes * (size_t)rows + 16);
+    int32_t *tslot = (int32_t *)malloc(sizeof(int32_t) * (size_t)R * T * k + 4);
+    int64_t *moved = (int64_t *)malloc(sizeof(int64_t) * (size_t)rows + 8);
+    uint32_t status = oracle_dispatch(R, E, T, H, k, 0, 0, num_tokens, x, idx, send_counts, send_offsets,
+                                      recv_offsets, tbase, tmp, tslot);
+    for (int d = 0; d < R; ++d) {
+        int64_t run = 0;
+        for (int le = 0; le < epr; ++le)
+            for (int s = 0; s < R; ++s) {
+                const int32_t *sc = send_counts + (size_t)s * E + d * epr;
+                int64_t start = recv_offsets[(size_t)d * R + s];
+                for (int l2 = 0; l2 < le; ++l2)
+                    start += sc[l2];
+                for (int32_t i = 0; i < sc[le]; ++i, ++run) {
+                    int64_t from = tbase[d] + start + i;
+                    if (layout == 1 && run >= window_rows) {
+                        moved[from] = -1;
+                        status |= ORACLE_WINDOW_OVERFLOW;
+                        continue;
+                    }
+                    memcpy(recv + ((size_t)window_base[d] + (size_t)run) * H, tmp + (size_t)from * H, row_bytes);
+                    moved[from] = run;
+                }
+            }
+    }
+    for (size_t a = 0; a < (size_t)R * T * k; ++a) {
+        if (tslot[a] < 0) {
+            slot_map[a] = -1;
+            continue;
+        }
+        int d = idx[a] / epr;
+        int64_t r = moved[tslot[a]];
+        slot_map[a] = r < 0 ? -1 : (int32_t)(window_base[d] + r);
+    }
+    free(moved);
+    free(tslot);
+    free(tmp);
+    free(tbase);
     return status;
 }
 

@@ -31,7 +31,7 @@ SPLIT_KEYS = ["send_counts", "send_offsets", "recv_counts", "recv_offsets",
 # ----------------------------------------------------------------------------
 # brute force: an independent formulation from sorted per-destination lists
 # ----------------------------------------------------------------------------
-def brute_force(R, E, idx, window_mode="packed", window_rows=0):
+def brute_force(R, E, idx, window_mode="packed", window_rows=0, recv_order="source"):
     idx = np.asarray(idx)
     _, T, k = idx.shape
     epr = E // R
@@ -39,6 +39,10 @@ def brute_force(R, E, idx, window_mode="packed", window_rows=0):
     valid = [it for it in items if 0 <= it[1] < E]
     status = 0 if len(valid) == len(items) else oracle.BAD_EXPERT
     windows = [sorted(it for it in valid if it[1] // epr == d) for d in range(R)]
+    # the order rows take inside a window: (source, expert, token, slot), or
+    # (expert, source, token, slot) for the expert-grouped view
+    order = (lambda it: it) if recv_order == "source" else (lambda it: (it[1], it[0], it[2], it[3]))
+    placed = [sorted(w, key=order) for w in windows]
     per_src = [sorted((e, t, j) for (s2, e, t, j) in valid if s2 == s) for s in range(R)]
     out = {
         "send_counts": np.array([[sum(1 for it in per_src[s] if it[0] == e) for e in range(E)] for s in range(R)]),
@@ -61,8 +65,17 @@ def brute_force(R, E, idx, window_mode="packed", window_rows=0):
         out["recv_offsets"] = np.array([[src * T * k for src in range(R)] for _ in range(R)])
     else:
         out["window_base"] = np.array([sum(len(w) for w in windows[:d]) for d in range(R)])
+    # first row of each (source, local expert) block: the rows placed before it
+    if window_mode == "padded":
+        out["recv_expert_offsets"] = np.array(
+            [[[s * T * k + sum(1 for it in windows[d] if it[0] == s and it[1] < d * epr + le)
+               for le in range(epr)] for s in range(R)] for d in range(R)])
+    else:
+        out["recv_expert_offsets"] = np.array(
+            [[[sum(1 for it in placed[d] if order(it)[:2] < order((s, d * epr + le, 0, 0))[:2])
+               for le in range(epr)] for s in range(R)] for d in range(R)])
     slot = -np.ones((R, T, k), dtype=np.int64)
-    for d, w in enumerate(windows):
+    for d, w in enumerate(placed):
         for pos, (s, e, t, j) in enumerate(w):
             if window_mode == "fixed" and pos >= window_rows:
                 continue
@@ -77,15 +90,32 @@ def brute_force(R, E, idx, window_mode="packed", window_rows=0):
     return out
 
 
-def check_against_brute(R, E, idx, window_mode="packed", window_rows=0):
-    bf = brute_force(R, E, idx, window_mode, window_rows)
-    sp = oracle.splits(R, E, idx, window_mode, window_rows)
-    for key in SPLIT_KEYS:
+def check_against_brute(R, E, idx, window_mode="packed", window_rows=0, recv_order="source"):
+    bf = brute_force(R, E, idx, window_mode, window_rows, recv_order)
+    sp = oracle.splits(R, E, idx, window_mode, window_rows, recv_order=recv_order)
+    for key in SPLIT_KEYS + ["recv_expert_offsets"]:
         np.testing.assert_array_equal(sp[key], bf[key].reshape(sp[key].shape), err_msg=key)
-    sm, st = oracle.slot_map(R, E, idx, sp, window_mode, window_rows)
+    sm, st = oracle.slot_map(R, E, idx, sp, window_mode, window_rows, recv_order=recv_order)
     np.testing.assert_array_equal(sm, bf["slot_map"], err_msg="slot_map")
     assert (sp["status"] | st) == bf["status"]
     return sp, sm
+
+
+def check_dispatch_against_brute(R, E, idx, window_mode="packed", window_rows=0, recv_order="source", H=3):
+    """The dispatch (payload moved the literal way) lands every row where the
+    brute force puts it, carrying its token's bits."""
+    bf = brute_force(R, E, idx, window_mode, window_rows, recv_order)
+    T = idx.shape[1]
+    x = (np.arange(R * T * H, dtype=np.uint32).reshape(R, T, H) * 7 + 0x3F80).astype(np.uint16)
+    sp = oracle.splits(R, E, idx, window_mode, window_rows, recv_order=recv_order)
+    recv, sm, st = oracle.dispatch(R, E, x, idx, sp, window_mode, window_rows, recv_order=recv_order)
+    np.testing.assert_array_equal(sm, bf["slot_map"], err_msg="dispatch slot_map")
+    for s_ in range(R):
+        for t in range(T):
+            for j in range(idx.shape[2]):
+                if sm[s_, t, j] >= 0:
+                    np.testing.assert_array_equal(recv[sm[s_, t, j]], x[s_, t])
+    assert (sp["status"] | st) == bf["status"]
 
 
 # ----------------------------------------------------------------------------
@@ -117,6 +147,96 @@ def test_hand_worked_example():
     np.testing.assert_array_equal(sm2, sm)
     assert recv.tolist() == [x[0, 1].tolist(), x[1, 0].tolist(), x[1, 2].tolist(),
                              x[0, 0].tolist(), x[0, 2].tolist(), x[1, 1].tolist()]
+
+
+def test_hand_worked_example_expert_order():
+    # The routing of the example above.  Window 1 holds experts 2 and 3; in
+    # the expert-grouped view expert 2's rows come first: (s1,e2,t1) -> row 3,
+    # then expert 3's: (s0,e3,t0) -> 4, (s0,e3,t2) -> 5.  Window 0 is the same
+    # in both orders: (s0,e0,t1) -> 0, (s1,e1,t0) -> 1, (s1,e1,t2) -> 2.
+    # recv_expert_offsets[d][s][le], expert order: window 0: expert 0 starts
+    # at 0 (s0 there, s1 after s0's 1 row), expert 1 at 1 (s0: 1, s1: 1 + 0);
+    # window 1: expert 2 at 0 (s0: 0, s1: 0), expert 3 at 1 (s0: 1, s1: 1+2).
+    # Source order: window 1's segments start at 0 (s0) and 2 (s1); s0 has no
+    # expert-2 rows, so its expert-3 block also starts at 0; s1's expert-3
+    # block starts after its one expert-2 row, at 3.
+    idx = np.array([[[3], [0], [3]], [[1], [2], [1]]], np.int32)
+    ex = oracle.splits(2, 4, idx, recv_order="expert")
+    src = oracle.splits(2, 4, idx)
+    for key in SPLIT_KEYS:
+        np.testing.assert_array_equal(ex[key], src[key], err_msg=key)
+    assert ex["recv_expert_offsets"].tolist() == [[[0, 1], [1, 1]], [[0, 1], [0, 3]]]
+    assert src["recv_expert_offsets"].tolist() == [[[0, 1], [1, 1]], [[0, 0], [2, 3]]]
+    sm, st = oracle.slot_map(2, 4, idx, ex, recv_order="expert")
+    assert st == 0
+    assert sm[..., 0].tolist() == [[4, 0, 5], [1, 3, 2]]
+    x = np.arange(2 * 3 * 2, dtype=np.uint16).reshape(2, 3, 2) + 0x3F00
+    recv, sm2, st2 = oracle.dispatch(2, 4, x, idx, ex, recv_order="expert")
+    np.testing.assert_array_equal(sm2, sm)
+    assert recv.tolist() == [x[0, 1].tolist(), x[1, 0].tolist(), x[1, 2].tolist(),
+                             x[1, 1].tolist(), x[0, 0].tolist(), x[0, 2].tolist()]
+
+
+@pytest.mark.parametrize("order", ["source", "expert"])
+def test_exhaustive_expert_order_r2_e4(order):
+    R, E, k, T = 2, 4, 1, 3
+    for combo in itertools.product(range(E), repeat=R * T * k):
+        idx = np.array(combo, np.int32).reshape(R, T, k)
+        check_against_brute(R, E, idx, recv_order=order)
+    pairs = [p for p in itertools.product(range(E), repeat=2) if p[0] != p[1]]
+    for combo in itertools.product(pairs, repeat=R):
+        check_dispatch_against_brute(R, E, np.array(combo, np.int32).reshape(R, 1, 2), recv_order=order)
+
+
+def test_expert_order_random_fixed_and_active_against_brute():
+    rng = np.random.default_rng(31)
+    for R, E, T, k in [(1, 3, 5, 2), (3, 6, 7, 2), (4, 8, 9, 3), (4, 16, 20, 4)]:
+        for _ in range(8):
+            idx = rng.integers(0, E, size=(R, T, k), dtype=np.int32)
+            check_against_brute(R, E, idx, recv_order="expert")
+            check_dispatch_against_brute(R, E, idx, recv_order="expert")
+            for W_ in (R * T * k, 7, 1):
+                check_against_brute(R, E, idx, "fixed", W_, recv_order="expert")
+                check_dispatch_against_brute(R, E, idx, "fixed", W_, recv_order="expert")
+            # tokens past num_tokens[s] take no part, in this order too
+            nt = rng.integers(0, T + 1, size=R).astype(np.int32)
+            masked = idx.copy()
+            for s_ in range(R):
+                masked[s_, nt[s_]:] = -1
+            bf = brute_force(R, E, masked, recv_order="expert")
+            sp = oracle.splits(R, E, idx, num_tokens=nt, recv_order="expert")
+            np.testing.assert_array_equal(sp["recv_expert_offsets"], bf["recv_expert_offsets"])
+            sm, st = oracle.slot_map(R, E, idx, sp, num_tokens=nt, recv_order="expert")
+            np.testing.assert_array_equal(sm, bf["slot_map"])
+            assert st == 0
+    with pytest.raises(ValueError):
+        oracle.splits(2, 4, np.zeros((2, 1, 1), np.int32), "padded", recv_order="expert")
+
+
+def test_expert_order_blocks_tile_each_window():
+    # each local expert's rows are one contiguous block, its sources back to
+    # back, and the blocks tile [0, recv_total[d]) in expert order
+    rng = np.random.default_rng(3)
+    R, E, T, k = 4, 16, 40, 4
+    idx = np.stack([np.stack([rng.choice(E, k, replace=False) for _ in range(T)]) for _ in range(R)]).astype(np.int32)
+    sp = oracle.splits(R, E, idx, recv_order="expert")
+    reo, rec = sp["recv_expert_offsets"], sp["recv_expert_counts"]
+    sm, _ = oracle.slot_map(R, E, idx, sp, recv_order="expert")
+    epr = E // R
+    for d in range(R):
+        nxt = 0
+        for le in range(epr):
+            for s_ in range(R):
+                assert reo[d, s_, le] == nxt
+                nxt += rec[d, s_, le]
+        assert nxt == sp["recv_total"][d]
+    rel = sm - sp["window_base"][idx // epr]
+    le_of = idx % epr
+    for d in range(R):
+        for le in range(epr):
+            rows = np.sort(rel[(idx // epr == d) & (le_of == le)])
+            lo = reo[d, 0, le]
+            np.testing.assert_array_equal(rows, np.arange(lo, lo + rows.size))
 
 
 @pytest.mark.parametrize("T", [1, 2, 3])
@@ -456,8 +576,13 @@ def test_bf16_rounding_matches_torch():
 # mutation checks: plant a mistake in a copy of the oracle, the pins must fail
 # ----------------------------------------------------------------------------
 MUTANTS = {
-    "transposed recv_offsets": ("(int64_t)recv_offsets[(size_t)d * R + s] + (pos[a] - so[d * epr]);\n            if (window_mode == 1 && rel >= window_rows) {\n                *slot = -1;\n                status",
-                                "(int64_t)recv_offsets[(size_t)s * R + d] + (pos[a] - so[d * epr]);\n            if (window_mode == 1 && rel >= window_rows) {\n                *slot = -1;\n                status"),
+    "transposed recv_offsets": ("(int64_t)recv_offsets[(size_t)d * R + s] + (pos[a] - so[d * epr]);\n            if (expert_order)",
+                                "(int64_t)recv_offsets[(size_t)s * R + d] + (pos[a] - so[d * epr]);\n            if (expert_order)"),
+    "expert blocks regrouped source-major": ("        for (int le = 0; le < epr; ++le)\n            for (int s = 0; s < R; ++s) {\n                const int32_t *sc",
+                                             "        for (int s = 0; s < R; ++s)\n            for (int le = 0; le < epr; ++le) {\n                const int32_t *sc"),
+    "expert offsets count own source": ("                    for (int s2 = 0; s2 < s; ++s2)\n                        v += recv_expert_counts[((size_t)d * R + s2) * epr + le];",
+                                        "                    for (int s2 = 0; s2 <= s; ++s2)\n                        v += recv_expert_counts[((size_t)d * R + s2) * epr + le];"),
+    "expert-order rank from segment start": ("+ (e - d * epr)] + (pos[a] - so[e]);", "+ (e - d * epr)] + (pos[a] - so[d * epr]);"),
     "inclusive send_offsets": ("            send_offsets[(size_t)s * E + e] = run;\n            run += cnt[e];",
                                "            run += cnt[e];\n            send_offsets[(size_t)s * E + e] = run;"),
     "unstable sort": ("    for (int t = 0; t < T; ++t)\n        for (int j = 0; j < k; ++j) {\n            int32_t e = idx_s[(size_t)t * k + j];\n            if (t >= Ts) {",
@@ -488,6 +613,9 @@ def _pin_suite():
     test_bf16_rounding_matches_torch()
     test_padded_layout_against_brute()
     test_router_against_numpy_sort_and_softmax()
+    test_hand_worked_example_expert_order()
+    test_exhaustive_expert_order_r2_e4("expert")
+    test_expert_order_random_fixed_and_active_against_brute()
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
