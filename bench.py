@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
     ap.add_argument("--mode", choices=["dynamic", "padded"], default="dynamic",
                     help="padded: the worst-case baseline (every pair sends T*k rows)")
+    ap.add_argument("--recv-order", choices=["source", "expert"], default="source",
+                    help="rows inside each window: source segments (AllToAllv convention) or grouped by local expert")
     ap.add_argument("--router", action="store_true",
                     help="start each step from per-token logits: router kernel (top-k + softmax) first")
     ap.add_argument("--active-frac", type=float, default=1.0,
@@ -203,7 +205,7 @@ def cpu_baseline(w: W.Workload, x_host_bits, idx, gate, budget_s: float):
 
     def run(wl, xb, ix, gt):
         t = time.perf_counter()
-        oracle.run_all(wl.R, wl.E, xb, ix, gt, wl.window_mode, wl.window_rows, wl.expert)
+        oracle.run_all(wl.R, wl.E, xb, ix, gt, wl.window_mode, wl.window_rows, wl.expert, recv_order=wl.recv_order)
         return time.perf_counter() - t
 
     # probe with a small slice of tokens, then size the sample to the budget
@@ -244,17 +246,18 @@ def run_reference(args, w: W.Workload):
     xs = W.bf16_bits(W.make_x(w.scaled(T=probe_T), 0))
     wp = w.scaled(T=probe_T)
     t = time.perf_counter()
-    oracle.run_all(wp.R, wp.E, xs, idx[:, :probe_T], gate[:, :probe_T], wp.window_mode, wp.window_rows, wp.expert)
+    oracle.run_all(wp.R, wp.E, xs, idx[:, :probe_T], gate[:, :probe_T], wp.window_mode, wp.window_rows, wp.expert,
+                   recv_order=wp.recv_order)
     per_token = (time.perf_counter() - t) / probe_T
     T_s = int(max(1, min(w.T, per_step / max(per_token, 1e-9))))
     ws = w.scaled(T=T_s)
     x_s = W.bf16_bits(W.make_x(ws, 0))
     ix, gt = np.ascontiguousarray(idx[:, :T_s]), np.ascontiguousarray(gate[:, :T_s])
     for _ in range(warm):
-        oracle.run_all(ws.R, ws.E, x_s, ix, gt, ws.window_mode, ws.window_rows, ws.expert)
+        oracle.run_all(ws.R, ws.E, x_s, ix, gt, ws.window_mode, ws.window_rows, ws.expert, recv_order=ws.recv_order)
     t0 = time.perf_counter()
     for _ in range(steps):
-        oracle.run_all(ws.R, ws.E, x_s, ix, gt, ws.window_mode, ws.window_rows, ws.expert)
+        oracle.run_all(ws.R, ws.E, x_s, ix, gt, ws.window_mode, ws.window_rows, ws.expert, recv_order=ws.recv_order)
     dt = (time.perf_counter() - t0) / steps
     value = ws.algorithmic_bytes() / dt / 1e9
     sample = f"CPU oracle, one thread, first {T_s} of {w.T} tokens per rank of every rank per step"
@@ -275,7 +278,8 @@ def run_reference(args, w: W.Workload):
 
 def config_block(w: W.Workload, l2: str):
     return {"workload": w.name, "R": w.R, "E": w.E, "T": w.T, "H": w.H, "k": w.k, "routing": w.routing,
-            "gate": w.gate, "window": w.window_mode, "l2": l2, "accumulate": "fp32", "parallelism": "replicas"}
+            "gate": w.gate, "window": w.window_mode, "recv_order": w.recv_order, "l2": l2, "accumulate": "fp32",
+            "parallelism": "replicas"}
 
 
 # ---------------------------------------------------------------------------
@@ -284,6 +288,10 @@ def main():
     w = W.WORKLOADS[args.workload]
     if args.tokens:
         w = w.scaled(T=args.tokens)
+    if args.recv_order != "source":
+        import dataclasses
+
+        w = dataclasses.replace(w, recv_order=args.recv_order)
     if args.impl == "reference":
         return run_reference(args, w)
 
@@ -320,7 +328,8 @@ def main():
     plan = A.Plan(w.R, w.E, w.T, w.H, w.k, w.window_mode, w.window_rows, device=dev, flags=args.flags,
                   pack_ctas_per_sm=args.pack_ctas_per_sm, pack_stage_bytes=args.pack_stage_bytes,
                   pack_store_lag=args.pack_store_lag, combine_ctas_per_sm=args.combine_ctas_per_sm,
-                  combine_stage_bytes=args.combine_stage_bytes, combine_unroll=args.combine_unroll)
+                  combine_stage_bytes=args.combine_stage_bytes, combine_unroll=args.combine_unroll,
+                  recv_order=w.recv_order)
     recv, slot_map, out = plan.new_buffers()
     sp = plan.new_splits()
     sendbuf = plan.new_send_buffer() if padded else None

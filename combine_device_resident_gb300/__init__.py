@@ -17,6 +17,8 @@ from .binding import (  # noqa: F401
     FLAG_PACK_LSU,
     FLAG_SPLITS_TILED,
     FLAG_COMBINE_TMA,
+    ORDER_EXPERT,
+    ORDER_SOURCE,
     Plan,
     Splits,
     load_library,

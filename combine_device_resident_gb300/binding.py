@@ -26,6 +26,8 @@ DEV_WAIT_TIMEOUT = 1 << 31
 WINDOW_PACKED = 0
 WINDOW_FIXED = 1
 WINDOW_PADDED = 2
+ORDER_SOURCE = 0  # windows in source order, each source segment sorted by expert
+ORDER_EXPERT = 1  # windows grouped by local expert, sources in order inside each expert
 FLAG_PACK_LSU = 1 << 0
 FLAG_SPLITS_TILED = 1 << 1
 FLAG_COMBINE_TMA = 1 << 2
@@ -58,13 +60,14 @@ class Config(ctypes.Structure):
         ("combine_ctas_per_sm", ctypes.c_int32),
         ("combine_stage_bytes", ctypes.c_int32),
         ("combine_unroll", ctypes.c_int32),
+        ("recv_order", ctypes.c_int32),
     ]
 
 
 class SplitsPtrs(ctypes.Structure):
     _fields_ = [(name, ctypes.c_void_p) for name in (
         "send_counts", "send_offsets", "recv_counts", "recv_offsets", "recv_expert_counts",
-        "recv_total", "window_base")]
+        "recv_total", "window_base", "recv_expert_offsets")]
 
 
 class A2avError(RuntimeError):
@@ -144,18 +147,19 @@ def _check(L, rc: int, what: str):
 
 def make_config(R, E, T, H, k, window_mode="packed", window_rows=0, device=0, flags=0,
                 pack_ctas_per_sm=0, pack_stage_bytes=0, pack_store_lag=0, combine_ctas_per_sm=0,
-                combine_stage_bytes=0, combine_unroll=0) -> Config:
+                combine_stage_bytes=0, combine_unroll=0, recv_order="source") -> Config:
     mode = {"packed": WINDOW_PACKED, "fixed": WINDOW_FIXED, "padded": WINDOW_PADDED}.get(window_mode, window_mode)
+    order = {"source": ORDER_SOURCE, "expert": ORDER_EXPERT}.get(recv_order, recv_order)
     return Config(int(R), int(E), int(T), int(H), int(k), int(mode), int(window_rows), int(device),
                   int(flags), int(pack_ctas_per_sm), int(pack_stage_bytes), int(pack_store_lag),
-                  int(combine_ctas_per_sm), int(combine_stage_bytes), int(combine_unroll))
+                  int(combine_ctas_per_sm), int(combine_stage_bytes), int(combine_unroll), int(order))
 
 
 class Splits:
     """Device-resident split counts/offsets of one dispatch (int32 tensors)."""
 
     NAMES = ("send_counts", "send_offsets", "recv_counts", "recv_offsets", "recv_expert_counts",
-             "recv_total", "window_base")
+             "recv_total", "window_base", "recv_expert_offsets")
 
     def __init__(self, R: int, E: int, device):
         import torch
@@ -163,7 +167,7 @@ class Splits:
         epr = E // R
         shapes = {"send_counts": (R, E), "send_offsets": (R, E), "recv_counts": (R, R),
                   "recv_offsets": (R, R), "recv_expert_counts": (R, R, epr), "recv_total": (R,),
-                  "window_base": (R,)}
+                  "window_base": (R,), "recv_expert_offsets": (R, R, epr)}
         for n in self.NAMES:
             setattr(self, n, torch.zeros(shapes[n], dtype=torch.int32, device=device))
         self._ptrs = SplitsPtrs(*[getattr(self, n).data_ptr() for n in self.NAMES])
@@ -189,7 +193,7 @@ class Plan:
 
     def __init__(self, R, E, T, H, k, window_mode="packed", window_rows=0, device=None, flags=0,
                  pack_ctas_per_sm=0, pack_stage_bytes=0, pack_store_lag=0, combine_ctas_per_sm=0,
-                 combine_stage_bytes=0, combine_unroll=0):
+                 combine_stage_bytes=0, combine_unroll=0, recv_order="source"):
         import torch
 
         self.lib = load_library()
@@ -200,9 +204,10 @@ class Plan:
         self.R, self.E, self.T, self.H, self.k = int(R), int(E), int(T), int(H), int(k)
         self.window_mode = window_mode
         self.window_rows = int(window_rows)
+        self.recv_order = recv_order
         self.cfg = make_config(R, E, T, H, k, window_mode, window_rows, dev.index, flags,
                                pack_ctas_per_sm, pack_stage_bytes, pack_store_lag, combine_ctas_per_sm,
-                               combine_stage_bytes, combine_unroll)
+                               combine_stage_bytes, combine_unroll, recv_order)
         handle = ctypes.c_void_p()
         _check(self.lib, self.lib.a2av_plan_create(ctypes.byref(self.cfg), ctypes.byref(handle)), "a2av_plan_create")
         self.handle = handle
@@ -362,7 +367,7 @@ class Plan:
 
 
 def dispatch_static(x, topk_idx, splits: Splits, recv, slot_map, dev_status, R, E, T, H, k,
-                    window_mode="packed", window_rows=0, flags=0, stream=None):
+                    window_mode="packed", window_rows=0, flags=0, stream=None, recv_order="source"):
     """Dispatch without a plan and without any allocation (a2av_dispatch_static).
 
     For callers that cannot allocate device memory at the point of dispatch:
@@ -376,7 +381,7 @@ def dispatch_static(x, topk_idx, splits: Splits, recv, slot_map, dev_status, R, 
 
     L = load_library()
     dev = x.device
-    cfg = make_config(R, E, T, H, k, window_mode, window_rows, dev.index, flags)
+    cfg = make_config(R, E, T, H, k, window_mode, window_rows, dev.index, flags, recv_order=recv_order)
     for t, dt, name in ((x, torch.bfloat16, "x"), (topk_idx, torch.int32, "topk_idx"), (recv, torch.bfloat16, "recv"),
                         (slot_map, torch.int32, "slot_map"), (dev_status, torch.int32, "dev_status")):
         if t.device != dev or t.dtype != dt or not t.is_contiguous():

@@ -36,15 +36,19 @@ struct DeviceGuard {
 
 bool aligned(const void *p, size_t a) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-bool splits_ok(const a2av_splits_t *sp) {
-    return sp && aligned(sp->send_counts, 4) && aligned(sp->send_offsets, 4) && aligned(sp->recv_counts, 4) &&
+// recv_expert_offsets: required in the expert-grouped order, optional otherwise.
+bool splits_ok(const a2av_plan_s *p, const a2av_splits_t *sp) {
+    if (!sp) return false;
+    const bool reo_ok = sp->recv_expert_offsets ? aligned(sp->recv_expert_offsets, 4)
+                                                : p->cfg.recv_order != A2AV_ORDER_EXPERT;
+    return reo_ok && aligned(sp->send_counts, 4) && aligned(sp->send_offsets, 4) && aligned(sp->recv_counts, 4) &&
            aligned(sp->recv_offsets, 4) && aligned(sp->recv_expert_counts, 4) && aligned(sp->recv_total, 4) &&
            aligned(sp->window_base, 4);
 }
 
 a2av::Splits to_internal(const a2av_splits_t *sp) {
-    return a2av::Splits{sp->send_counts, sp->send_offsets, sp->recv_counts, sp->recv_offsets,
-                        sp->recv_expert_counts, sp->recv_total, sp->window_base};
+    return a2av::Splits{sp->send_counts,        sp->send_offsets, sp->recv_counts,  sp->recv_offsets,
+                        sp->recv_expert_counts, sp->recv_total,   sp->window_base, sp->recv_expert_offsets};
 }
 
 bool overlap(const void *a, size_t na, const void *b, size_t nb) {
@@ -92,6 +96,8 @@ a2av_status_t a2av_config_check(const a2av_config_t *c) {
     if (c->pack_ctas_per_sm < 0 || c->pack_ctas_per_sm > 4) return A2AV_ERR_INVALID_ARG;
     if (c->pack_stage_bytes < 0 || c->pack_stage_bytes % 16 != 0 || c->pack_stage_bytes > 65536)
         return A2AV_ERR_INVALID_ARG;
+    if (c->recv_order != A2AV_ORDER_SOURCE && c->recv_order != A2AV_ORDER_EXPERT) return A2AV_ERR_INVALID_ARG;
+    if (c->recv_order == A2AV_ORDER_EXPERT && c->window_mode == A2AV_WINDOW_PADDED) return A2AV_ERR_INVALID_ARG;
     return A2AV_OK;
 }
 
@@ -128,6 +134,7 @@ a2av_status_t a2av_plan_create(const a2av_config_t *cfg, a2av_plan_t *out_plan) 
     while ((1 << g.key_bits) <= g.E) ++g.key_bits;
     g.tiles = (int32_t)(((long long)g.T * g.k + a2av::kHistTile - 1) / a2av::kHistTile);
     g.window_mode = cfg->window_mode;
+    g.recv_order = cfg->recv_order;
     g.window_rows = cfg->window_mode == A2AV_WINDOW_FIXED ? cfg->window_rows : 0;
     p->pack_tma = (cfg->flags & A2AV_FLAG_PACK_LSU) ? 0 : 1;
 
@@ -179,7 +186,7 @@ a2av_status_t a2av_plan_destroy(a2av_plan_t p) {
 
 a2av_status_t a2av_splits(a2av_plan_t p, const int32_t *topk_idx, const a2av_splits_t *splits, int32_t *slot_map,
                           void *stream) {
-    if (!p || !aligned(topk_idx, 4) || !aligned(slot_map, 4) || !splits_ok(splits)) return A2AV_ERR_INVALID_ARG;
+    if (!p || !aligned(topk_idx, 4) || !aligned(slot_map, 4) || !splits_ok(p, splits)) return A2AV_ERR_INVALID_ARG;
     DeviceGuard guard(p->cfg.device);
     if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
     a2av::HistArgs a;
@@ -222,7 +229,7 @@ a2av_status_t a2av_pack_padded(a2av_plan_t p, const void *x, const int32_t *topk
 static a2av_status_t pack_into(a2av_plan_t p, const void *x, const int32_t *topk_idx, const a2av_splits_t *splits,
                                void *recv, int32_t *slot_map, void *stream, bool padded) {
     if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(topk_idx, 4) || !aligned(slot_map, 4) ||
-        !splits_ok(splits))
+        !splits_ok(p, splits))
         return A2AV_ERR_INVALID_ARG;
     const int64_t rows = a2av_recv_arena_rows(&p->cfg);
     if (overlap(x, tokens(p) * row_bytes(p), recv, (size_t)rows * row_bytes(p))) return A2AV_ERR_INVALID_ARG;
@@ -239,6 +246,7 @@ static a2av_status_t pack_into(a2av_plan_t p, const void *x, const int32_t *topk
     a.send_offsets = splits->send_offsets;
     a.recv_offsets = splits->recv_offsets;
     a.window_base = splits->window_base;
+    a.recv_expert_offsets = splits->recv_expert_offsets;
     a.recv = static_cast<uint16_t *>(recv);
     a.status = p->status;
     a.padded_tk = padded ? (int64_t)p->g.T * p->g.k : 0;
@@ -287,7 +295,7 @@ a2av_status_t a2av_dispatch(a2av_plan_t p, const void *x, const int32_t *topk_id
         return A2AV_ERR_INVALID_ARG;
     }
     if (!p || !aligned(x, 16) || !aligned(recv, 16) || !aligned(topk_idx, 4) || !aligned(slot_map, 4) ||
-        !splits_ok(splits))
+        !splits_ok(p, splits))
         return A2AV_ERR_INVALID_ARG;
     const int64_t rows = a2av_recv_arena_rows(&p->cfg);
     if (overlap(x, tokens(p) * row_bytes(p), recv, (size_t)rows * row_bytes(p))) return A2AV_ERR_INVALID_ARG;

@@ -26,6 +26,7 @@ constexpr uint32_t kDevWaitTimeout = 1u << 31;
 struct Splits {
     int32_t *send_counts, *send_offsets, *recv_counts, *recv_offsets, *recv_expert_counts, *recv_total,
         *window_base;
+    int32_t *recv_expert_offsets;  // may be null in source order (then not written)
 };
 
 // Geometry every kernel needs.
@@ -33,7 +34,8 @@ struct Geometry {
     int32_t R, E, T, H, k, epr;
     int32_t key_bits;     // bits of an expert key in [0, E] (E marks a dropped id)
     int32_t tiles;        // histogram tiles per rank
-    int32_t window_mode;  // 0 packed, 1 fixed
+    int32_t window_mode;  // A2AV_WINDOW_*
+    int32_t recv_order;   // A2AV_ORDER_*
     int64_t window_rows;
 };
 
@@ -59,6 +61,7 @@ struct PackArgs {
     const int32_t *send_offsets;  // splits arrays written by the splits kernel
     const int32_t *recv_offsets;
     const int32_t *window_base;
+    const int32_t *recv_expert_offsets;  // [R][R][Epr]; read in the expert-grouped order
     uint16_t *recv;
     uint32_t *status;
     // TMA variant: chunking of a row into stage-sized pieces

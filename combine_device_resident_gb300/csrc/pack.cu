@@ -8,6 +8,8 @@
 // Row of assignment (s, t, j) with expert e on rank d = e / (E/R):
 //   rel = recv_offsets[d][s] + send_offsets[s][e] - send_offsets[s][d*E/R]
 //         + tile_base[s][tile(t*k+j)][e] + rank_in_tile
+//   (expert-grouped receive order: rel = recv_expert_offsets[d][s][e - d*E/R]
+//    + tile_base[s][tile(t*k+j)][e] + rank_in_tile)
 //   row = window_base[d] + rel        (dropped if rel >= window_rows, fixed mode)
 // (all produced on the device by the splits kernel; with the cluster splits
 // kernel slot_map already holds the row).
@@ -67,10 +69,15 @@ __device__ __forceinline__ int32_t final_row(const PackArgs &a, long long tok, i
     const int t = (int)(tok - (long long)s * g.T);
     const int tl = (t * g.k + j) / kHistTile;
     const int d = e / g.epr;
-    const long long rel = (long long)__ldg(a.recv_offsets + (size_t)d * g.R + s) +
-                          __ldg(a.send_offsets + (size_t)s * g.E + e) -
-                          __ldg(a.send_offsets + (size_t)s * g.E + (size_t)d * g.epr) +
-                          __ldg(a.tile_base + ((size_t)s * g.tiles + tl) * g.E + e) + r;
+    // rank of the assignment among rank s's rows for expert e, plus where
+    // that (s, e) block starts in window d
+    const long long in_block = (long long)__ldg(a.tile_base + ((size_t)s * g.tiles + tl) * g.E + e) + r;
+    const long long rel =
+        in_block + (g.recv_order == A2AV_ORDER_EXPERT
+                        ? (long long)__ldg(a.recv_expert_offsets + ((size_t)d * g.R + s) * g.epr + (e - d * g.epr))
+                        : (long long)__ldg(a.recv_offsets + (size_t)d * g.R + s) +
+                              __ldg(a.send_offsets + (size_t)s * g.E + e) -
+                              __ldg(a.send_offsets + (size_t)s * g.E + (size_t)d * g.epr));
     const long long cap = g.window_mode == A2AV_WINDOW_FIXED ? g.window_rows : (long long)g.R * g.T * g.k;
     // (packed: a window holds at most R*T*k rows; padded: a window is R*T*k rows)
     if (rel < 0 || rel >= cap) {

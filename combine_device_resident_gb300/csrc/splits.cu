@@ -258,10 +258,60 @@ __global__ void __launch_bounds__(kHistThreads) hist_scan_kernel(const HistArgs 
         if (__any_sync(kFull, ovf) && lane == 0) atomicOr(a.status, (uint32_t)A2AV_DEV_WINDOW_OVERFLOW);
         if (lane == 0) a.counters[R] = 0;  // re-arm
     }
+
+    // ---- first row of every (source, local expert) block ----------------------
+    // One warp per destination d: d's received counts rec[d][s][le] (E
+    // contiguous ints) are staged in the warp's scratch and scanned there.
+    int32_t *reo = a.sp.recv_expert_offsets;
+    if (!reo) return;
+    int *buf = smem + R * R + R + warp * E;  // [E] per warp
+    const bool padded = g.window_mode == A2AV_WINDOW_PADDED;
+    for (int d = warp; d < R; d += kHistWarps) {
+        const int32_t *rec = a.sp.recv_expert_counts + (size_t)d * E;  // [R][epr]
+        for (int i = lane; i < E; i += 32) buf[i] = __ldcg(rec + i);
+        __syncwarp();
+        int32_t *out = reo + (size_t)d * E;
+        int carry = 0;
+        if (g.recv_order == A2AV_ORDER_EXPERT) {
+            // lane = local expert: its block starts after the lower experts'
+            // rows (all sources); inside it the sources follow in order
+            for (int l0 = 0; l0 < epr; l0 += 32) {
+                const int le = l0 + lane;
+                int tot = 0;
+                if (le < epr)
+                    for (int src = 0; src < R; ++src) tot += buf[src * epr + le];
+                const int incl = warp_inclusive_scan(tot, lane);
+                int run = carry + incl - tot;
+                if (le < epr)
+                    for (int src = 0; src < R; ++src) {
+                        out[src * epr + le] = run;
+                        run += buf[src * epr + le];
+                    }
+                carry += __shfl_sync(kFull, incl, 31);
+            }
+        } else {
+            // lane = source: its segment start, then its rows for the lower
+            // local experts
+            for (int s0 = 0; s0 < R; s0 += 32) {
+                const int src = s0 + lane;
+                const int v = src < R ? rc[d * R + src] : 0;
+                const int incl = warp_inclusive_scan(v, lane);
+                if (src < R) {
+                    int run = padded ? (int)((long long)src * g.T * g.k) : carry + incl - v;
+                    for (int le = 0; le < epr; ++le) {
+                        out[src * epr + le] = run;
+                        run += buf[src * epr + le];
+                    }
+                }
+                carry += __shfl_sync(kFull, incl, 31);
+            }
+        }
+        __syncwarp();  // the scratch is refilled for the next destination
+    }
 }
 
 size_t hist_smem_bytes(const Geometry &g) {
-    const size_t a = (size_t)kHistWarps * (g.E + 1), b = (size_t)g.R * g.R + g.R;
+    const size_t a = (size_t)kHistWarps * (g.E + 1), b = (size_t)g.R * g.R + g.R + (size_t)kHistWarps * g.E;
     return sizeof(int) * (a > b ? a : b);
 }
 
@@ -306,7 +356,11 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
     int *rc = so + (E + 1);              // [R][R] recv counts, [d][src]
     int *ro = rc + R * R;                // [R] receive offset of this rank in window d
     int *wb = ro + R;                    // [R] window totals, then bases
+    int *xb = wb + R;                    // [E] expert order: rows of expert e on ranks below s
+    int *xt = xb + E;                    // [E] expert order: rows of e on all ranks, then e's block start
+    const bool by_expert = g.recv_order == A2AV_ORDER_EXPERT;
     for (int i = tid; i < kClusterWarps * ES; i += kClusterThreads) cnt[i] = 0;
+    for (int i = tid; i < 2 * E; i += kClusterThreads) xb[i] = 0;  // xb and xt
     __syncthreads();
 
     int key[kClusterRounds], rank[kClusterRounds];
@@ -359,6 +413,15 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
         const int d = p / R, src = p - d * R;
         rc[p] = ld_dsmem(peer_smem(so + (d + 1) * epr, src)) - ld_dsmem(peer_smem(so + d * epr, src));
     }
+    if (by_expert)  // one (source, expert) pair per thread, summed with shared-memory atomics
+        for (int p = tid; p < R * E; p += kClusterThreads) {
+            const int src = p / E, e = p - src * E;
+            const int c = ld_dsmem(peer_smem(so + e + 1, src)) - ld_dsmem(peer_smem(so + e, src));
+            if (c) {
+                atomicAdd(&xt[e], c);
+                if (src < s) atomicAdd(&xb[e], c);
+            }
+        }
     // no CTA may leave (or reuse) its shared memory until every peer has read it
     cluster_barrier();
 
@@ -394,7 +457,25 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
             if (s == 0) a.sp.window_base[lane] = (int)base;
         }
     }
+    if (by_expert)  // block start of each expert: scan of the totals over its window's experts
+        for (int d = warp; d < R; d += kClusterWarps) {
+            int carry = 0;
+            for (int c0 = 0; c0 < epr; c0 += 32) {
+                const int le = c0 + lane;
+                const int v = le < epr ? xt[d * epr + le] : 0;
+                const int incl = warp_inclusive_scan(v, lane);
+                if (le < epr) xt[d * epr + le] = carry + incl - v;
+                carry += __shfl_sync(kFull, incl, 31);
+            }
+        }
     __syncthreads();
+    // first row of each of this rank's (destination, local expert) blocks
+    if (a.sp.recv_expert_offsets)
+        for (int e = tid; e < E; e += kClusterThreads) {
+            const int d = e / epr, le = e - d * epr;
+            a.sp.recv_expert_offsets[((size_t)d * R + s) * epr + le] =
+                by_expert ? xt[e] + xb[e] : ro[d] + so[e] - so[d * epr];
+        }
 
     bool ovf = false;
     int32_t *sm = a.slot_map + (size_t)s * A;
@@ -407,7 +488,8 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
             const int e = key[r];
             if (e >= 0) {
                 const int d = e / epr;
-                const long long rel = (long long)ro[d] + so[e] - so[d * epr] + mine[e] + rank[r];
+                const long long rel = (by_expert ? (long long)xt[e] + xb[e] : (long long)ro[d] + so[e] - so[d * epr]) +
+                                      mine[e] + rank[r];
                 if (g.window_mode == A2AV_WINDOW_FIXED && rel >= g.window_rows)
                     ovf = true;
                 else
@@ -420,7 +502,8 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
 }
 
 size_t cluster_smem_bytes(const Geometry &g) {
-    return sizeof(int) * ((size_t)kClusterWarps * (g.E + 1) + (g.E + 1) + (size_t)g.R * g.R + 2 * (size_t)g.R);
+    return sizeof(int) *
+           ((size_t)kClusterWarps * (g.E + 1) + (g.E + 1) + (size_t)g.R * g.R + 2 * (size_t)g.R + 2 * (size_t)g.E);
 }
 
 bool cluster_eligible(const Geometry &g) {

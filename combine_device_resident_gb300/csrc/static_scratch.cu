@@ -62,7 +62,9 @@ extern "C" a2av_status_t a2av_dispatch_static(const a2av_config_t *cfg, const vo
         !aligned(dev_status, 4) || !splits || !aligned(splits->send_counts, 4) || !aligned(splits->send_offsets, 4) ||
         !aligned(splits->recv_counts, 4) || !aligned(splits->recv_offsets, 4) ||
         !aligned(splits->recv_expert_counts, 4) || !aligned(splits->recv_total, 4) ||
-        !aligned(splits->window_base, 4)) {
+        !aligned(splits->window_base, 4) ||
+        (splits->recv_expert_offsets ? !aligned(splits->recv_expert_offsets, 4)
+                                     : cfg->recv_order == A2AV_ORDER_EXPERT)) {
         a2av::set_last_error("a2av_dispatch_static: null or misaligned pointer");
         return A2AV_ERR_INVALID_ARG;
     }
@@ -80,6 +82,7 @@ extern "C" a2av_status_t a2av_dispatch_static(const a2av_config_t *cfg, const vo
     while ((1 << g.key_bits) <= g.E) ++g.key_bits;
     g.tiles = (int32_t)(((long long)g.T * g.k + a2av::kHistTile - 1) / a2av::kHistTile);
     g.window_mode = cfg->window_mode;
+    g.recv_order = cfg->recv_order;
     g.window_rows = cfg->window_mode == A2AV_WINDOW_FIXED ? cfg->window_rows : 0;
     p.pack_tma = (cfg->flags & A2AV_FLAG_PACK_LSU) ? 0 : 1;
 
@@ -134,7 +137,8 @@ extern "C" a2av_status_t a2av_dispatch_static(const a2av_config_t *cfg, const vo
         h.counters = p.counters;
         h.status = dev_status;
         h.sp = a2av::Splits{splits->send_counts, splits->send_offsets, splits->recv_counts, splits->recv_offsets,
-                            splits->recv_expert_counts, splits->recv_total, splits->window_base};
+                            splits->recv_expert_counts, splits->recv_total, splits->window_base,
+                            splits->recv_expert_offsets};
         e = a2av::launch_hist(p, h, s);
     }
     if (e == cudaSuccess) {
@@ -147,6 +151,7 @@ extern "C" a2av_status_t a2av_dispatch_static(const a2av_config_t *cfg, const vo
         a.send_offsets = splits->send_offsets;
         a.recv_offsets = splits->recv_offsets;
         a.window_base = splits->window_base;
+        a.recv_expert_offsets = splits->recv_expert_offsets;
         a.recv = static_cast<uint16_t *>(recv);
         a.status = dev_status;
         e = a2av::launch_pack(p, a, s);

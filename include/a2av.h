@@ -21,7 +21,11 @@
  *   - expert e lives on rank e / (E/R) (contiguous blocks);
  *   - "sorted by expert" is stable: expert, then token t, then slot j;
  *   - window d holds the segments of sources 0..R-1 back to back, in source
- *     order, with no gaps;
+ *     order, with no gaps (the AllToAllv convention); or, in the
+ *     expert-grouped receive order, the rows of local expert 0 from every
+ *     source, then those of local expert 1, ... -- the layout one GEMM per
+ *     local expert reads after the exchange (Inference section, Figure 13:
+ *     the received tokens go on to their experts), the counts unchanged;
  *   - combine: out = bf16_rne(sum_j w_j * y[slot(t,j)]) accumulated in fp32
  *     from 0 in slot order, product and sum each rounded on its own.
  *
@@ -59,6 +63,12 @@
  *   splits.recv_counts        [R][R]       [d][s] rows window d receives from s
  *   splits.recv_offsets       [R][R]       [d][s] exclusive scan over s
  *   splits.recv_expert_counts [R][R][Epr]  [d][s][le] = send_counts[s][d*Epr+le]
+ *   splits.recv_expert_offsets [R][R][Epr] [d][s][le] window-relative first row of the
+ *                                          rows s sends to local expert le of rank d:
+ *                                          source order: recv_offsets[d][s] + s's rows for
+ *                                          the lower local experts; expert order: all rows
+ *                                          of the lower local experts + those of le from
+ *                                          sources below s
  *   splits.recv_total         [R]          rows window d receives
  *   splits.window_base        [R]          arena row where window d starts
  */
@@ -98,6 +108,13 @@ enum {
                                padded baseline the dynamic collective is compared with */
 };
 
+/* Order of the rows inside each window (a2av_config_t.recv_order). */
+enum {
+    A2AV_ORDER_SOURCE = 0, /* AllToAllv convention: source segments in source order, each sorted by expert */
+    A2AV_ORDER_EXPERT = 1, /* expert-grouped: local expert blocks in expert order, each holding its sources'
+                              rows in source order; not with A2AV_WINDOW_PADDED */
+};
+
 /* Variant flags (a2av_config_t.flags). */
 enum {
     A2AV_FLAG_PACK_LSU = 1u << 0,     /* pack+exchange with 16-byte vector loads/stores instead of TMA bulk copies */
@@ -124,6 +141,7 @@ typedef struct {
     int32_t combine_stage_bytes;  /* TMA combine: bytes of the k row chunks per stage, multiple of 16 (0 = 16 KiB) */
     int32_t combine_unroll;       /* vector combine: 16-byte loads per lane and slot per step, 1..8
                                      (0 = 2 for k <= 2, else 1) */
+    int32_t recv_order;           /* A2AV_ORDER_SOURCE (0) or A2AV_ORDER_EXPERT */
 } a2av_config_t;
 
 /* Caller-owned device arrays the split counts and offsets are written to
@@ -137,6 +155,7 @@ typedef struct {
     int32_t *recv_expert_counts;
     int32_t *recv_total;
     int32_t *window_base;
+    int32_t *recv_expert_offsets; /* [R][R][Epr]; required with A2AV_ORDER_EXPERT, else may be NULL (not written) */
 } a2av_splits_t;
 
 /* Host-only check of a configuration against the limits above; touches no GPU. */

@@ -15,7 +15,7 @@ import workloads as W
 from tests.bf16util import ulp_diff
 
 SPLIT_KEYS = ("send_counts", "send_offsets", "recv_counts", "recv_offsets", "recv_expert_counts",
-              "recv_total", "window_base")
+              "recv_total", "window_base", "recv_expert_offsets")
 COMBINE_ULP_TOL = 1
 
 
@@ -38,7 +38,8 @@ def gpu_run(w: W.Workload, x, idx: np.ndarray, gate: np.ndarray, flags=0, pack_c
         plan = Plan(w.R, w.E, w.T, w.H, w.k, w.window_mode, w.window_rows, device=dev, flags=flags,
                     pack_ctas_per_sm=pack_ctas_per_sm, pack_stage_bytes=pack_stage_bytes,
                     pack_store_lag=pack_store_lag, combine_ctas_per_sm=combine_ctas_per_sm,
-                    combine_stage_bytes=combine_stage_bytes, combine_unroll=combine_unroll)
+                    combine_stage_bytes=combine_stage_bytes, combine_unroll=combine_unroll,
+                    recv_order=w.recv_order)
     nt_t = None
     if num_tokens is not None:
         nt_t = torch.from_numpy(np.ascontiguousarray(num_tokens, np.int32)).to(dev)
@@ -102,7 +103,7 @@ def full_parity(w: W.Workload, seed=0, idx=None, gate=None, x=None, **kw):
     xh = bits(x)
     nt = kw.get("num_tokens")
     ref = oracle.run_all(w.R, w.E, xh, idx, gate, w.window_mode, w.window_rows, kw.get("expert") or w.expert,
-                         num_tokens=nt)
+                         num_tokens=nt, recv_order=w.recv_order)
     check_splits(g["splits"], ref["splits"])
     np.testing.assert_array_equal(g["slot_map"], ref["slot_map"], err_msg="slot_map")
     assert g["status"] == ref["status"], (g["status"], ref["status"])

@@ -56,17 +56,34 @@ def _cfg(**kw):
 
 def test_config_check_host_only(lib):
     ok = [_cfg(), _cfg(R=1, E=1, T=1, H=8, k=1), _cfg(R=64, E=2048, T=3, H=8, k=32),
-          _cfg(window_mode="fixed", window_rows=100), _cfg(window_mode="padded")]
+          _cfg(window_mode="fixed", window_rows=100), _cfg(window_mode="padded"), _cfg(recv_order="expert"),
+          _cfg(window_mode="fixed", window_rows=100, recv_order="expert")]
     bad = [_cfg(R=0), _cfg(R=65, E=130), _cfg(E=12, R=8), _cfg(E=4096, R=8), _cfg(H=12), _cfg(H=0), _cfg(k=0),
            _cfg(k=33), _cfg(T=0), _cfg(window_mode=3), _cfg(window_mode="fixed", window_rows=-1),
            _cfg(R=64, E=64, T=65536, k=8, window_mode="padded"),
            _cfg(R=64, E=64, T=1 << 20, k=32), _cfg(flags=1 << 7), _cfg(flags=1 << 3), _cfg(pack_stage_bytes=24),
-           _cfg(pack_ctas_per_sm=9)]
+           _cfg(pack_ctas_per_sm=9), _cfg(recv_order=2), _cfg(recv_order=-1),
+           _cfg(window_mode="padded", recv_order="expert")]
     for c in ok:
         assert lib.a2av_config_check(ctypes.byref(c)) == 0
     for c in bad:
         assert lib.a2av_config_check(ctypes.byref(c)) == 1
     assert lib.a2av_config_check(None) == 1
+
+
+def test_struct_layouts_match_the_header():
+    # the binding's ctypes mirrors of a2av_config_t / a2av_splits_t
+    from combine_device_resident_gb300.binding import Config, SplitsPtrs
+
+    assert Config.recv_order.offset == Config.combine_unroll.offset + 4
+    assert ctypes.sizeof(Config) == (Config.recv_order.offset + 4 + 7) // 8 * 8  # int64 member: 8-byte alignment
+    assert SplitsPtrs.recv_expert_offsets.offset == 7 * ctypes.sizeof(ctypes.c_void_p)
+    hdr = open(os.path.join(ROOT, "include", "a2av.h")).read()
+    cfg_body = hdr[hdr.index("typedef struct {\n    int32_t num_ranks;"):hdr.index("} a2av_config_t;")]
+    fields = re.findall(r"^\s*(?:u?int\d+_t)\s+(\w+);", cfg_body, re.M)
+    assert fields == [f[0] for f in Config._fields_]
+    sp_body = hdr[hdr.index("typedef struct {\n    int32_t *send_counts;"):hdr.index("} a2av_splits_t;")]
+    assert re.findall(r"int32_t \*(\w+);", sp_body) == [f[0] for f in SplitsPtrs._fields_]
 
 
 def test_arena_rows(lib):

@@ -487,3 +487,77 @@ def test_router_leaves_inactive_tokens_alone():
         np.testing.assert_array_equal(got[s_, :nt[s_]], ridx[s_, :nt[s_]])
         assert (got[s_, nt[s_]:] == -9).all()
         assert (gate.cpu().numpy()[s_, nt[s_]:] == -1.0).all()
+
+
+# ---------------------------------------------------------------------------
+# expert-grouped receive order
+# ---------------------------------------------------------------------------
+def _by_expert(w, **kw):
+    import dataclasses
+
+    return dataclasses.replace(w, recv_order="expert", name=w.name + "-by-expert", **kw)
+
+
+@pytest.mark.parametrize("wid,T,H", SCALED, ids=[f"w{s[0]}" for s in SCALED])
+def test_expert_order_parity(wid, T, H):
+    w = W.WORKLOADS[wid] if T is None else W.WORKLOADS[wid].scaled(T=T, H=H)
+    P.full_parity(_by_expert(w))
+
+
+@pytest.mark.parametrize("flags", [1, 2, 3], ids=["lsu", "tiled", "tiled-lsu"])
+def test_expert_order_variants(flags):
+    for wid, T, H in [(1, None, None), (2, 1100, 264), (4, 900, 72), (5, 200, 64)]:
+        w = W.WORKLOADS[wid] if T is None else W.WORKLOADS[wid].scaled(T=T, H=H)
+        P.full_parity(_by_expert(w), flags=flags)
+
+
+@pytest.mark.parametrize("wid,T,H", [(2, 1100, 264), (4, 700, 72), (5, 300, 64)])
+def test_expert_order_same_output_and_contiguous_experts(wid, T, H):
+    w = W.WORKLOADS[wid].scaled(T=T, H=H)
+    x = W.make_x(w, 0, device=P.device())
+    rg = W.make_routing_gate(w, 0)
+    src = P.full_parity(w, x=x, idx=rg["topk_idx"], gate=rg["gate_w"])
+    ex = P.full_parity(_by_expert(w), x=x, idx=rg["topk_idx"], gate=rg["gate_w"])
+    np.testing.assert_array_equal(ex["out"], src["out"])
+    for key in P.SPLIT_KEYS[:-1]:  # the counts are the same; only the places differ
+        np.testing.assert_array_equal(ex["splits"][key], src["splits"][key], err_msg=key)
+    # each local expert's rows are one contiguous block, starting where
+    # recv_expert_offsets says
+    sp, idx, epr = ex["splits"], rg["topk_idx"], w.E // w.R
+    rel = ex["slot_map"] - sp["window_base"][idx // epr]
+    reo, rec = sp["recv_expert_offsets"], sp["recv_expert_counts"]
+    for d in range(w.R):
+        for le in range(epr):
+            rows = np.sort(rel[idx == d * epr + le])
+            assert rows.size == rec[d, :, le].sum()
+            np.testing.assert_array_equal(rows, reo[d, 0, le] + np.arange(rows.size))
+
+
+def test_expert_order_fixed_windows_overflow_and_active_counts():
+    import dataclasses
+
+    w3 = W.WORKLOADS[3].scaled(T=700, H=72)
+    # windows too small for the hot ranks: rows past the window are dropped
+    # by their expert-order position, with the overflow bit
+    g = P.full_parity(_by_expert(w3, window_rows=300))
+    assert g["status"] & 2
+    # per-rank active counts in expert order
+    w5 = W.WORKLOADS[5].scaled(T=500, H=64)
+    nt = np.array([(s * 37) % 501 for s in range(w5.R)], np.int32)
+    P.full_parity(_by_expert(w5), num_tokens=nt)
+    P.full_parity(_by_expert(dataclasses.replace(w3, window_rows=w3.R * w3.T)), num_tokens=nt[:w3.R], flags=2)
+
+
+def test_expert_order_plan_requires_the_offsets_array():
+    import torch
+
+    import combine_device_resident_gb300 as A
+
+    w = _by_expert(W.WORKLOADS[1])
+    plan = A.Plan(w.R, w.E, w.T, w.H, w.k, device=P.device(), recv_order="expert")
+    sp = plan.new_splits()
+    sp.ptrs.recv_expert_offsets = None
+    recv, slot_map, _ = plan.new_buffers()
+    idx_t = torch.zeros((w.R, w.T, w.k), dtype=torch.int32, device=P.device())
+    with pytest.raises(A.A2avError):
+        plan.splits(idx_t, sp, slot_map)

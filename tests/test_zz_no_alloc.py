@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 def _plan_dispatch(w, x, idx_t):
     import combine_device_resident_gb300 as A
 
-    plan = A.Plan(w.R, w.E, w.T, w.H, w.k, w.window_mode, w.window_rows, device=x.device)
+    plan = A.Plan(w.R, w.E, w.T, w.H, w.k, w.window_mode, w.window_rows, device=x.device, recv_order=w.recv_order)
     recv, slot_map, _ = plan.new_buffers()
     recv.zero_()
     sp = plan.new_splits()
@@ -41,16 +41,20 @@ def _static_dispatch(w, x, idx_t):
     recv = torch.zeros((arena, w.H), dtype=torch.bfloat16, device=dev)
     slot_map = torch.full((w.R, w.T, w.k), -5, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    dispatch_static(x, idx_t, sp, recv, slot_map, status, w.R, w.E, w.T, w.H, w.k, w.window_mode, w.window_rows)
+    dispatch_static(x, idx_t, sp, recv, slot_map, status, w.R, w.E, w.T, w.H, w.k, w.window_mode, w.window_rows,
+                    recv_order=w.recv_order)
     return sp, recv, slot_map, status
 
 
-@pytest.mark.parametrize("wid,T,H", [(5, 700, 264), (3, 900, 136), (4, 3000, 72)])
-def test_static_dispatch_matches_plan_dispatch_on_two_calls(wid, T, H):
+@pytest.mark.parametrize("wid,T,H,order", [(5, 700, 264, "source"), (3, 900, 136, "source"), (4, 3000, 72, "source"),
+                                           (5, 500, 72, "expert"), (2, 900, 64, "expert")])
+def test_static_dispatch_matches_plan_dispatch_on_two_calls(wid, T, H, order):
+    import dataclasses
+
     import torch
 
     dev = torch.device("cuda", 0)
-    w = W.WORKLOADS[wid].scaled(T=T, H=H)
+    w = dataclasses.replace(W.WORKLOADS[wid].scaled(T=T, H=H), recv_order=order)
     x = W.make_x(w, 0, device=dev)
     for seed in (11, 12):
         idx_t = torch.from_numpy(W.make_routing_gate(w, seed)["topk_idx"]).to(dev)

@@ -70,6 +70,7 @@ class Workload:
     expert: str = "identity"    # "identity" or "scale" (y = x * (1 + e/E))
     window_mode: str = "packed"  # "packed" arena or "fixed" per-rank windows
     window_rows: int = 0         # fixed mode: rows per destination window
+    recv_order: str = "source"   # "source" (AllToAllv convention) or "expert" (grouped by local expert)
 
     @property
     def assignments(self) -> int:
