@@ -156,28 +156,33 @@ def make_config(R, E, T, H, k, window_mode="packed", window_rows=0, device=0, fl
 
 
 class Splits:
-    """Device-resident split counts/offsets of one dispatch (int32 tensors)."""
+    """Device-resident split counts/offsets of one dispatch (int32 tensors).
+
+    ``recv_expert_offsets`` is allocated and filled only when
+    ``expert_offsets`` is true (the expert-grouped receive order needs it;
+    in source order it is an optional extra output of the splits kernel)."""
 
     NAMES = ("send_counts", "send_offsets", "recv_counts", "recv_offsets", "recv_expert_counts",
              "recv_total", "window_base", "recv_expert_offsets")
 
-    def __init__(self, R: int, E: int, device):
+    def __init__(self, R: int, E: int, device, expert_offsets: bool = True):
         import torch
 
         epr = E // R
         shapes = {"send_counts": (R, E), "send_offsets": (R, E), "recv_counts": (R, R),
                   "recv_offsets": (R, R), "recv_expert_counts": (R, R, epr), "recv_total": (R,),
                   "window_base": (R,), "recv_expert_offsets": (R, R, epr)}
+        self.names = self.NAMES if expert_offsets else self.NAMES[:-1]
         for n in self.NAMES:
-            setattr(self, n, torch.zeros(shapes[n], dtype=torch.int32, device=device))
-        self._ptrs = SplitsPtrs(*[getattr(self, n).data_ptr() for n in self.NAMES])
+            setattr(self, n, torch.zeros(shapes[n], dtype=torch.int32, device=device) if n in self.names else None)
+        self._ptrs = SplitsPtrs(*[getattr(self, n).data_ptr() if n in self.names else None for n in self.NAMES])
 
     @property
     def ptrs(self) -> SplitsPtrs:
         return self._ptrs
 
     def to_numpy(self) -> dict:
-        return {n: getattr(self, n).cpu().numpy() for n in self.NAMES}
+        return {n: getattr(self, n).cpu().numpy() for n in self.names}
 
 
 def _stream_ptr(stream, device):
@@ -225,8 +230,12 @@ class Plan:
             pass
 
     # ---- tensors ------------------------------------------------------------
-    def new_splits(self) -> Splits:
-        return Splits(self.R, self.E, self.device)
+    def new_splits(self, expert_offsets=None) -> Splits:
+        """Split arrays for this plan; ``expert_offsets`` None = only when the
+        receive order needs them (the expert-grouped order)."""
+        if expert_offsets is None:
+            expert_offsets = self.recv_order in ("expert", ORDER_EXPERT)
+        return Splits(self.R, self.E, self.device, expert_offsets=bool(expert_offsets))
 
     def new_buffers(self):
         """(recv [arena_rows][H] bf16, slot_map [R][T][k] int32, out [R][T][H] bf16), uninitialised."""

@@ -94,6 +94,11 @@ __device__ __forceinline__ int count_round(int *cnt, int e, bool good, int E, in
 // ---------------------------------------------------------------------------
 // Tiled kernel
 // ---------------------------------------------------------------------------
+// WRITE_REO: fill splits.recv_expert_offsets (compile-time: a caller that
+// does not ask for them gets a kernel without that code -- measured: the
+// mere presence of the extra stores in these latency-bound kernels cost about
+// 1 us per call).
+template <bool WRITE_REO>
 __global__ void __launch_bounds__(kHistThreads) hist_scan_kernel(const HistArgs a) {
     extern __shared__ int smem[];
     __shared__ int wtot[33];
@@ -262,8 +267,8 @@ __global__ void __launch_bounds__(kHistThreads) hist_scan_kernel(const HistArgs 
     // ---- first row of every (source, local expert) block ----------------------
     // One warp per destination d: d's received counts rec[d][s][le] (E
     // contiguous ints) are staged in the warp's scratch and scanned there.
+    if (!WRITE_REO) return;
     int32_t *reo = a.sp.recv_expert_offsets;
-    if (!reo) return;
     int *buf = smem + R * R + R + warp * E;  // [E] per warp
     const bool padded = g.window_mode == A2AV_WINDOW_PADDED;
     for (int d = warp; d < R; d += kHistWarps) {
@@ -310,8 +315,9 @@ __global__ void __launch_bounds__(kHistThreads) hist_scan_kernel(const HistArgs 
     }
 }
 
-size_t hist_smem_bytes(const Geometry &g) {
-    const size_t a = (size_t)kHistWarps * (g.E + 1), b = (size_t)g.R * g.R + g.R + (size_t)kHistWarps * g.E;
+size_t hist_smem_bytes(const Geometry &g, bool write_reo) {
+    const size_t a = (size_t)kHistWarps * (g.E + 1),
+                 b = (size_t)g.R * g.R + g.R + (write_reo ? (size_t)kHistWarps * g.E : 0);
     return sizeof(int) * (a > b ? a : b);
 }
 
@@ -339,6 +345,10 @@ __device__ __forceinline__ int ld_dsmem(uint32_t addr) {
     return v;
 }
 
+// BY_EXPERT: the expert-grouped receive order; WRITE_REO: fill
+// splits.recv_expert_offsets.  Both compile-time, so the plain source-order
+// instantiation carries none of their work.
+template <bool BY_EXPERT, bool WRITE_REO>
 __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(const HistArgs a) {
     extern __shared__ int smem[];
     __shared__ int wtot[33];
@@ -358,9 +368,10 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
     int *wb = ro + R;                    // [R] window totals, then bases
     int *xb = wb + R;                    // [E] expert order: rows of expert e on ranks below s
     int *xt = xb + E;                    // [E] expert order: rows of e on all ranks, then e's block start
-    const bool by_expert = g.recv_order == A2AV_ORDER_EXPERT;
+    constexpr bool by_expert = BY_EXPERT;
     for (int i = tid; i < kClusterWarps * ES; i += kClusterThreads) cnt[i] = 0;
-    for (int i = tid; i < 2 * E; i += kClusterThreads) xb[i] = 0;  // xb and xt
+    if (by_expert)
+        for (int i = tid; i < 2 * E; i += kClusterThreads) xb[i] = 0;  // xb and xt
     __syncthreads();
 
     int key[kClusterRounds], rank[kClusterRounds];
@@ -469,13 +480,6 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
             }
         }
     __syncthreads();
-    // first row of each of this rank's (destination, local expert) blocks
-    if (a.sp.recv_expert_offsets)
-        for (int e = tid; e < E; e += kClusterThreads) {
-            const int d = e / epr, le = e - d * epr;
-            a.sp.recv_expert_offsets[((size_t)d * R + s) * epr + le] =
-                by_expert ? xt[e] + xb[e] : ro[d] + so[e] - so[d * epr];
-        }
 
     bool ovf = false;
     int32_t *sm = a.slot_map + (size_t)s * A;
@@ -499,11 +503,18 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
         }
     }
     if (__any_sync(kFull, ovf) && lane == 0) atomicOr(a.status, (uint32_t)A2AV_DEV_WINDOW_OVERFLOW);
+    // first row of each of this rank's (destination, local expert) blocks
+    if (WRITE_REO)
+        for (int e = tid; e < E; e += kClusterThreads) {
+            const int d = e / epr, le = e - d * epr;
+            a.sp.recv_expert_offsets[((size_t)d * R + s) * epr + le] =
+                by_expert ? xt[e] + xb[e] : ro[d] + so[e] - so[d * epr];
+        }
 }
 
 size_t cluster_smem_bytes(const Geometry &g) {
-    return sizeof(int) *
-           ((size_t)kClusterWarps * (g.E + 1) + (g.E + 1) + (size_t)g.R * g.R + 2 * (size_t)g.R + 2 * (size_t)g.E);
+    return sizeof(int) * ((size_t)kClusterWarps * (g.E + 1) + (g.E + 1) + (size_t)g.R * g.R + 2 * (size_t)g.R +
+                          (g.recv_order == A2AV_ORDER_EXPERT ? 2 * (size_t)g.E : 0));
 }
 
 bool cluster_eligible(const Geometry &g) {
@@ -512,6 +523,14 @@ bool cluster_eligible(const Geometry &g) {
     const long long chunk = ((A + kClusterWarps - 1) / kClusterWarps + 31) / 32 * 32;
     return chunk <= 32 * kClusterRounds && cluster_smem_bytes(g) <= 160 * 1024;
 }
+
+using SplitsKernel = void (*)(const HistArgs);
+// (the expert order always writes the offsets: the pack reads them)
+SplitsKernel cluster_kernel_for(const Geometry &g, bool write_reo) {
+    if (g.recv_order == A2AV_ORDER_EXPERT) return splits_cluster_kernel<true, true>;
+    return write_reo ? splits_cluster_kernel<false, true> : splits_cluster_kernel<false, false>;
+}
+SplitsKernel hist_kernel_for(bool write_reo) { return write_reo ? hist_scan_kernel<true> : hist_scan_kernel<false>; }
 
 cudaLaunchConfig_t cluster_launch_config(const a2av_plan_s &p, cudaLaunchAttribute *at, cudaStream_t s) {
     cudaLaunchConfig_t lc = {};
@@ -532,16 +551,19 @@ cudaLaunchConfig_t cluster_launch_config(const a2av_plan_s &p, cudaLaunchAttribu
 
 cudaError_t configure_hist(a2av_plan_s &p) {
     if (!(p.cfg.flags & A2AV_FLAG_SPLITS_TILED) && cluster_eligible(p.g)) {
-        cudaError_t e = cudaFuncSetAttribute(splits_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             160 * 1024);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(splits_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        cudaError_t e = cudaSuccess;
+        for (auto k : {splits_cluster_kernel<false, false>, splits_cluster_kernel<false, true>,
+                       splits_cluster_kernel<true, true>}) {
+            if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+            if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        }
         if (e != cudaSuccess) return e;
+        const auto kern = cluster_kernel_for(p.g, true);
         // Can a cluster of R such CTAs be resident at all on this device?
         cudaLaunchAttribute at[1];
         cudaLaunchConfig_t lc = cluster_launch_config(p, at, nullptr);
         int clusters = 0;
-        e = cudaOccupancyMaxActiveClusters(&clusters, splits_cluster_kernel, &lc);
+        e = cudaOccupancyMaxActiveClusters(&clusters, kern, &lc);
         if (e == cudaSuccess && clusters >= 1) {
             p.splits_small = 1;
             p.hist.block = kClusterThreads;
@@ -553,25 +575,30 @@ cudaError_t configure_hist(a2av_plan_s &p) {
     }
     p.splits_small = 0;
     p.hist.block = kHistThreads;
-    p.hist.smem = hist_smem_bytes(p.g);
+    p.hist.smem = hist_smem_bytes(p.g, true);  // launches without the offsets take less
     p.hist.grid = p.g.tiles;
     // Per-kernel cap shared by every plan: the largest any valid plan needs.
     Geometry worst{};
     worst.R = kMaxRanks;
     worst.E = kMaxExperts;
-    return cudaFuncSetAttribute(hist_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)hist_smem_bytes(worst));
+    cudaError_t e = cudaSuccess;
+    for (bool w : {false, true})
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(hist_kernel_for(w), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)hist_smem_bytes(worst, true));
+    return e;
 }
 
 cudaError_t launch_hist(const a2av_plan_s &p, const HistArgs &a, cudaStream_t s) {
+    const bool reo = a.sp.recv_expert_offsets != nullptr;
     if (p.splits_small) {
         cudaLaunchAttribute at[1];
         cudaLaunchConfig_t lc = cluster_launch_config(p, at, s);
-        cudaError_t e = cudaLaunchKernelEx(&lc, splits_cluster_kernel, a);
+        cudaError_t e = cudaLaunchKernelEx(&lc, cluster_kernel_for(p.g, reo), a);
         if (e != cudaSuccess) return e;
     } else {
         dim3 grid(p.g.tiles, p.g.R);
-        hist_scan_kernel<<<grid, p.hist.block, p.hist.smem, s>>>(a);
+        hist_kernel_for(reo)<<<grid, p.hist.block, hist_smem_bytes(p.g, reo), s>>>(a);
     }
     return cudaGetLastError();
 }

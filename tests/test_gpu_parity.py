@@ -561,3 +561,22 @@ def test_expert_order_plan_requires_the_offsets_array():
     idx_t = torch.zeros((w.R, w.T, w.k), dtype=torch.int32, device=P.device())
     with pytest.raises(A.A2avError):
         plan.splits(idx_t, sp, slot_map)
+
+
+def test_expert_offsets_are_optional_in_source_order():
+    # asked for or not, everything else is the same; when asked for they are
+    # the oracle's
+    import torch
+
+    for wid, T, H in [(2, 1100, 264), (5, 300, 64)]:
+        w = W.WORKLOADS[wid].scaled(T=T, H=H)
+        x = W.make_x(w, 0, device=P.device())
+        rg = W.make_routing_gate(w, 0)
+        a = P.full_parity(w, x=x, idx=rg["topk_idx"], gate=rg["gate_w"], expert_offsets=True)
+        b = P.full_parity(w, x=x, idx=rg["topk_idx"], gate=rg["gate_w"], expert_offsets=False)
+        assert "recv_expert_offsets" in a["splits"] and "recv_expert_offsets" not in b["splits"]
+        np.testing.assert_array_equal(a["slot_map"], b["slot_map"])
+        np.testing.assert_array_equal(a["out"], b["out"])
+        for g in (a, b):
+            g["plan"].close()
+        torch.cuda.synchronize()

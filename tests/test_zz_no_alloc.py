@@ -24,7 +24,7 @@ def _plan_dispatch(w, x, idx_t):
     plan = A.Plan(w.R, w.E, w.T, w.H, w.k, w.window_mode, w.window_rows, device=x.device, recv_order=w.recv_order)
     recv, slot_map, _ = plan.new_buffers()
     recv.zero_()
-    sp = plan.new_splits()
+    sp = plan.new_splits(expert_offsets=True)
     plan.dispatch(x, idx_t, sp, recv, slot_map)
     return plan, sp, recv, slot_map
 
