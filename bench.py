@@ -108,27 +108,37 @@ def read_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def csrc_hash() -> str:
+# The sources each timed kernel is built from (its .cu file, the internal
+# header, the C ABI header).
+KERNEL_SOURCES = {
+    "splits": ["csrc/splits.cu"],
+    "pack": ["csrc/pack.cu"],
+    "combine": ["csrc/combine.cu"],
+    "route": ["csrc/router.cu"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "combine_device_resident_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        h.update(f.encode())
-        h.update(open(os.path.join(csrc, f), "rb").read())
+    pkg = os.path.join(ROOT, "combine_device_resident_gb300")
+    for rel in KERNEL_SOURCES[kernel] + ["csrc/a2av_internal.cuh"]:
+        h.update(rel.encode())
+        h.update(open(os.path.join(pkg, rel), "rb").read())
     h.update(open(os.path.join(ROOT, "include", "a2av.h"), "rb").read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    the kernel's current sources and on this workload (else None)."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         d = json.load(open(p))
     except Exception:
         return None
-    if d.get("source_sha") != csrc_hash():
-        return None
     ent = d.get("kernels", {}).get(kernel, {})
+    if kernel not in KERNEL_SOURCES or ent.get("source_sha") != kernel_source_hash(kernel):
+        return None
     if ent.get("workload") != workload:
         return None
     return ent.get("dram_bytes_per_launch")
@@ -478,7 +488,8 @@ def main():
     kus = {n: 1e3 * sum(v) / len(v) for n, v in kt.items() if v}
     dom = max((n for n in names if n not in ("splits", "route")), key=lambda n: kus.get(n, 0.0))
     ach = kbytes[dom] / (kus[dom] * 1e-6) / 1e9
-    traffic = None if (padded or t_active != w.T) else ncu_traffic(dom, w.name)
+    # (captured on the plain path: source order, every token, no padding)
+    traffic = None if (padded or t_active != w.T or w.recv_order != "source") else ncu_traffic(dom, w.name)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
                 "kernel_us": {n: round(v, 3) for n, v in kus.items()},
