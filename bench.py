@@ -53,7 +53,9 @@ def parse():
     ap.add_argument("--recv-order", choices=["source", "expert"], default="source",
                     help="rows inside each window: source segments (AllToAllv convention) or grouped by local expert")
     ap.add_argument("--router", action="store_true",
-                    help="start each step from per-token logits: router kernel (top-k + softmax) first")
+                    help="start each step from per-token logits: the router kernel, then the splits kernel")
+    ap.add_argument("--router-fused", action="store_true",
+                    help="with --router: the router inside the splits kernel (a2av_route_splits, fused flag)")
     ap.add_argument("--active-frac", type=float, default=1.0,
                     help="tokens taking part per rank, as a fraction of T (read from device memory)")
     ap.add_argument("--tokens", type=int, default=0,
@@ -335,7 +337,8 @@ def main():
     x = W.make_x(w, 0, device=dev)
     idx = torch.from_numpy(idx_h).to(dev)
     gate = torch.from_numpy(gate_h).to(dev)
-    plan = A.Plan(w.R, w.E, w.T, w.H, w.k, w.window_mode, w.window_rows, device=dev, flags=args.flags,
+    plan = A.Plan(w.R, w.E, w.T, w.H, w.k, w.window_mode, w.window_rows, device=dev,
+                  flags=args.flags | (A.FLAG_ROUTE_FUSED if args.router and args.router_fused else 0),
                   pack_ctas_per_sm=args.pack_ctas_per_sm, pack_stage_bytes=args.pack_stage_bytes,
                   pack_store_lag=args.pack_store_lag, combine_ctas_per_sm=args.combine_ctas_per_sm,
                   combine_stage_bytes=args.combine_stage_bytes, combine_unroll=args.combine_unroll,
@@ -367,12 +370,19 @@ def main():
                 ("pack", lambda s: plan.pack(x_, idx_, sp_, recv_, slot_, stream=s)),
                 ("combine", lambda s: plan.combine(recv_, gate_, slot_, out_, stream=s))]
 
-    stages = make_stages(x, idx, gate, sp, recv, slot_map, out, sendbuf)
-    logits = None
-    if args.router:
-        # the router writes idx and gate in place from logits resident in HBM
-        logits = W.make_logits(w, 0, device=dev)
-        stages = [("route", lambda s: plan.route(logits, idx, gate, stream=s))] + stages
+    logits = W.make_logits(w, 0, device=dev) if args.router else None
+
+    def with_router(st, idx_, gate_, sp_, slot_, logits_):
+        """The router writes idx and gate in place from logits resident in HBM:
+        fused into the splits kernel, or as its own kernel before it."""
+        if not args.router:
+            return st
+        if not args.router_fused:
+            return [("route", lambda s: plan.route(logits_, idx_, gate_, stream=s))] + st
+        return [("route+splits", lambda s: plan.route_splits(logits_, idx_, gate_, sp_, slot_, stream=s))] + st[1:]
+
+    stages = with_router(make_stages(x, idx, gate, sp, recv, slot_map, out, sendbuf), idx, gate, sp, slot_map,
+                         logits)
 
     def capture(stage_list):
         g = torch.cuda.CUDAGraph()
@@ -481,12 +491,13 @@ def main():
     kbytes = {
         "route": w.R * t_active * w.E * 4 + 8 * A_,
         "splits": 8 * A_,
+        "route+splits": w.R * t_active * w.E * 4 + 8 * A_,  # logits in, idx and gates out (no idx re-read)
         "pack": w.R * t_active * w.H * 2 * (1 + w.k) + 8 * A_,
         "exchange": 2 * w.R * w.R * w.T * w.k * w.H * 2,
         "combine": w.R * t_active * w.H * 2 * (1 + w.k) + 8 * A_,
     }
     kus = {n: 1e3 * sum(v) / len(v) for n, v in kt.items() if v}
-    dom = max((n for n in names if n not in ("splits", "route")), key=lambda n: kus.get(n, 0.0))
+    dom = max((n for n in names if n not in ("splits", "route", "route+splits")), key=lambda n: kus.get(n, 0.0))
     ach = kbytes[dom] / (kus[dom] * 1e-6) / 1e9
     # (captured on the plain path: source order, every token, no padding)
     traffic = None if (padded or t_active != w.T or w.recv_order != "source") else ncu_traffic(dom, w.name)
@@ -505,22 +516,26 @@ def main():
     # device buffers, each with its own captured graph; step i+1's inputs
     # stream in while step i computes and step i-1's result streams out (the
     # kernels of all steps stay on one stream and one plan).
-    x_pin = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
-    x_pin.copy_(x)
-    idx_pin = torch.from_numpy(idx_h).pin_memory()
-    gate_pin = torch.from_numpy(gate_h).pin_memory()
+    # The step's inputs: x with the routing (idx, gate), or x with the router's
+    # logits when the router is on the path.
+    def pinned(t):
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        return h
+
+    in_pins = [pinned(x)] + ([pinned(logits)] if args.router else [pinned(idx), pinned(gate)])
     outs_pin = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
-    h2d = x_pin.numel() * 2 + idx_pin.numel() * 4 + gate_pin.numel() * 4
+    h2d = sum(p_.numel() * p_.element_size() for p_ in in_pins)
     d2h = outs_pin[0].numel() * 2
+    ins1 = [x] + ([logits] if args.router else [idx, gate])
     serial_ms = []
     with torch.cuda.stream(stream):
         for i in range(min(args.e2e_steps, 10) + 3):
             flush_l2()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            x.copy_(x_pin, non_blocking=True)
-            idx.copy_(idx_pin, non_blocking=True)
-            gate.copy_(gate_pin, non_blocking=True)
+            for dst, src in zip(ins1, in_pins):
+                dst.copy_(src, non_blocking=True)
             graph.replay()
             outs_pin[0].copy_(out, non_blocking=True)
             b.record(stream)
@@ -534,12 +549,13 @@ def main():
     recv2, slot_map2, out2 = plan.new_buffers()
     sp2 = plan.new_splits()
     send2 = plan.new_send_buffer() if padded else None
-    sets = [(x, idx, gate, recv, slot_map, out, sp, graph)]
-    st2 = make_stages(x2, idx2, gate2, sp2, recv2, slot_map2, out2, send2)
-    if args.router:
-        st2 = [("route", lambda s: plan.route(logits, idx2, gate2, stream=s))] + st2
+    logits2 = torch.empty_like(logits) if args.router else None
+    ins2 = [x2] + ([logits2] if args.router else [idx2, gate2])
+    sets = [(ins1, out, graph)]
+    st2 = with_router(make_stages(x2, idx2, gate2, sp2, recv2, slot_map2, out2, send2), idx2, gate2, sp2,
+                      slot_map2, logits2)
     g2 = capture(st2)
-    sets.append((x2, idx2, gate2, recv2, slot_map2, out2, sp2, g2))
+    sets.append((ins2, out2, g2))
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_comp = [torch.cuda.Event() for _ in range(2)]
@@ -552,13 +568,12 @@ def main():
         t0.record(s_in)
         for i in range(n):
             b = i % 2
-            xb, ib, gb, _, _, ob, _, gr = sets[b]
+            ins, ob, gr = sets[b]
             with torch.cuda.stream(s_in):
                 if i >= 2:
                     s_in.wait_event(ev_comp[b])  # step i-2 has finished reading this set
-                xb.copy_(x_pin, non_blocking=True)
-                ib.copy_(idx_pin, non_blocking=True)
-                gb.copy_(gate_pin, non_blocking=True)
+                for dst, src in zip(ins, in_pins):
+                    dst.copy_(src, non_blocking=True)
                 ev_in[b].record(s_in)
             with torch.cuda.stream(stream):
                 stream.wait_event(ev_in[b])
@@ -583,7 +598,8 @@ def main():
     e2e = {"value": round(whole_job(bytes_step, w.R * t_active, pipe_ms, world)["gbs"], 2), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(pipe_ms, 4),
            "steps": n_pipe,
-           "path": ("double-buffered loop: pinned host x/idx/gate -> HBM (copy stream), graph replay "
+           "path": ("double-buffered loop: pinned host inputs (x and " +
+                    ("logits" if args.router else "idx/gate") + ") -> HBM (copy stream), graph replay "
                     "(compute stream), out -> pinned host (copy stream); every step copies its own "
                     "inputs and result"),
            "serial": {"value": round(whole_job(bytes_step, w.R * t_active, serial_t, world)["gbs"], 2),
@@ -601,7 +617,8 @@ def main():
             "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_block(w, f"flushed between steps (read of a {FLUSH_BYTES >> 20} MiB buffer)"),
-            "mode": args.mode, "active_tokens_per_rank": t_active, "router": bool(args.router),
+            "mode": args.mode, "active_tokens_per_rank": t_active,
+            "router": (("fused" if args.router_fused else "separate") if args.router else False),
             "pct_of_peak": round(100 * gbs / world / peak, 2), "peak_gbs": peak,
             "tokens_per_s": round(job["tokens_per_s"], 1), "us_per_call": round(job["us_per_call"], 3),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,

@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     FLAG_PACK_LSU,
     FLAG_SPLITS_TILED,
     FLAG_COMBINE_TMA,
+    FLAG_ROUTE_FUSED,
     ORDER_EXPERT,
     ORDER_SOURCE,
     Plan,

@@ -31,6 +31,7 @@ ORDER_EXPERT = 1  # windows grouped by local expert, sources in order inside eac
 FLAG_PACK_LSU = 1 << 0
 FLAG_SPLITS_TILED = 1 << 1
 FLAG_COMBINE_TMA = 1 << 2
+FLAG_ROUTE_FUSED = 1 << 3
 
 # Every function the header declares, for load checks.
 EXPORTED = [
@@ -39,7 +40,7 @@ EXPORTED = [
     "a2av_read_device_status", "a2av_device_status_ptr", "a2av_plan_launches",
     "a2av_status_string", "a2av_last_error", "a2av_dispatch_static",
     "a2av_dispatch_padded", "a2av_pack_padded", "a2av_exchange_padded", "a2av_set_active_tokens",
-    "a2av_route",
+    "a2av_route", "a2av_route_splits",
 ]
 
 
@@ -133,6 +134,8 @@ def load_library(path: Optional[str] = None):
     L.a2av_set_active_tokens.restype = i32
     L.a2av_route.argtypes = [vp, vp, vp, vp, vp]
     L.a2av_route.restype = i32
+    L.a2av_route_splits.argtypes = [vp, vp, vp, vp, spp, vp, vp]
+    L.a2av_route_splits.restype = i32
     if path is None:
         _lib = L
     return L
@@ -302,6 +305,18 @@ class Plan:
             self._t(topk_idx, torch.int32, (self.R, self.T, self.k), "topk_idx"),
             self._t(gate_w, torch.float32, (self.R, self.T, self.k), "gate_w"),
             _stream_ptr(stream, self.device)), "a2av_route")
+
+    def route_splits(self, logits, topk_idx, gate_w, splits: Splits, slot_map, stream=None):
+        """Router + splits in one kernel where possible (a2av_route_splits);
+        follow with ``pack`` as after ``splits``."""
+        import torch
+
+        _check(self.lib, self.lib.a2av_route_splits(
+            self.handle, self._t(logits, torch.float32, (self.R, self.T, self.E), "logits"),
+            self._t(topk_idx, torch.int32, (self.R, self.T, self.k), "topk_idx"),
+            self._t(gate_w, torch.float32, (self.R, self.T, self.k), "gate_w"), ctypes.byref(splits.ptrs),
+            self._t(slot_map, torch.int32, (self.R, self.T, self.k), "slot_map"),
+            _stream_ptr(stream, self.device)), "a2av_route_splits")
 
     def set_active_tokens(self, num_tokens=None):
         """Read per-rank token counts from the int32 device tensor `num_tokens`

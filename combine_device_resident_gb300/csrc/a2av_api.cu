@@ -86,7 +86,8 @@ a2av_status_t a2av_config_check(const a2av_config_t *c) {
         return A2AV_ERR_INVALID_ARG;
     }
     if (c->device < 0) return A2AV_ERR_INVALID_ARG;
-    if (c->flags & ~(uint32_t)(A2AV_FLAG_PACK_LSU | A2AV_FLAG_SPLITS_TILED | A2AV_FLAG_COMBINE_TMA))
+    if (c->flags & ~(uint32_t)(A2AV_FLAG_PACK_LSU | A2AV_FLAG_SPLITS_TILED | A2AV_FLAG_COMBINE_TMA |
+                               A2AV_FLAG_ROUTE_FUSED))
         return A2AV_ERR_INVALID_ARG;
     if (c->pack_store_lag < 0 || c->pack_store_lag > 8) return A2AV_ERR_INVALID_ARG;
     if (c->combine_ctas_per_sm < 0 || c->combine_ctas_per_sm > 8) return A2AV_ERR_INVALID_ARG;
@@ -167,6 +168,7 @@ a2av_status_t a2av_plan_create(const a2av_config_t *cfg, a2av_plan_t *out_plan) 
     if (e == cudaSuccess) e = a2av::configure_pack(*p);
     if (e == cudaSuccess) e = a2av::configure_combine(*p);
     if (e == cudaSuccess) e = a2av::configure_route(*p);
+    p->last_rows_final = p->splits_small;
     if (e != cudaSuccess) {
         cudaFree(p->workspace);
         delete p;
@@ -190,6 +192,7 @@ a2av_status_t a2av_splits(a2av_plan_t p, const int32_t *topk_idx, const a2av_spl
     DeviceGuard guard(p->cfg.device);
     if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
     a2av::HistArgs a;
+    memset(&a, 0, sizeof a);
     a.g = p->g;
     a.num_tokens = p->num_tokens;
     a.idx = topk_idx;
@@ -202,6 +205,7 @@ a2av_status_t a2av_splits(a2av_plan_t p, const int32_t *topk_idx, const a2av_spl
     cudaError_t e = a2av::launch_hist(*p, a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "splits kernel launch");
     p->launches += 1;
+    p->last_rows_final = p->splits_small;
     return A2AV_OK;
 }
 
@@ -250,6 +254,7 @@ static a2av_status_t pack_into(a2av_plan_t p, const void *x, const int32_t *topk
     a.recv = static_cast<uint16_t *>(recv);
     a.status = p->status;
     a.padded_tk = padded ? (int64_t)p->g.T * p->g.k : 0;
+    a.rows_final = p->last_rows_final;
     cudaError_t e = a2av::launch_pack(*p, a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "pack kernel launch");
     p->launches += 1;
@@ -378,6 +383,42 @@ a2av_status_t a2av_route(a2av_plan_t p, const float *logits, int32_t *topk_idx, 
     cudaError_t e = a2av::launch_route(*p, a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "route kernel launch");
     p->launches += 1;
+    return A2AV_OK;
+}
+
+a2av_status_t a2av_route_splits(a2av_plan_t p, const float *logits, int32_t *topk_idx, float *gate_w,
+                                const a2av_splits_t *splits, int32_t *slot_map, void *stream) {
+    if (!p || !aligned(logits, 4) || !aligned(topk_idx, 4) || !aligned(gate_w, 4) || !aligned(slot_map, 4) ||
+        !splits_ok(p, splits))
+        return A2AV_ERR_INVALID_ARG;
+    if (p->g.k > p->g.E) {
+        a2av::set_last_error("a2av_route_splits: k distinct experts need k <= E");
+        return A2AV_ERR_INVALID_ARG;
+    }
+    if (!(p->cfg.flags & A2AV_FLAG_ROUTE_FUSED) || !a2av::routed_splits_supported(*p)) {  // the two kernels
+        a2av_status_t st = a2av_route(p, logits, topk_idx, gate_w, stream);
+        return st == A2AV_OK ? a2av_splits(p, topk_idx, splits, slot_map, stream) : st;
+    }
+    DeviceGuard guard(p->cfg.device);
+    if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+    a2av::HistArgs a;
+    memset(&a, 0, sizeof a);
+    a.g = p->g;
+    a.num_tokens = p->num_tokens;
+    a.idx = topk_idx;
+    a.slot_map = slot_map;
+    a.tile_base = p->tile_base;
+    a.rank_total = p->rank_total;
+    a.counters = p->counters;
+    a.status = p->status;
+    a.sp = to_internal(splits);
+    a.logits = logits;
+    a.idx_out = topk_idx;
+    a.gate_out = gate_w;
+    cudaError_t e = a2av::launch_routed_hist(*p, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "routed splits kernel launch");
+    p->launches += 1;
+    p->last_rows_final = 0;
     return A2AV_OK;
 }
 

@@ -49,6 +49,10 @@ struct HistArgs {
     uint32_t *counters;   // [R + 1] last-block-done counters (left at 0)
     uint32_t *status;
     Splits sp;
+    // routed variant (a2av_route_splits): logits in, topk_idx and gates out
+    const float *logits;  // [R][T][E]
+    int32_t *idx_out;     // [R][T][k]
+    float *gate_out;      // [R][T][k]
 };
 
 struct PackArgs {
@@ -145,6 +149,9 @@ struct a2av_plan_s {
     int pack_tma = 1;
     int32_t pack_chunk_bytes = 0, pack_nchunks = 0, pack_stages = 0, pack_lag = 1;
     int64_t launches = 0;
+    // 1: the last splits launch left final rows in slot_map (cluster kernel);
+    // 0: tile ranks (tiled kernels).  The next pack reads it.
+    int last_rows_final = 0;
 };
 
 namespace a2av {
@@ -173,6 +180,10 @@ cudaError_t launch_combine(const a2av_plan_s &p, const CombineArgs &a, cudaStrea
 cudaError_t launch_scale(const a2av_plan_s &p, const ScaleArgs &a, cudaStream_t s);
 cudaError_t launch_exchange_padded(const a2av_plan_s &p, const ExchangeArgs &a, cudaStream_t s);
 cudaError_t launch_route(const a2av_plan_s &p, const RouteArgs &a, cudaStream_t s);
+// Router fused into the tiled histogram (E <= 256, k | 32); slot_map then
+// holds tile ranks.
+bool routed_splits_supported(const a2av_plan_s &p);
+cudaError_t launch_routed_hist(const a2av_plan_s &p, const HistArgs &a, cudaStream_t s);
 cudaError_t configure_route(a2av_plan_s &p);
 
 // Records the text a2av_last_error() returns on the calling thread.

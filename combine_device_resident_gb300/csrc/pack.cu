@@ -413,8 +413,7 @@ cudaError_t launch_exchange_padded(const a2av_plan_s &p, const ExchangeArgs &a, 
 }
 
 cudaError_t launch_pack(const a2av_plan_s &p, const PackArgs &a, cudaStream_t s) {
-    PackArgs b = a;
-    b.rows_final = p.splits_small;
+    PackArgs b = a;  // b.rows_final: set by the caller from the splits launch that preceded it
     cudaError_t e;
     if (p.pack_tma) {
         b.chunk_bytes = p.pack_chunk_bytes;

@@ -33,6 +33,7 @@
 // Both let the pack kernel begin launching at once (programmatic dependent
 // launch); the pack kernel waits for this grid before reading its output.
 #include "a2av_internal.cuh"
+#include "route_select.cuh"
 
 namespace a2av {
 namespace {
@@ -97,9 +98,15 @@ __device__ __forceinline__ int count_round(int *cnt, int e, bool good, int E, in
 // WRITE_REO: fill splits.recv_expert_offsets (compile-time: a caller that
 // does not ask for them gets a kernel without that code -- measured: the
 // mere presence of the extra stores in these latency-bound kernels cost about
-// 1 us per call).
-template <bool WRITE_REO>
-__global__ void __launch_bounds__(kHistThreads) hist_scan_kernel(const HistArgs a) {
+// 1 us per call).  ROUTE_EPL > 0: the router runs here -- each warp routes the
+// tokens of its assignments from the logits (route_token, ROUTE_EPL logits
+// per lane), writes topk_idx and gate_w, and counts the ids it just chose,
+// without reading topk_idx back (needs k | 32).  NW warps per CTA, ROUNDS
+// rounds of 32 assignments per warp: one tile = NW * 32 * ROUNDS.
+template <bool WRITE_REO, int ROUTE_EPL, int NW>
+__global__ void __launch_bounds__(NW * 32) hist_scan_kernel(const HistArgs a) {
+    constexpr int ROUNDS = kHistTile / (NW * 32);
+    static_assert(NW * 32 * ROUNDS == kHistTile, "a CTA covers one tile");
     extern __shared__ int smem[];
     __shared__ int wtot[33];
     __shared__ int last;
@@ -115,18 +122,44 @@ __global__ void __launch_bounds__(kHistThreads) hist_scan_kernel(const HistArgs 
     int *cnt = smem + warp * ES;
     for (int e = lane; e < E; e += 32) cnt[e] = 0;
     __syncwarp();
-    const int w0 = tile * kHistTile + warp * (32 * kHistRounds);
-    const int32_t *idx = a.idx + (size_t)s * A;
-    int key[kHistRounds], rank[kHistRounds];
-    int vals[kHistRounds];
+    const int w0 = tile * kHistTile + warp * (32 * ROUNDS);
+    int key[ROUNDS], rank[ROUNDS];
+    int vals[ROUNDS];
+    if (ROUTE_EPL == 0) {
+        const int32_t *idx = a.idx + (size_t)s * A;
 #pragma unroll
-    for (int r = 0; r < kHistRounds; ++r) {
-        const int ai = w0 + r * 32 + lane;
-        vals[r] = ai < A ? __ldg(idx + ai) : -1;
+        for (int r = 0; r < ROUNDS; ++r) {
+            const int ai = w0 + r * 32 + lane;
+            vals[r] = ai < A ? __ldg(idx + ai) : -1;
+        }
+    } else {
+        // a round of 32 assignments is 32/k whole tokens; lane l counts slot
+        // l % k of token l / k
+        const int k = g.k, tpr = 32 / k, lt = lane / k, ls = lane - lt * k;
+        const int Ts = active_tokens(a.num_tokens, s, g.T);
+#pragma unroll
+        for (int r = 0; r < ROUNDS; ++r) {
+            vals[r] = -1;
+            const int t0 = (w0 + r * 32) / k;
+            for (int m = 0; m < tpr; ++m) {
+                const int t = t0 + m;
+                if (t >= Ts) break;  // warp-uniform: past the rank's active (or all) tokens
+                int32_t id;
+                float w;
+                const size_t tok = (size_t)s * g.T + t;
+                route_token<(ROUTE_EPL > 0 ? ROUTE_EPL : 1)>(a.logits + tok * E, E, k, lane, id, w);
+                if (lane < k) {
+                    a.idx_out[tok * k + lane] = id;
+                    a.gate_out[tok * k + lane] = w;
+                }
+                const int got = __shfl_sync(kFull, id, ls);
+                if (lt == m) vals[r] = got;
+            }
+        }
     }
     bool bad = false;
 #pragma unroll
-    for (int r = 0; r < kHistRounds; ++r) {
+    for (int r = 0; r < ROUNDS; ++r) {
         if (w0 + r * 32 >= A) break;  // warp-uniform
         const int ai = w0 + r * 32 + lane;
         const int e = vals[r];
@@ -144,7 +177,7 @@ __global__ void __launch_bounds__(kHistThreads) hist_scan_kernel(const HistArgs 
     for (int e = tid; e < E; e += blockDim.x) {
         int run = 0;
 #pragma unroll
-        for (int w = 0; w < kHistWarps; ++w) {
+        for (int w = 0; w < NW; ++w) {
             const int v = smem[w * ES + e];
             smem[w * ES + e] = run;
             run += v;
@@ -154,7 +187,7 @@ __global__ void __launch_bounds__(kHistThreads) hist_scan_kernel(const HistArgs 
     __syncthreads();
     int32_t *sm = a.slot_map + (size_t)s * A;
 #pragma unroll
-    for (int r = 0; r < kHistRounds; ++r) {
+    for (int r = 0; r < ROUNDS; ++r) {
         if (w0 + r * 32 >= A) break;
         const int ai = w0 + r * 32 + lane;
         if (ai < A) sm[ai] = key[r] >= 0 ? cnt[key[r]] + rank[r] : -1;
@@ -226,7 +259,7 @@ __global__ void __launch_bounds__(kHistThreads) hist_scan_kernel(const HistArgs 
     }
     __syncthreads();
     // one warp per window: receive offsets (scan over sources) and totals
-    for (int d = warp; d < R; d += kHistWarps) {
+    for (int d = warp; d < R; d += NW) {
         int carry = 0;
         for (int c0 = 0; c0 < R; c0 += 32) {
             const int src = c0 + lane;
@@ -271,7 +304,7 @@ __global__ void __launch_bounds__(kHistThreads) hist_scan_kernel(const HistArgs 
     int32_t *reo = a.sp.recv_expert_offsets;
     int *buf = smem + R * R + R + warp * E;  // [E] per warp
     const bool padded = g.window_mode == A2AV_WINDOW_PADDED;
-    for (int d = warp; d < R; d += kHistWarps) {
+    for (int d = warp; d < R; d += NW) {
         const int32_t *rec = a.sp.recv_expert_counts + (size_t)d * E;  // [R][epr]
         for (int i = lane; i < E; i += 32) buf[i] = __ldcg(rec + i);
         __syncwarp();
@@ -315,10 +348,19 @@ __global__ void __launch_bounds__(kHistThreads) hist_scan_kernel(const HistArgs 
     }
 }
 
-size_t hist_smem_bytes(const Geometry &g, bool write_reo) {
-    const size_t a = (size_t)kHistWarps * (g.E + 1),
-                 b = (size_t)g.R * g.R + g.R + (write_reo ? (size_t)kHistWarps * g.E : 0);
+size_t hist_smem_bytes(const Geometry &g, bool write_reo, int nw) {
+    const size_t a = (size_t)nw * (g.E + 1), b = (size_t)g.R * g.R + g.R + (write_reo ? (size_t)nw * g.E : 0);
     return sizeof(int) * (a > b ? a : b);
+}
+
+// The routed tiled kernel: 32 warps of 2 rounds per tile (more warps in
+// flight for the routing work), E <= 32 * 8, k dividing 32.
+constexpr int kRoutedWarps = 32;
+constexpr int kRoutedMaxEpl = 8;
+int routed_epl(const Geometry &g) {
+    if (g.k < 1 || 32 % g.k != 0 || g.k > g.E) return 0;
+    const int need = (g.E + 31) / 32;
+    return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : need <= kRoutedMaxEpl ? 8 : 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -530,7 +572,15 @@ SplitsKernel cluster_kernel_for(const Geometry &g, bool write_reo) {
     if (g.recv_order == A2AV_ORDER_EXPERT) return splits_cluster_kernel<true, true>;
     return write_reo ? splits_cluster_kernel<false, true> : splits_cluster_kernel<false, false>;
 }
-SplitsKernel hist_kernel_for(bool write_reo) { return write_reo ? hist_scan_kernel<true> : hist_scan_kernel<false>; }
+SplitsKernel hist_kernel_for(bool write_reo, int route_epl = 0) {
+    switch (route_epl) {
+        case 1: return write_reo ? hist_scan_kernel<true, 1, kRoutedWarps> : hist_scan_kernel<false, 1, kRoutedWarps>;
+        case 2: return write_reo ? hist_scan_kernel<true, 2, kRoutedWarps> : hist_scan_kernel<false, 2, kRoutedWarps>;
+        case 4: return write_reo ? hist_scan_kernel<true, 4, kRoutedWarps> : hist_scan_kernel<false, 4, kRoutedWarps>;
+        case 8: return write_reo ? hist_scan_kernel<true, 8, kRoutedWarps> : hist_scan_kernel<false, 8, kRoutedWarps>;
+        default: return write_reo ? hist_scan_kernel<true, 0, kHistWarps> : hist_scan_kernel<false, 0, kHistWarps>;
+    }
+}
 
 cudaLaunchConfig_t cluster_launch_config(const a2av_plan_s &p, cudaLaunchAttribute *at, cudaStream_t s) {
     cudaLaunchConfig_t lc = {};
@@ -549,7 +599,31 @@ cudaLaunchConfig_t cluster_launch_config(const a2av_plan_s &p, cudaLaunchAttribu
 
 }  // namespace
 
+// Per-kernel caps shared by every plan: the largest any valid plan needs.
+cudaError_t configure_tiled_hist_attributes() {
+    Geometry worst{};
+    worst.R = kMaxRanks;
+    worst.E = kMaxExperts;
+    Geometry worst_routed = worst;
+    worst_routed.E = 32 * kRoutedMaxEpl;
+    cudaError_t e = cudaSuccess;
+    for (bool w : {false, true}) {
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(hist_kernel_for(w), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)hist_smem_bytes(worst, true, kHistWarps));
+        for (int epl : {1, 2, 4, 8})
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(hist_kernel_for(w, epl), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)hist_smem_bytes(worst_routed, true, kRoutedWarps));
+    }
+    return e;
+}
+
 cudaError_t configure_hist(a2av_plan_s &p) {
+    {  // the tiled kernels serve every plan (the routed one even cluster-eligible ones)
+        cudaError_t e = configure_tiled_hist_attributes();
+        if (e != cudaSuccess) return e;
+    }
     if (!(p.cfg.flags & A2AV_FLAG_SPLITS_TILED) && cluster_eligible(p.g)) {
         cudaError_t e = cudaSuccess;
         for (auto k : {splits_cluster_kernel<false, false>, splits_cluster_kernel<false, true>,
@@ -575,18 +649,9 @@ cudaError_t configure_hist(a2av_plan_s &p) {
     }
     p.splits_small = 0;
     p.hist.block = kHistThreads;
-    p.hist.smem = hist_smem_bytes(p.g, true);  // launches without the offsets take less
+    p.hist.smem = hist_smem_bytes(p.g, true, kHistWarps);  // launches without the offsets take less
     p.hist.grid = p.g.tiles;
-    // Per-kernel cap shared by every plan: the largest any valid plan needs.
-    Geometry worst{};
-    worst.R = kMaxRanks;
-    worst.E = kMaxExperts;
-    cudaError_t e = cudaSuccess;
-    for (bool w : {false, true})
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(hist_kernel_for(w), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)hist_smem_bytes(worst, true));
-    return e;
+    return cudaSuccess;
 }
 
 cudaError_t launch_hist(const a2av_plan_s &p, const HistArgs &a, cudaStream_t s) {
@@ -598,8 +663,25 @@ cudaError_t launch_hist(const a2av_plan_s &p, const HistArgs &a, cudaStream_t s)
         if (e != cudaSuccess) return e;
     } else {
         dim3 grid(p.g.tiles, p.g.R);
-        hist_kernel_for(reo)<<<grid, p.hist.block, hist_smem_bytes(p.g, reo), s>>>(a);
+        hist_kernel_for(reo)<<<grid, kHistThreads, hist_smem_bytes(p.g, reo, kHistWarps), s>>>(a);
     }
+    return cudaGetLastError();
+}
+
+}  // namespace a2av
+
+namespace a2av {
+
+bool routed_splits_supported(const a2av_plan_s &p) { return routed_epl(p.g) != 0; }
+
+// The router fused into the tiled histogram: always the tiled kernel, so
+// slot_map holds tile ranks afterwards (the pack assembles the rows).
+cudaError_t launch_routed_hist(const a2av_plan_s &p, const HistArgs &a, cudaStream_t s) {
+    const int epl = routed_epl(p.g);
+    if (!epl) return cudaErrorInvalidValue;
+    const bool reo = a.sp.recv_expert_offsets != nullptr;
+    dim3 grid(p.g.tiles, p.g.R);
+    hist_kernel_for(reo, epl)<<<grid, kRoutedWarps * 32, hist_smem_bytes(p.g, reo, kRoutedWarps), s>>>(a);
     return cudaGetLastError();
 }
 

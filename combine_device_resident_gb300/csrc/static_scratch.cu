@@ -154,6 +154,7 @@ extern "C" a2av_status_t a2av_dispatch_static(const a2av_config_t *cfg, const vo
         a.recv_expert_offsets = splits->recv_expert_offsets;
         a.recv = static_cast<uint16_t *>(recv);
         a.status = dev_status;
+        a.rows_final = p.splits_small;
         e = a2av::launch_pack(p, a, s);
     }
     if (prev >= 0 && prev != cfg->device) cudaSetDevice(prev);

@@ -120,6 +120,8 @@ enum {
     A2AV_FLAG_PACK_LSU = 1u << 0,     /* pack+exchange with 16-byte vector loads/stores instead of TMA bulk copies */
     A2AV_FLAG_SPLITS_TILED = 1u << 1, /* always use the multi-CTA tiled splits kernel (else one CTA when it fits) */
     A2AV_FLAG_COMBINE_TMA = 1u << 2,  /* combine through TMA bulk copies into shared memory (default: vector gathers) */
+    A2AV_FLAG_ROUTE_FUSED = 1u << 3,  /* a2av_route_splits: the router inside the tiled histogram kernel (default: the
+                                         router kernel, then the splits kernel -- measured faster, see the call) */
 };
 
 typedef struct {
@@ -275,6 +277,21 @@ a2av_status_t a2av_exchange_padded(a2av_plan_t plan, const void *sendbuf, void *
  * [Inference section, Figure 13: a router kernel picks each token's experts
  * before the tokens are sorted by expert; the pages do not define it.] */
 a2av_status_t a2av_route(a2av_plan_t plan, const float *logits, int32_t *topk_idx, float *gate_w, void *stream);
+
+/* The router and the first half of dispatch: the same routing as a2av_route
+ * (written to topk_idx and gate_w) and the same splits and slot_map contents
+ * as a2av_splits.  By default it enqueues exactly those two kernels.  With
+ * A2AV_FLAG_ROUTE_FUSED in the plan's flags, and when k divides 32 and
+ * E <= 256, it is one kernel instead: the tiled histogram kernel routes the
+ * tokens of its own tiles and counts the ids as it chooses them, without
+ * reading topk_idx back.  (Measured on GB300 the fused kernel is slower: a
+ * histogram tile of 2048 assignments gives the routing too few warps.)
+ * Follow it with a2av_pack on the same plan and stream, as after
+ * a2av_splits.  Same argument rules as those two calls; needs k <= E.
+ * [Inference section, Figure 13: the router kernel picks the experts, and the
+ * tokens are then sorted and counted by expert.] */
+a2av_status_t a2av_route_splits(a2av_plan_t plan, const float *logits, int32_t *topk_idx, float *gate_w,
+                                const a2av_splits_t *splits, int32_t *slot_map, void *stream);
 
 /* Variable batches (decode): from now on every kernel this plan enqueues
  * reads num_tokens[s] -- a caller-owned DEVICE array of R int32, read when

@@ -580,3 +580,103 @@ def test_expert_offsets_are_optional_in_source_order():
         for g in (a, b):
             g["plan"].close()
         torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------------------
+# router fused into the histogram (a2av_route_splits)
+# ---------------------------------------------------------------------------
+def _routed_step(w, x, logits, fused, nt=None, flags=0):
+    """fused: a2av_route_splits with the router inside the histogram kernel;
+    else the router kernel and the splits kernel as two calls."""
+    import torch
+    from combine_device_resident_gb300 import FLAG_ROUTE_FUSED, Plan
+
+    dev = P.device()
+    plan = Plan(w.R, w.E, w.T, w.H, w.k, w.window_mode, w.window_rows, device=dev,
+                flags=flags | (FLAG_ROUTE_FUSED if fused else 0), recv_order=w.recv_order)
+    if nt is not None:
+        plan.set_active_tokens(torch.from_numpy(nt).to(dev))
+    idx = torch.full((w.R, w.T, w.k), -9, dtype=torch.int32, device=dev)
+    gate = torch.full((w.R, w.T, w.k), -1.0, dtype=torch.float32, device=dev)
+    recv = torch.full((plan.arena_rows, w.H), -7.0, dtype=torch.bfloat16, device=dev)
+    slot_map = torch.empty((w.R, w.T, w.k), dtype=torch.int32, device=dev)
+    out = torch.full((w.R, w.T, w.H), 3.0, dtype=torch.bfloat16, device=dev)
+    sp = plan.new_splits(expert_offsets=True)
+    if fused:
+        plan.route_splits(logits, idx, gate, sp, slot_map)
+    else:
+        plan.route(logits, idx, gate)
+        plan.splits(idx, sp, slot_map)
+    plan.pack(x, idx, sp, recv, slot_map)
+    plan.combine(recv, gate, slot_map, out)
+    torch.cuda.synchronize()
+    res = {"idx": idx.cpu().numpy(), "gate": gate.cpu().numpy(), "splits": sp.to_numpy(),
+           "slot_map": slot_map.cpu().numpy(), "recv": P.bits(recv), "out": P.bits(out),
+           "status": plan.read_status()}
+    plan.close()
+    return res
+
+
+ROUTED = [
+    (4, 900, 72, 0, "fused: r16 E128 top-2, cluster-eligible plan"),
+    (5, 300, 64, 0, "fused: r32 E256 top-8, tiled plan"),
+    (2, 1100, 64, 0, "fused: r8 E16 top-1"),
+    (4, 700, 72, 2, "fused, plan forced tiled"),
+]
+
+
+@pytest.mark.parametrize("wid,T,H,flags,_", ROUTED, ids=[r[4] for r in ROUTED])
+def test_route_splits_equals_route_then_splits_and_oracle(wid, T, H, flags, _):
+    w = W.WORKLOADS[wid].scaled(T=T, H=H)
+    x = W.make_x(w, 0, device=P.device())
+    logits = W.make_logits(w, 0, device=P.device())
+    a = _routed_step(w, x, logits, fused=True, flags=flags)
+    b = _routed_step(w, x, logits, fused=False, flags=flags)
+    for key in ("idx", "gate", "slot_map", "out"):
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    for key in a["splits"]:
+        np.testing.assert_array_equal(a["splits"][key], b["splits"][key], err_msg=key)
+    rows = a["slot_map"][a["slot_map"] >= 0]
+    np.testing.assert_array_equal(a["recv"][rows], b["recv"][rows])
+    # against the oracle's router and path
+    ridx, rgate = oracle.route(logits.cpu().numpy(), w.k)
+    ref = oracle.run_all(w.R, w.E, P.bits(x), ridx, rgate.astype(np.float32))
+    np.testing.assert_array_equal(a["idx"], ridx)
+    P.check_splits(a["splits"], ref["splits"])
+    np.testing.assert_array_equal(a["slot_map"], ref["slot_map"])
+    assert ulp_diff(a["out"], ref["out"]).max() <= P.COMBINE_ULP_TOL
+    assert a["status"] == 0
+
+
+def test_route_splits_fallback_active_tokens_and_layouts():
+    # not fusable (k = 3, or E > 256): the two kernels; fusable with active
+    # counts, fixed windows and the expert-grouped order
+    import dataclasses
+
+    cases = [
+        (W.Workload("k3", R=3, E=111, T=200, H=40, k=3), None),
+        (W.Workload("e512", R=4, E=512, T=64, H=24, k=8), None),
+        (W.WORKLOADS[5].scaled(T=300, H=40), "counts"),
+        (dataclasses.replace(W.WORKLOADS[3].scaled(T=500, H=40), window_rows=400), None),
+        (dataclasses.replace(W.WORKLOADS[5].scaled(T=200, H=40), recv_order="expert"), "counts"),
+    ]
+    for w, mode in cases:
+        nt = np.array([(s_ * 37 + 11) % (w.T + 1) for s_ in range(w.R)], np.int32) if mode else None
+        x = W.make_x(w, 0, device=P.device())
+        logits = W.make_logits(w, 3, device=P.device())
+        a = _routed_step(w, x, logits, fused=True, nt=nt)
+        b = _routed_step(w, x, logits, fused=False, nt=nt)
+        for key in ("idx", "gate", "slot_map", "out"):
+            np.testing.assert_array_equal(a[key], b[key], err_msg=f"{w.name} {key}")
+        for key in a["splits"]:
+            np.testing.assert_array_equal(a["splits"][key], b["splits"][key], err_msg=f"{w.name} {key}")
+        assert a["status"] == b["status"]
+        ridx, rgate = oracle.route(logits.cpu().numpy(), w.k, num_tokens=nt)
+        ref = oracle.run_all(w.R, w.E, P.bits(x), ridx, rgate.astype(np.float32), w.window_mode, w.window_rows,
+                             num_tokens=nt, recv_order=w.recv_order)
+        P.check_splits(a["splits"], ref["splits"])
+        np.testing.assert_array_equal(a["slot_map"], ref["slot_map"], err_msg=w.name)
+        assert a["status"] == ref["status"], w.name
+        if nt is not None:  # tokens that take no part keep their idx/gate/out
+            for s_ in range(w.R):
+                assert (a["idx"][s_, nt[s_]:] == -9).all() and (a["gate"][s_, nt[s_]:] == -1.0).all()
