@@ -594,6 +594,28 @@ def main():
 
     pipelined(4)  # warm-up
     pipe_ms = max_over_ranks(pipelined(n_pipe))
+
+    def copies_only(n):
+        """The same per-step copies with no kernels: inputs in on s_in, the
+        result out on s_out, concurrently -- the host link's floor for a step."""
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        t0.record(s_in)
+        s_out.wait_stream(s_in)
+        for i in range(n):
+            ins, ob, _ = sets[i % 2]
+            with torch.cuda.stream(s_in):
+                for dst, src in zip(ins, in_pins):
+                    dst.copy_(src, non_blocking=True)
+            with torch.cuda.stream(s_out):
+                outs_pin[i % 2].copy_(ob, non_blocking=True)
+        s_in.wait_stream(s_out)
+        t1.record(s_in)
+        t1.synchronize()
+        return t0.elapsed_time(t1) / n
+
+    copies_only(2)
+    link_ms = max_over_ranks(copies_only(n_pipe))
     serial_t = max_over_ranks(sum(serial_ms) / len(serial_ms))
     e2e = {"value": round(whole_job(bytes_step, w.R * t_active, pipe_ms, world)["gbs"], 2), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(pipe_ms, 4),
@@ -602,6 +624,8 @@ def main():
                     ("logits" if args.router else "idx/gate") + ") -> HBM (copy stream), graph replay "
                     "(compute stream), out -> pinned host (copy stream); every step copies its own "
                     "inputs and result"),
+           "link_only_ms_per_step": round(link_ms, 4),
+           "link_gbs": round((h2d + d2h) / (link_ms * 1e-3) / 1e9, 1),
            "serial": {"value": round(whole_job(bytes_step, w.R * t_active, serial_t, world)["gbs"], 2),
                       "ms_per_step": round(serial_t, 4), "path": "one step at a time on one stream"}}
 
