@@ -23,6 +23,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -73,6 +74,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--l2", choices=["flush", "warm"], default="flush",
+                    help="flush L2 before every step (default) or replay back to back with a warm L2 "
+                         "(context for workloads that fit in L2; not the reported default)")
     ap.add_argument("--reference-seconds", type=float, default=90.0, help="reference arm: total budget")
     return ap.parse_args()
 
@@ -236,7 +240,29 @@ def cpu_baseline(w: W.Workload, x_host_bits, idx, gate, budget_s: float):
     sample = (f"oracle (splits, dispatch, combine) on the first {T_s} of {w.T} tokens per rank "
               f"of every rank, {reps} rep(s), {spent:.1f} s")
     return {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
-            "tokens_per_s": round(ws.R * ws.T * reps / spent, 1)}
+            "tokens_per_s": round(ws.R * ws.T * reps / spent, 1), "host": host_cpu()}
+
+
+def host_cpu() -> dict:
+    """The host the CPU figures come from: usable cores and CPU model."""
+    model = platform.machine()
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                return {"usable_cores": len(os.sched_getaffinity(0)),
+                        "cpu": f"{platform.machine()} {line.split(':', 1)[1].strip()}"}
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            key = line.split(":")[0].strip().lower()
+            if key in ("model name", "cpu part", "hardware"):
+                model = f"{platform.machine()} {line.split(':', 1)[1].strip()}"
+                break
+    except OSError:
+        pass
+    return {"usable_cores": len(os.sched_getaffinity(0)), "cpu": model}
 
 
 # ---------------------------------------------------------------------------
@@ -279,7 +305,8 @@ def run_reference(args, w: W.Workload):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_block(w, "none (host memory)"),
         "tokens_per_s": round(ws.R * ws.T / dt, 2), "us_per_call": round(dt * 1e6, 2),
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
+                         "host": host_cpu()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -412,7 +439,8 @@ def main():
     prefixes = [capture(stages[:n]) for n in range(1, len(stages))] + [graph]
 
     def flush_l2():
-        torch.sum(flush, dim=0, out=flush_out)
+        if args.l2 == "flush":
+            torch.sum(flush, dim=0, out=flush_out)
 
     # graph-launch floor: a graph holding one tiny kernel, timed like a step
     g_null = torch.cuda.CUDAGraph()
@@ -451,6 +479,7 @@ def main():
     sampler.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = max_over_ranks(sum(step_ms) / K)
+    ms_median = max_over_ranks(sorted(step_ms)[K // 2])
     status = plan.read_status()
     if status != 0:
         raise RuntimeError(f"device status word set during the timed region: {status:#x}")
@@ -638,9 +667,11 @@ def main():
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
-            "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5), "higher_is_better": True,
+            "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5), "ms_median_per_step": round(ms_median, 5),
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": config_block(w, f"flushed between steps (read of a {FLUSH_BYTES >> 20} MiB buffer)"),
+            "config": config_block(w, f"flushed between steps (read of a {FLUSH_BYTES >> 20} MiB buffer)"
+                                   if args.l2 == "flush" else "warm: steps back to back, no flush"),
             "mode": args.mode, "active_tokens_per_rank": t_active,
             "router": (("fused" if args.router_fused else "separate") if args.router else False),
             "pct_of_peak": round(100 * gbs / world / peak, 2), "peak_gbs": peak,
