@@ -32,6 +32,13 @@
 // shared-memory update, and each lane gets its stable rank in the group.
 // Both let the pack kernel begin launching at once (programmatic dependent
 // launch); the pack kernel waits for this grid before reading its output.
+//
+// Compile-time variants: with or without the code that fills
+// recv_expert_offsets (the first row of each (source, local expert) block;
+// chosen per launch from whether the caller passed that array), the cluster
+// kernel per receive order, and a routed instantiation of the tiled kernel
+// (A2AV_FLAG_ROUTE_FUSED: each warp routes its own tokens from the logits
+// and counts the ids it chose, 32 warps of 2 rounds per tile).
 #include "a2av_internal.cuh"
 #include "route_select.cuh"
 
