@@ -680,3 +680,32 @@ def test_route_splits_fallback_active_tokens_and_layouts():
         if nt is not None:  # tokens that take no part keep their idx/gate/out
             for s_ in range(w.R):
                 assert (a["idx"][s_, nt[s_]:] == -9).all() and (a["gate"][s_, nt[s_]:] == -1.0).all()
+
+
+# ---------------------------------------------------------------------------
+# seeded random shapes x options, element by element against the oracle
+# ---------------------------------------------------------------------------
+def _random_case(i):
+    rng = np.random.default_rng(1000 + i)
+    R = int(rng.choice([1, 2, 3, 4, 8, 16]))
+    epr = int(rng.choice([1, 2, 3, 8]))
+    E = R * epr
+    k = int(rng.integers(1, min(E, 8) + 1))
+    T = int(rng.choice([1, 2, 7, 64, 257, 300]))
+    H = int(rng.choice([8, 16, 72, 136, 520]))
+    routing = "zipf_distinct" if k > 1 else str(rng.choice(["uniform", "zipf"]))
+    w = W.Workload(f"fuzz{i}", R=R, E=E, T=T, H=H, k=k, routing=routing, zipf_s=float(rng.choice([0.0, 1.1])),
+                   gate="softmax" if k > 1 else "ones", expert=str(rng.choice(["identity", "scale"])),
+                   recv_order=str(rng.choice(["source", "expert"])))
+    if rng.random() < 0.3:
+        import dataclasses
+        w = dataclasses.replace(w, window_mode="fixed", window_rows=int(rng.integers(1, T * k * R + 2)))
+    nt = rng.integers(0, T + 1, size=R).astype(np.int32) if rng.random() < 0.4 else None
+    flags = int(rng.choice([0, 1, 2, 3, 4]))
+    return w, nt, flags
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_shapes_and_options(i):
+    w, nt, flags = _random_case(i)
+    P.full_parity(w, seed=i, num_tokens=nt, flags=flags)
