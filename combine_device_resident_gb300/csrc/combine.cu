@@ -1,9 +1,8 @@
 // Combine: the return trip of the MoE exchange.  For every token the k expert
 // outputs are gathered from the windows and summed with the gate weights:
 //   out[s][t] = bf16_rne( sum_{j=0..k-1, slot>=0} w[s][t][j] * y[slot_map[s][t][j]] )
-// accumulated in fp32 from 0 in slot order, with each product and each sum
-// rounded on its own (__fmul_rn / __fadd_rn: no FMA contraction), so the
-// result does not depend on the launch shape.  NCCLX pages: qiguanping deep
+// accumulated in fp32 from 0 in slot order, one fused multiply-add (one
+// rounding) per slot, so the result does not depend on the launch shape.  NCCLX pages: qiguanping deep
 // dive section 7, Figure 13 (the dispatch shuffle and the combine).
 //
 // Work unit = one of `nsplit` pieces of one token's row (nsplit is chosen so
@@ -34,25 +33,42 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return l | (h << 16);
 }
 
-__device__ __forceinline__ void accumulate2(float &a0, float &a1, uint32_t q, float w) {
-    a0 = __fadd_rn(a0, __fmul_rn(w, bf16lo(q)));
-    a1 = __fadd_rn(a1, __fmul_rn(w, bf16hi(q)));
+// Eight accumulators as four fp32 pairs in 64-bit registers, worked on by the
+// packed two-lane fp32 FMA of the sm_100 family: acc = fma(w, y, acc) per
+// lane, one rounding, in a quarter of the issue slots of a scalar multiply
+// and add.
+__device__ __forceinline__ uint64_t pair_w(float w) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(d) : "f"(w));
+    return d;
 }
 
-__device__ __forceinline__ void accumulate(float (&acc)[8], const uint4 &v, float w) {
-    accumulate2(acc[0], acc[1], v.x, w);
-    accumulate2(acc[2], acc[3], v.y, w);
-    accumulate2(acc[4], acc[5], v.z, w);
-    accumulate2(acc[6], acc[7], v.w, w);
+// acc = fma(w, (the two bf16 values of q, the low half-word first), acc)
+__device__ __forceinline__ void accumulate_pair(uint64_t &acc, uint64_t w2, uint32_t q) {
+    asm("{\n\t.reg .b32 lo, hi;\n\t.reg .b64 y;\n\t"
+        "shl.b32 lo, %2, 16;\n\tand.b32 hi, %2, 0xffff0000;\n\tmov.b64 y, {lo, hi};\n\t"
+        "fma.rn.f32x2 %0, %1, y, %0;\n\t}"
+        : "+l"(acc)
+        : "l"(w2), "r"(q));
 }
 
-__device__ __forceinline__ uint4 to_bf16x8(const float (&acc)[8]) {
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    return o;
+__device__ __forceinline__ void accumulate(uint64_t (&acc)[4], const uint4 &v, uint64_t w2) {
+    accumulate_pair(acc[0], w2, v.x);
+    accumulate_pair(acc[1], w2, v.y);
+    accumulate_pair(acc[2], w2, v.z);
+    accumulate_pair(acc[3], w2, v.w);
+}
+
+// round both lanes to bf16 (nearest-even), the low lane into the low half-word
+__device__ __forceinline__ uint32_t pair_to_bf16x2(uint64_t a) {
+    uint32_t d;
+    asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tcvt.rn.bf16x2.f32 %0, hi, lo;\n\t}" : "=r"(d) : "l"(a));
+    return d;
+}
+
+__device__ __forceinline__ uint4 to_bf16x8(const uint64_t (&acc)[4]) {
+    return make_uint4(pair_to_bf16x2(acc[0]), pair_to_bf16x2(acc[1]), pair_to_bf16x2(acc[2]),
+                      pair_to_bf16x2(acc[3]));
 }
 
 template <int KT, int U>
@@ -60,32 +76,35 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
     const Geometry &g = a.g;
     const int k = KT > 0 ? KT : g.k;
     const int lane = threadIdx.x & 31;
-    const long long ntok = (long long)g.R * g.T;
     const int nv = g.H >> 3;               // 16-byte vectors per row
     const int step = 32 * U;               // vectors per inner step
-    const int nsplit = a.nsplit;           // pieces per row (1 = whole-row units)
+    const uint32_t nsplit = (uint32_t)a.nsplit;  // pieces per row (1 = whole-row units)
     const int steps_per_row = (nv + step - 1) / step;
-    const int steps_per_unit = (steps_per_row + nsplit - 1) / nsplit;
-    const long long units = ntok * nsplit;
-    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
-    const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int steps_per_unit = (steps_per_row + (int)nsplit - 1) / (int)nsplit;
+    // 32-bit unit indices (a 64-bit divide is a subroutine call): units =
+    // R*T*nsplit < 2^31, since R*T*k < 2^31 and nsplit > 1 only when R*T is
+    // below four units per warp; unsigned, so that un + nw cannot overflow
+    const uint32_t units = (uint32_t)g.R * (uint32_t)g.T * nsplit;
+    const uint32_t T = (uint32_t)g.T;
+    const uint32_t nw = (gridDim.x * blockDim.x) >> 5;
+    const uint32_t gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const size_t rowb = (size_t)g.H * 2;
     const char *y = reinterpret_cast<const char *>(a.y);
     bool bad_slot = false;
     grid_dependency_wait();  // slot_map and y come from the kernels before
-    long long cur = -1;
+    uint32_t cur = 0xffffffffu;
     int32_t row = -1;
     float w = 0.f;
     bool active = true;
     // token-major grid stride: the warps active at one time cover a compact
     // stretch of `out` (and of each token's gathered rows)
-    for (long long un = gw; un < units; un += nw) {
-        const long long u = un / nsplit;
+    for (uint32_t un = gw; un < units; un += nw) {
+        const uint32_t u = un / nsplit;
         const int piece = (int)(un - u * nsplit);
         if (u != cur) {
             cur = u;
-            const int s_tok = (int)(u / g.T);
-            active = u - (long long)s_tok * g.T < active_tokens(a.num_tokens, s_tok, g.T);
+            const uint32_t s_tok = u / T;
+            active = (int)(u - s_tok * T) < active_tokens(a.num_tokens, (int)s_tok, g.T);
             row = -1;
             w = 0.f;
             if (lane < k) {
@@ -101,11 +120,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
         char *dst = reinterpret_cast<char *>(a.out) + (size_t)u * rowb;
         const int vb_end = min(nv, (piece + 1) * steps_per_unit * step);
         for (int vb = piece * steps_per_unit * step; vb < vb_end; vb += step) {
-        float acc[U][8];
+        uint64_t acc[U][4];  // fp32 pairs, +0.0 each
 #pragma unroll
         for (int q = 0; q < U; ++q)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[q][i] = 0.f;
+            for (int i = 0; i < 4; ++i) acc[q][i] = 0ull;
         if constexpr (KT > 0) {
             uint4 buf[KT][U];
             int32_t rows[KT];
@@ -122,9 +141,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
 #pragma unroll
             for (int j = 0; j < KT; ++j) {
                 const float wj = __shfl_sync(kFull, w, j);
+                const uint64_t wj2 = pair_w(wj);
                 if (rows[j] < 0) continue;
 #pragma unroll
-                for (int q = 0; q < U; ++q) accumulate(acc[q], buf[j][q], wj);
+                for (int q = 0; q < U; ++q) accumulate(acc[q], buf[j][q], wj2);
             }
         } else {
             for (int j = 0; j < k; ++j) {
@@ -139,7 +159,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
                     if (v < vb_end) buf[q] = ld_stream_v4(y + (size_t)rj * rowb + (size_t)v * 16);
                 }
 #pragma unroll
-                for (int q = 0; q < U; ++q) accumulate(acc[q], buf[q], wj);
+                for (int q = 0; q < U; ++q) accumulate(acc[q], buf[q], pair_w(wj));
             }
         }
 #pragma unroll
@@ -274,13 +294,11 @@ __global__ void __launch_bounds__(32, 1) combine_tma_kernel(const CombineArgs a)
         const unsigned char *stage = smem + (size_t)st * stage_bytes;
         char *dst = outp + (size_t)tok * rowb + off;
         for (int v = lane; v < nvec && !skip; v += 32) {
-            float acc[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // fp32 pairs, +0.0 each
             for (int j = 0; j < k; ++j) {
                 if (!((mask >> j) & 1u)) continue;
                 const uint4 val = *reinterpret_cast<const uint4 *>(stage + (size_t)j * CH + (size_t)v * 16);
-                accumulate(acc, val, meta[st].w[j]);
+                accumulate(acc, val, pair_w(meta[st].w[j]));
             }
             st_stream_v4(dst + (size_t)v * 16, to_bf16x8(acc));
         }
