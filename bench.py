@@ -24,6 +24,7 @@ import json
 import math
 import os
 import platform
+import re
 import statistics
 import subprocess
 import sys
@@ -124,13 +125,26 @@ KERNEL_SOURCES = {
 }
 
 
+_C_TOKENS = re.compile(r'"(?:\\.|[^"\\\n])*"|\'(?:\\.|[^\'\\\n])*\'|/\*.*?\*/|//[^\n]*', re.S)
+
+
+def _code_only(text: str) -> str:
+    """C/CUDA source with comments removed and whitespace runs collapsed
+    (string and character literals kept), so that a comment edit does not
+    count as a change of the kernel."""
+    t = _C_TOKENS.sub(lambda m: m.group(0) if m.group(0)[0] in "\"'" else " ", text)
+    return re.sub(r"\s+", " ", t).strip()
+
+
 def kernel_source_hash(kernel: str) -> str:
+    """Hash of the code a kernel is built from: its .cu file, the internal
+    header and the public header, comments and whitespace excluded."""
     h = hashlib.sha256()
     pkg = os.path.join(ROOT, "combine_device_resident_gb300")
     for rel in KERNEL_SOURCES[kernel] + ["csrc/a2av_internal.cuh"]:
         h.update(rel.encode())
-        h.update(open(os.path.join(pkg, rel), "rb").read())
-    h.update(open(os.path.join(ROOT, "include", "a2av.h"), "rb").read())
+        h.update(_code_only(open(os.path.join(pkg, rel)).read()).encode())
+    h.update(_code_only(open(os.path.join(ROOT, "include", "a2av.h")).read()).encode())
     return h.hexdigest()[:16]
 
 
