@@ -361,14 +361,12 @@ const CombineVariant kCombineVariants[] = {
 };
 
 // Measured on GB300: fewer loads per lane and more resident warps win
-// (k*U of 2 to 8 vectors in flight per lane) -- except for top-1 calls with
-// few tokens, where there are few units per warp and each unit should keep
-// more loads in flight (r8 T256 H5120: 26.6 vs 27.3 us per step with U=4;
-// r8 T1024: 52.6 vs 53.2 us with U=2), if a row has the 128 vectors a warp
-// step of U=4 covers (r2 T128 H256 was slower with it).
-int default_unroll(int k, long long tokens, int H) {
+// (k*U of 2 to 8 vectors in flight per lane).  With the packed fp32
+// arithmetic U=2 also wins for top-1 batches of few tokens (r8 T256 H5120:
+// 25.6 vs 26.0 us per step with U=4), where the scalar code had preferred U=4.
+int default_unroll(int k) {
     switch (k) {
-        case 1: return tokens <= 4096 && H / 8 >= 32 * 4 ? 4 : 2;
+        case 1: return 2;
         case 2: return 2;
         case 4: return 1;
         case 8: return 1;
@@ -377,9 +375,9 @@ int default_unroll(int k, long long tokens, int H) {
 }
 
 // Kernel for this plan's k and requested unroll (nearest instantiated one).
-const CombineVariant *pick_variant(int k, int want_u, long long tokens, int H) {
+const CombineVariant *pick_variant(int k, int want_u) {
     const int kk = (k == 1 || k == 2 || k == 4 || k == 8) ? k : 0;
-    const int u = want_u > 0 ? want_u : (kk ? default_unroll(kk, tokens, H) : 2);
+    const int u = want_u > 0 ? want_u : (kk ? default_unroll(kk) : 2);
     const CombineVariant *best = nullptr;
     for (const auto &v : kCombineVariants) {
         if (v.k != kk) continue;
@@ -452,7 +450,7 @@ cudaError_t configure_combine(a2av_plan_s &p) {
         return e;
     }
     p.combine_tma = 0;
-    e = occupancy_grid(p, pick_variant(p.g.k, p.cfg.combine_unroll, (long long)p.g.R * p.g.T, p.g.H));
+    e = occupancy_grid(p, pick_variant(p.g.k, p.cfg.combine_unroll));
     if (e != cudaSuccess) return e;
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, expert_scale_kernel, 256, 0);
@@ -471,8 +469,7 @@ cudaError_t launch_combine(const a2av_plan_s &p, const CombineArgs &a, cudaStrea
         return e != cudaSuccess ? e : cudaGetLastError();
     }
     b.nsplit = p.comb_nsplit;
-    e = launch_pdl(pick_variant(p.g.k, p.comb_unroll, (long long)p.g.R * p.g.T, p.g.H)->fn, p.combine.grid, 256, 0,
-                   s, b);
+    e = launch_pdl(pick_variant(p.g.k, p.comb_unroll)->fn, p.combine.grid, 256, 0, s, b);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -142,7 +142,7 @@ typedef struct {
     int32_t combine_ctas_per_sm;  /* TMA combine: resident CTAs per SM, 1..8 (0 = 4) */
     int32_t combine_stage_bytes;  /* TMA combine: bytes of the k row chunks per stage, multiple of 16 (0 = 16 KiB) */
     int32_t combine_unroll;       /* vector combine: 16-byte loads per lane and slot per step, 1..8
-                                     (0 = 2 for k <= 2, else 1; 4 for k = 1, R*T <= 4096, H >= 1024) */
+                                     (0 = 2 for k <= 2, else 1) */
     int32_t recv_order;           /* A2AV_ORDER_SOURCE (0) or A2AV_ORDER_EXPERT */
 } a2av_config_t;
 
