@@ -1,9 +1,10 @@
 // Combine: the return trip of the MoE exchange.  For every token the k expert
 // outputs are gathered from the windows and summed with the gate weights:
 //   out[s][t] = bf16_rne( sum_{j=0..k-1, slot>=0} w[s][t][j] * y[slot_map[s][t][j]] )
-// accumulated in fp32 from 0 in slot order, one fused multiply-add (one
-// rounding) per slot, so the result does not depend on the launch shape.  NCCLX pages: qiguanping deep
-// dive section 7, Figure 13 (the dispatch shuffle and the combine).
+// accumulated in fp32 from +0 in slot order, each product and each sum
+// rounded on its own, so the result does not depend on the launch shape.
+// NCCLX pages: qiguanping deep dive section 7, Figure 13 (the dispatch
+// shuffle and the combine).
 //
 // Work unit = one of `nsplit` pieces of one token's row (nsplit is chosen so
 // that there are several units per warp: whole rows for many tokens, pieces
@@ -27,48 +28,60 @@ constexpr uint32_t kFull = 0xffffffffu;
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// both values rounded to bf16 (nearest-even), lo into the low half-word: one
+// cvt.rn.bf16x2.f32, which rounds each lane as cvt.rn.bf16.f32 does
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-    const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-    return l | (h << 16);
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
 }
 
-// Eight accumulators as four fp32 pairs in 64-bit registers, worked on by the
-// packed two-lane fp32 FMA of the sm_100 family: acc = fma(w, y, acc) per
-// lane, one rounding, in a quarter of the issue slots of a scalar multiply
-// and add.
+// Eight fp32 accumulators.  The first slot that contributes goes through the
+// packed two-lane fp32 FMA of the sm_100 family with a +0 addend: fma(w, y,
+// +0) rounds only the product, and adding +0 is exact (it turns a -0 product
+// into +0), so this is bit for bit the separately rounded product added to
+// the +0 accumulator, one instruction per pair of values; slot 0 takes this
+// path when it has a row.  Every other slot (slot 0 included, when it has no
+// row and the accumulators stay +0) is a scalar __fmul_rn then __fadd_rn,
+// which is correct whatever the accumulators hold: a packed multiply followed by a
+// packed add is evaluated as one fused operation on this target (a device
+// probe over 4M random triples matched fmaf in every case), which would drop
+// the product's rounding.
 __device__ __forceinline__ uint64_t pair_w(float w) {
     uint64_t d;
     asm("mov.b64 %0, {%1, %1};" : "=l"(d) : "f"(w));
     return d;
 }
 
-// acc = fma(w, (the two bf16 values of q, the low half-word first), acc)
-__device__ __forceinline__ void accumulate_pair(uint64_t &acc, uint64_t w2, uint32_t q) {
-    asm("{\n\t.reg .b32 lo, hi;\n\t.reg .b64 y;\n\t"
-        "shl.b32 lo, %2, 16;\n\tand.b32 hi, %2, 0xffff0000;\n\tmov.b64 y, {lo, hi};\n\t"
-        "fma.rn.f32x2 %0, %1, y, %0;\n\t}"
-        : "+l"(acc)
-        : "l"(w2), "r"(q));
+// (lo, hi) = fma(w, (the two bf16 values of q, the low half-word first), +0)
+__device__ __forceinline__ void first_pair(float &lo, float &hi, uint64_t w2, uint32_t q) {
+    asm("{\n\t.reg .b32 l, h;\n\t.reg .b64 y, d;\n\t"
+        "shl.b32 l, %2, 16;\n\tand.b32 h, %2, 0xffff0000;\n\tmov.b64 y, {l, h};\n\t"
+        "fma.rn.f32x2 d, %3, y, %4;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(q), "l"(w2), "l"(0ull));
 }
 
-__device__ __forceinline__ void accumulate(uint64_t (&acc)[4], const uint4 &v, uint64_t w2) {
-    accumulate_pair(acc[0], w2, v.x);
-    accumulate_pair(acc[1], w2, v.y);
-    accumulate_pair(acc[2], w2, v.z);
-    accumulate_pair(acc[3], w2, v.w);
+// one slot's eight values into the accumulators; `first`: the accumulators
+// still hold +0 (then either path gives the same bits)
+__device__ __forceinline__ void accumulate(float (&acc)[8], const uint4 &v, float w, bool first) {
+    const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+    if (first) {
+        const uint64_t w2 = pair_w(w);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) first_pair(acc[2 * i], acc[2 * i + 1], w2, q[i]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(w, bf16lo(q[i])));
+            acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(w, bf16hi(q[i])));
+        }
+    }
 }
 
-// round both lanes to bf16 (nearest-even), the low lane into the low half-word
-__device__ __forceinline__ uint32_t pair_to_bf16x2(uint64_t a) {
-    uint32_t d;
-    asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tcvt.rn.bf16x2.f32 %0, hi, lo;\n\t}" : "=r"(d) : "l"(a));
-    return d;
-}
-
-__device__ __forceinline__ uint4 to_bf16x8(const uint64_t (&acc)[4]) {
-    return make_uint4(pair_to_bf16x2(acc[0]), pair_to_bf16x2(acc[1]), pair_to_bf16x2(acc[2]),
-                      pair_to_bf16x2(acc[3]));
+__device__ __forceinline__ uint4 to_bf16x8(const float (&acc)[8]) {
+    return make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                      pack_bf16x2(acc[6], acc[7]));
 }
 
 template <int KT, int U>
@@ -120,11 +133,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
         char *dst = reinterpret_cast<char *>(a.out) + (size_t)u * rowb;
         const int vb_end = min(nv, (piece + 1) * steps_per_unit * step);
         for (int vb = piece * steps_per_unit * step; vb < vb_end; vb += step) {
-        uint64_t acc[U][4];  // fp32 pairs, +0.0 each
+        float acc[U][8];
 #pragma unroll
         for (int q = 0; q < U; ++q)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[q][i] = 0ull;
+            for (int i = 0; i < 8; ++i) acc[q][i] = 0.f;
         if constexpr (KT > 0) {
             uint4 buf[KT][U];
             int32_t rows[KT];
@@ -141,10 +154,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
 #pragma unroll
             for (int j = 0; j < KT; ++j) {
                 const float wj = __shfl_sync(kFull, w, j);
-                const uint64_t wj2 = pair_w(wj);
-                if (rows[j] < 0) continue;
+                if (rows[j] < 0) continue;  // warp-uniform: rows[] are the same in every lane
 #pragma unroll
-                for (int q = 0; q < U; ++q) accumulate(acc[q], buf[j][q], wj2);
+                for (int q = 0; q < U; ++q) accumulate(acc[q], buf[j][q], wj, j == 0);
             }
         } else {
             for (int j = 0; j < k; ++j) {
@@ -159,7 +171,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
                     if (v < vb_end) buf[q] = ld_stream_v4(y + (size_t)rj * rowb + (size_t)v * 16);
                 }
 #pragma unroll
-                for (int q = 0; q < U; ++q) accumulate(acc[q], buf[q], pair_w(wj));
+                for (int q = 0; q < U; ++q) accumulate(acc[q], buf[q], wj, j == 0);
             }
         }
 #pragma unroll
@@ -294,11 +306,13 @@ __global__ void __launch_bounds__(32, 1) combine_tma_kernel(const CombineArgs a)
         const unsigned char *stage = smem + (size_t)st * stage_bytes;
         char *dst = outp + (size_t)tok * rowb + off;
         for (int v = lane; v < nvec && !skip; v += 32) {
-            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // fp32 pairs, +0.0 each
+            float acc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = 0.f;
             for (int j = 0; j < k; ++j) {
                 if (!((mask >> j) & 1u)) continue;
                 const uint4 val = *reinterpret_cast<const uint4 *>(stage + (size_t)j * CH + (size_t)v * 16);
-                accumulate(acc, val, pair_w(meta[st].w[j]));
+                accumulate(acc, val, meta[st].w[j], j == 0);
             }
             st_stream_v4(dst + (size_t)v * 16, to_bf16x8(acc));
         }

@@ -27,7 +27,7 @@
  *     local expert reads after the exchange (Inference section, Figure 13:
  *     the received tokens go on to their experts), the counts unchanged;
  *   - combine: out = bf16_rne(sum_j w_j * y[slot(t,j)]) accumulated in fp32
- *     from 0 in slot order, one fused multiply-add (one rounding) per slot.
+ *     from 0 in slot order, product and sum each rounded on its own.
  *
  * Conventions for every call below.
  *   - Every tensor pointer is a DEVICE pointer into memory of the plan's
@@ -206,7 +206,7 @@ a2av_status_t a2av_pack(a2av_plan_t plan, const void *x, const int32_t *topk_idx
 
 /* Combine (one kernel): out[s][t] = bf16_rne(sum_{j=0..k-1, slot>=0}
  * gate_w[s][t][j] * y[slot_map[s][t][j]]), fp32 accumulation from 0 in slot
- * order, one fused multiply-add per slot.  y has the recv layout
+ * order with separately rounded products and sums.  y has the recv layout
  * (the expert outputs written in place of, or beside, the received rows).
  * out must not overlap y.  [Deep dive section 7, Figure 13: the token
  * shuffle is followed by the combine.] */

@@ -4,9 +4,8 @@ TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline / reference arm may import this package.  The product
 path (``combine_device_resident_gb300``) never imports it and shares no code
 with it: the arithmetic lives in ``a2av_oracle.c`` (plain C, one thread, built
-with ``-O2 -ffp-contract=off`` so every fp32 step is rounded on its own, the
-combine's fused multiply-adds being explicit ``fmaf`` calls), and this module
-only marshals numpy arrays into it.
+with ``-O2 -ffp-contract=off`` so every fp32 product and sum is rounded on its
+own), and this module only marshals numpy arrays into it.
 
 What each function computes, and the passages and readings it follows, is
 written in ``a2av_oracle.c``.  Pinning status (what checks each function against

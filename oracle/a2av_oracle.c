@@ -36,10 +36,8 @@
  *       destination) pair gets T*k rows, so window d starts at d*R*T*k and
  *       source s's segment inside it at s*T*k;
  *   R5  combine: out = bf16_rne( sum_j w_j * y[slot(t,j)] ), accumulated in
- *       fp32 from 0.0f in slot order j = 0..k-1 as fused multiply-adds,
- *       acc = fmaf(w_j, y_j, acc): one rounding per slot (C's fmaf is
- *       correctly rounded; every other fp32 step in this file is rounded on
- *       its own, so it is built with -ffp-contract=off);
+ *       fp32 from 0.0f in slot order j = 0..k-1, each product and each sum
+ *       rounded on its own (this file must be built with -ffp-contract=off);
  *   R7  variable batches: when a per-rank count num_tokens[s] is given, only
  *       tokens t < num_tokens[s] of rank s take part (the others are not
  *       counted, get slot -1 and no combine output) -- the counts change from
@@ -500,7 +498,8 @@ void oracle_combine(int H, int k, const uint16_t *y, const float *gate, const in
             for (int j = 0; j < k; ++j) {
                 if (slots[j] < 0)
                     continue;
-                acc = fmaf(w[j], oracle_bf16_to_f32(y[(size_t)slots[j] * H + h]), acc);
+                float prod = w[j] * oracle_bf16_to_f32(y[(size_t)slots[j] * H + h]);
+                acc = acc + prod;
             }
             o[h] = oracle_f32_to_bf16(acc);
         }

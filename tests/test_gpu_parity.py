@@ -61,30 +61,31 @@ def test_combine_is_bit_exact_against_oracle(flags):
 @pytest.mark.parametrize("k,variant", [(2, {}), (2, dict(combine_unroll=1)), (2, dict(combine_unroll=4)),
                                        (2, dict(flags=4)), (3, {}), (3, dict(flags=4))],
                          ids=["k2", "k2-u1", "k2-u4", "k2-tma", "k3-generic", "k3-tma"])
-def test_combine_fuses_each_slot_hand_case(k, variant):
-    # The oracle pin's slot pair whose fused and separately rounded readings
+def test_combine_rounds_product_and_sum_hand_case(k, variant):
+    # The oracle pin's slot pair whose separately rounded and fused readings
     # differ in the output bf16, through the C ABI: every column of every
-    # token must come out as the fused reading (k = 3: a third, empty slot).
+    # token must come out as the separately rounded reading (k = 3: a third,
+    # empty slot).
     import torch
     from combine_device_resident_gb300 import Plan
-    from tests.test_oracle_pins import FMA_CASE_FUSED, FMA_CASE_W, FMA_CASE_Y
+    from tests.test_oracle_pins import SLOT_PAIR_SEPARATE, SLOT_PAIR_W, SLOT_PAIR_Y
 
     R, E, T, H = 2, 4, 40, 264
     dev = P.device()
     plan = Plan(R, E, T, H, k, device=dev, **variant)
     recv, slot_map, out = plan.new_buffers()
     rows = recv.view(torch.int16)
-    rows[0].fill_(int(FMA_CASE_Y[0].view(np.int16)))
-    rows[1].fill_(int(FMA_CASE_Y[1].view(np.int16)))
+    rows[0].fill_(int(SLOT_PAIR_Y[0].view(np.int16)))
+    rows[1].fill_(int(SLOT_PAIR_Y[1].view(np.int16)))
     sm = np.full((R, T, k), -1, np.int32)
     sm[..., 0], sm[..., 1] = 0, 1
     gate = np.zeros((R, T, k), np.float32)
-    gate[..., :2] = FMA_CASE_W
+    gate[..., :2] = SLOT_PAIR_W
     slot_map.copy_(torch.from_numpy(sm))
     plan.combine(recv, torch.from_numpy(gate).to(dev), slot_map, out)
     torch.cuda.synchronize()
     got = P.bits(out)
-    assert (got == FMA_CASE_FUSED).all(), np.unique(got)
+    assert (got == SLOT_PAIR_SEPARATE).all(), np.unique(got)
     assert plan.read_status() == 0
 
 

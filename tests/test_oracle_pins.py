@@ -511,25 +511,6 @@ def test_identity_softmax_weights_close_to_gate_sum_times_x():
     assert d.max() <= 1
 
 
-def fma_f32(w, y, acc):
-    """Elementwise fp32 fused multiply-add: the exact w*y + acc rounded once to
-    fp32 (nearest-even), from float64 arithmetic.  w*y is exact in float64 (two
-    24-bit significands); s = p + acc is rounded, and the error term e of the
-    error-free two-sum makes s + e exact.  s rounds to the right fp32 value
-    unless it lies exactly halfway between two fp32 values: there the sign of
-    e says on which side the exact sum lies."""
-    p = np.asarray(w, np.float32).astype(np.float64) * np.asarray(y, np.float32).astype(np.float64)
-    a = np.asarray(acc, np.float32).astype(np.float64)
-    s = p + a
-    bp = s - a
-    e = (p - bp) + (a - (s - bp))
-    r = s.astype(np.float32)
-    other = np.where(s > r, np.nextafter(r, np.float32(np.inf)), np.nextafter(r, np.float32(-np.inf)))
-    mid = (r.astype(np.float64) + other.astype(np.float64)) / 2
-    tie = (s != r) & (s == mid) & (e != 0)
-    return np.where(tie & ((e > 0) == (other > r)), other, r).astype(np.float32)
-
-
 def _f32_nearest_even(q):
     """fp32 nearest (ties to even) to an exact rational q in fp32's normal range."""
     from fractions import Fraction
@@ -548,58 +529,40 @@ def _f32_nearest_even(q):
     return np.float32(sign * n * 2.0 ** (e - 23))
 
 
-# A hand-made slot pair whose two readings of the fp32 accumulation differ in
-# the output bf16.  Slot 0: w0 = 2 - 3*2^-8 + 2^-21, y0 = -1, so acc = -w0
-# exactly.  Slot 1: w1 = 1 + 2^-23, y1 = 3, exact product 3 + 3*2^-23, which
-# rounds (a tie, to even) to 3 + 2^-21.  Fused: 3 + 3*2^-23 - w0 =
-# 1 + 3*2^-8 - 2^-23 exactly, below the bf16 midpoint 1 + 3*2^-8, so bf16
-# 1 + 2^-7 = 0x3F81.  Separately rounded: 3 + 2^-21 - w0 = 1 + 3*2^-8 exactly,
-# the midpoint, which rounds to the even 1 + 2^-6 = 0x3F82.
-FMA_CASE_W = np.array([2.0 - 3 * 2.0 ** -8 + 2.0 ** -21, 1.0 + 2.0 ** -23], np.float32)
-FMA_CASE_Y = np.array([0xBF80, 0x4040], np.uint16)  # bf16 -1, 3
-FMA_CASE_FUSED, FMA_CASE_SEPARATE = 0x3F81, 0x3F82
+# A hand-made slot pair on which a separately rounded product and sum and a
+# fused multiply-add give different output bf16.  Slot 0: w0 = 2 - 3*2^-8 +
+# 2^-21, y0 = -1, so acc = -w0 exactly.  Slot 1: w1 = 1 + 2^-23, y1 = 3, exact
+# product 3 + 3*2^-23, which rounds (a tie, to even) to 3 + 2^-21.
+# Separately rounded: 3 + 2^-21 - w0 = 1 + 3*2^-8 exactly, the bf16 midpoint
+# between 1 + 2^-7 and 1 + 2^-6, which rounds to the even 1 + 2^-6 = 0x3F82.
+# Fused: 3 + 3*2^-23 - w0 = 1 + 3*2^-8 - 2^-23, below the midpoint, so
+# 1 + 2^-7 = 0x3F81.
+SLOT_PAIR_W = np.array([2.0 - 3 * 2.0 ** -8 + 2.0 ** -21, 1.0 + 2.0 ** -23], np.float32)
+SLOT_PAIR_Y = np.array([0xBF80, 0x4040], np.uint16)  # bf16 -1, 3
+SLOT_PAIR_SEPARATE, SLOT_PAIR_FUSED = 0x3F82, 0x3F81
 
 
-def test_fma_f32_helper_matches_exact_rationals():
-    from fractions import Fraction
-
-    rng = np.random.default_rng(5)
-    n = 3000
-    w = (rng.standard_normal(n) * np.exp2(rng.integers(-12, 12, n))).astype(np.float32)
-    y = bits_to_f32(rng.integers(0, 1 << 16, n).astype(np.uint16) & 0x3FFF | 0x3000)  # finite bf16
-    y = np.where(rng.random(n) < 0.5, -y, y).astype(np.float32)
-    acc = (rng.standard_normal(n) * np.exp2(rng.integers(-12, 12, n))).astype(np.float32)
-    acc[: n // 3] = -(w[: n // 3].astype(np.float64) * y[: n // 3]).astype(np.float32)  # cancellation
-    w = np.concatenate([w, FMA_CASE_W[1:]])
-    y = np.concatenate([y, np.float32([3.0])])
-    acc = np.concatenate([acc, -FMA_CASE_W[:1]])
-    want = np.array([_f32_nearest_even(Fraction(float(a)) * Fraction(float(b)) + Fraction(float(c)))
-                     for a, b, c in zip(w, y, acc)], np.float32)
-    np.testing.assert_array_equal(fma_f32(w, y, acc).view(np.uint32), want.view(np.uint32))
-
-
-def test_combine_fuses_each_slot_hand_case():
+def test_combine_rounds_product_and_sum_hand_case():
     from fractions import Fraction
 
     # the two readings, in exact rationals, do differ on this case ...
-    w0, w1 = (Fraction(float(v)) for v in FMA_CASE_W)
-    y0, y1 = Fraction(-1), Fraction(3)
-    acc = _f32_nearest_even(w0 * y0)
-    fused = _f32_nearest_even(w1 * y1 + Fraction(float(acc)))
-    sep = _f32_nearest_even(Fraction(float(_f32_nearest_even(w1 * y1))) + Fraction(float(acc)))
-    assert int(f32_to_bits_torch(np.float32([fused]))[0]) == FMA_CASE_FUSED
-    assert int(f32_to_bits_torch(np.float32([sep]))[0]) == FMA_CASE_SEPARATE
-    # ... and the oracle takes the fused one, in every column
+    w0, w1 = (Fraction(float(v)) for v in SLOT_PAIR_W)
+    acc = _f32_nearest_even(w0 * -1)
+    sep = _f32_nearest_even(Fraction(float(_f32_nearest_even(w1 * 3))) + Fraction(float(acc)))
+    fused = _f32_nearest_even(w1 * 3 + Fraction(float(acc)))
+    assert int(f32_to_bits_torch(np.float32([sep]))[0]) == SLOT_PAIR_SEPARATE
+    assert int(f32_to_bits_torch(np.float32([fused]))[0]) == SLOT_PAIR_FUSED
+    # ... and the oracle rounds the product and then the sum, in every column
     H = 16
-    y = np.repeat(FMA_CASE_Y[:, None], H, axis=1)
-    out = oracle.combine(y, FMA_CASE_W.reshape(1, 1, 2), np.array([[[0, 1]]], np.int32))
-    assert (out == FMA_CASE_FUSED).all(), out
+    y = np.repeat(SLOT_PAIR_Y[:, None], H, axis=1)
+    out = oracle.combine(y, SLOT_PAIR_W.reshape(1, 1, 2), np.array([[[0, 1]]], np.int32))
+    assert (out == SLOT_PAIR_SEPARATE).all(), out
 
 
 def test_scaled_experts_closed_form_numpy_f32():
     # out = bf16( sum_j w_j * bf16(x * (1 + e_j/E)) ), accumulated in fp32 in j order
-    # from 0, one fused multiply-add per slot -- computed straight from
-    # (x, idx, w) with numpy and no dispatch at all.
+    # from 0, products and sums rounded separately -- computed straight from
+    # (x, idx, w) with numpy float32 and no dispatch at all.
     w, x, idx, gate = _small(4, 64, 40)
     res = oracle.run_all(w.R, w.E, x, idx, gate, expert="scale")
     xf = bits_to_f32(x)
@@ -607,7 +570,7 @@ def test_scaled_experts_closed_form_numpy_f32():
     for j in range(w.k):
         scale = (np.float32(1.0) + idx[..., j].astype(np.float32) / np.float32(w.E)).astype(np.float32)
         yj = bits_to_f32(f32_to_bits_torch(xf * scale[..., None]))
-        acc = fma_f32(np.broadcast_to(gate[..., j][..., None], yj.shape), yj, acc)
+        acc = (acc + (gate[..., j][..., None] * yj).astype(np.float32)).astype(np.float32)
     np.testing.assert_array_equal(res["out"], f32_to_bits_torch(acc))
 
 
@@ -672,9 +635,9 @@ MUTANTS = {
                                "            run += cnt[e];\n            send_offsets[(size_t)s * E + e] = run;"),
     "unstable sort": ("    for (int t = 0; t < T; ++t)\n        for (int j = 0; j < k; ++j) {\n            int32_t e = idx_s[(size_t)t * k + j];\n            if (t >= Ts) {",
                       "    for (int t = T - 1; t >= 0; --t)\n        for (int j = 0; j < k; ++j) {\n            int32_t e = idx_s[(size_t)t * k + j];\n            if (t >= Ts) {"),
-    "dropped gate weight": ("acc = fmaf(w[j], oracle_bf16_to_f32(", "acc = fmaf(1.0f, oracle_bf16_to_f32("),
-    "separately rounded product and sum": ("acc = fmaf(w[j], oracle_bf16_to_f32(y[(size_t)slots[j] * H + h]), acc);",
-                                           "acc = acc + w[j] * oracle_bf16_to_f32(y[(size_t)slots[j] * H + h]);"),
+    "dropped gate weight": ("float prod = w[j] * oracle_bf16_to_f32(", "float prod = 1.0f * oracle_bf16_to_f32("),
+    "fused multiply-add": ("float prod = w[j] * oracle_bf16_to_f32(y[(size_t)slots[j] * H + h]);\n                acc = acc + prod;",
+                           "acc = fmaf(w[j], oracle_bf16_to_f32(y[(size_t)slots[j] * H + h]), acc);"),
     "truncating bf16 rounding": ("u += 0x7fffu + keep_lsb;", "u += 0u * keep_lsb;"),
     "window base off by one window": ("            window_base[d] = (int32_t)base;\n        base += recv_total[d];",
                                       "        base += recv_total[d];\n            window_base[d] = (int32_t)base;"),
@@ -696,7 +659,7 @@ def _pin_suite():
     test_identity_unit_weights_give_k_times_x(2)
     test_identity_softmax_weights_close_to_gate_sum_times_x()
     test_scaled_experts_closed_form_numpy_f32()
-    test_combine_fuses_each_slot_hand_case()
+    test_combine_rounds_product_and_sum_hand_case()
     test_expert_scale_closed_form_torch()
     test_bf16_rounding_matches_torch()
     test_padded_layout_against_brute()
