@@ -58,14 +58,17 @@ def test_combine_is_bit_exact_against_oracle(flags):
         np.testing.assert_array_equal(g["out"], g["ref"]["out"])
 
 
-@pytest.mark.parametrize("k,variant", [(2, {}), (2, dict(combine_unroll=1)), (2, dict(combine_unroll=4)),
-                                       (2, dict(flags=4)), (3, {}), (3, dict(flags=4))],
-                         ids=["k2", "k2-u1", "k2-u4", "k2-tma", "k3-generic", "k3-tma"])
-def test_combine_rounds_product_and_sum_hand_case(k, variant):
+@pytest.mark.parametrize("k,first,variant", [(2, 0, {}), (2, 0, dict(combine_unroll=1)), (2, 0, dict(combine_unroll=4)),
+                                             (2, 0, dict(flags=4)), (3, 0, {}), (3, 0, dict(flags=4)),
+                                             (3, 1, {}), (3, 1, dict(flags=4)), (4, 2, {}), (4, 2, dict(combine_unroll=2))],
+                         ids=["k2", "k2-u1", "k2-u4", "k2-tma", "k3-generic", "k3-tma", "k3-slot0-empty",
+                              "k3-slot0-empty-tma", "k4-slots01-empty", "k4-slots01-empty-u2"])
+def test_combine_rounds_product_and_sum_hand_case(k, first, variant):
     # The oracle pin's slot pair whose separately rounded and fused readings
-    # differ in the output bf16, through the C ABI: every column of every
-    # token must come out as the separately rounded reading (k = 3: a third,
-    # empty slot).
+    # differ in the output bf16, through the C ABI, in slots first and
+    # first + 1 (the other slots empty): every column of every token must come
+    # out as the separately rounded reading.  With first > 0 the pair's first
+    # value is not in slot 0, so it is accumulated on the scalar path from +0.
     import torch
     from combine_device_resident_gb300 import Plan
     from tests.test_oracle_pins import SLOT_PAIR_SEPARATE, SLOT_PAIR_W, SLOT_PAIR_Y
@@ -78,9 +81,9 @@ def test_combine_rounds_product_and_sum_hand_case(k, variant):
     rows[0].fill_(int(SLOT_PAIR_Y[0].view(np.int16)))
     rows[1].fill_(int(SLOT_PAIR_Y[1].view(np.int16)))
     sm = np.full((R, T, k), -1, np.int32)
-    sm[..., 0], sm[..., 1] = 0, 1
-    gate = np.zeros((R, T, k), np.float32)
-    gate[..., :2] = SLOT_PAIR_W
+    sm[..., first], sm[..., first + 1] = 0, 1
+    gate = np.full((R, T, k), np.float32(np.inf))  # empty slots: a weight used anyway would give inf or NaN
+    gate[..., first:first + 2] = SLOT_PAIR_W
     slot_map.copy_(torch.from_numpy(sm))
     plan.combine(recv, torch.from_numpy(gate).to(dev), slot_map, out)
     torch.cuda.synchronize()
