@@ -546,6 +546,9 @@ def main():
     traffic = None if (padded or t_active != w.T or w.recv_order != "source") else ncu_traffic(dom, w.name)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
+                # the DRAM side of the same launch: measured DRAM bytes over the same
+                # duration (below frac when rows are served by or left in L2)
+                "traffic_frac": (round(traffic / (kus[dom] * 1e-6) / 1e9 / peak, 4) if traffic else None),
                 "kernel_us": {n: round(v, 3) for n, v in kus.items()},
                 "kernel_gbs": {n: round(kbytes[n] / (kus[n] * 1e-6) / 1e9, 1) for n in kus},
                 "timing": (f"marginal: nested graphs of the first 1..{len(stages)} kernels, "
