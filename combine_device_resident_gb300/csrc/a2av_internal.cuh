@@ -75,6 +75,7 @@ struct PackArgs {
     int32_t rows_final;   // 1: slot_map already holds final rows (single-CTA splits)
     int32_t lag;          // store groups allowed to read a stage before it is refilled
     int64_t padded_tk;    // padded plans: T*k, and `recv` is the padded send buffer
+    int32_t trigger_early;  // 1: let the dependent grid launch at once (few tokens: latency-bound call)
 };
 
 struct RouteArgs {
@@ -146,6 +147,8 @@ struct a2av_plan_s {
     const int32_t *num_tokens = nullptr;  // a2av_set_active_tokens
     int combine_tma = 1;
     int32_t comb_chunk_bytes = 0, comb_nchunks = 0, comb_stages = 0, comb_nsplit = 1, comb_unroll = 2;
+    bool comb_batch = false;  // combine_batched_kernel (set with few_tokens where rows split into pieces)
+    bool few_tokens = false;  // R*T below the combine's warps: the pack triggers the combine's launch early
     int pack_tma = 1;
     int32_t pack_chunk_bytes = 0, pack_nchunks = 0, pack_stages = 0, pack_lag = 1;
     int64_t launches = 0;

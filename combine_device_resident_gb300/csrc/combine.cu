@@ -84,6 +84,60 @@ __device__ __forceinline__ uint4 to_bf16x8(const float (&acc)[8]) {
                       pack_bf16x2(acc[6], acc[7]));
 }
 
+// One step of a unit: vectors [vb, min(vb + 32*U, vb_end)) of one token's
+// row, gathered from its k slots, accumulated in slot order and stored to
+// dst.  Lane m0 + j holds slot j's arena row (-1: no row) and gate weight.
+template <int KT, int U>
+__device__ __forceinline__ void combine_step(int k, int lane, const char *y, size_t rowb, int32_t row, float w,
+                                             int m0, int vb, int vb_end, char *dst) {
+    float acc[U][8];
+#pragma unroll
+    for (int q = 0; q < U; ++q)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[q][i] = 0.f;
+    if constexpr (KT > 0) {
+        uint4 buf[KT][U];
+        int32_t rows[KT];
+#pragma unroll
+        for (int j = 0; j < KT; ++j) {
+            rows[j] = __shfl_sync(kFull, row, m0 + j);
+#pragma unroll
+            for (int q = 0; q < U; ++q) {
+                const int v = vb + q * 32 + lane;
+                buf[j][q] = make_uint4(0u, 0u, 0u, 0u);
+                if (rows[j] >= 0 && v < vb_end) buf[j][q] = ld_stream_v4(y + (size_t)rows[j] * rowb + (size_t)v * 16);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < KT; ++j) {
+            const float wj = __shfl_sync(kFull, w, m0 + j);
+            if (rows[j] < 0) continue;  // warp-uniform: rows[] are the same in every lane
+#pragma unroll
+            for (int q = 0; q < U; ++q) accumulate(acc[q], buf[j][q], wj, j == 0);
+        }
+    } else {
+        for (int j = 0; j < k; ++j) {
+            const int32_t rj = __shfl_sync(kFull, row, m0 + j);
+            const float wj = __shfl_sync(kFull, w, m0 + j);
+            if (rj < 0) continue;
+            uint4 buf[U];
+#pragma unroll
+            for (int q = 0; q < U; ++q) {
+                const int v = vb + q * 32 + lane;
+                buf[q] = make_uint4(0u, 0u, 0u, 0u);
+                if (v < vb_end) buf[q] = ld_stream_v4(y + (size_t)rj * rowb + (size_t)v * 16);
+            }
+#pragma unroll
+            for (int q = 0; q < U; ++q) accumulate(acc[q], buf[q], wj, j == 0);
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < U; ++q) {
+        const int v = vb + q * 32 + lane;
+        if (v < vb_end) st_stream_v4(dst + (size_t)v * 16, to_bf16x8(acc[q]));
+    }
+}
+
 template <int KT, int U>
 __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
     const Geometry &g = a.g;
@@ -132,53 +186,67 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
         if (!active) continue;  // warp-uniform: the token takes no part, its out row is left alone
         char *dst = reinterpret_cast<char *>(a.out) + (size_t)u * rowb;
         const int vb_end = min(nv, (piece + 1) * steps_per_unit * step);
-        for (int vb = piece * steps_per_unit * step; vb < vb_end; vb += step) {
-        float acc[U][8];
-#pragma unroll
-        for (int q = 0; q < U; ++q)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[q][i] = 0.f;
-        if constexpr (KT > 0) {
-            uint4 buf[KT][U];
-            int32_t rows[KT];
-#pragma unroll
-            for (int j = 0; j < KT; ++j) {
-                rows[j] = __shfl_sync(kFull, row, j);
-#pragma unroll
-                for (int q = 0; q < U; ++q) {
-                    const int v = vb + q * 32 + lane;
-                    buf[j][q] = make_uint4(0u, 0u, 0u, 0u);
-                    if (rows[j] >= 0 && v < vb_end) buf[j][q] = ld_stream_v4(y + (size_t)rows[j] * rowb + (size_t)v * 16);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < KT; ++j) {
-                const float wj = __shfl_sync(kFull, w, j);
-                if (rows[j] < 0) continue;  // warp-uniform: rows[] are the same in every lane
-#pragma unroll
-                for (int q = 0; q < U; ++q) accumulate(acc[q], buf[j][q], wj, j == 0);
-            }
-        } else {
-            for (int j = 0; j < k; ++j) {
-                const int32_t rj = __shfl_sync(kFull, row, j);
-                const float wj = __shfl_sync(kFull, w, j);
-                if (rj < 0) continue;
-                uint4 buf[U];
-#pragma unroll
-                for (int q = 0; q < U; ++q) {
-                    const int v = vb + q * 32 + lane;
-                    buf[q] = make_uint4(0u, 0u, 0u, 0u);
-                    if (v < vb_end) buf[q] = ld_stream_v4(y + (size_t)rj * rowb + (size_t)v * 16);
-                }
-#pragma unroll
-                for (int q = 0; q < U; ++q) accumulate(acc[q], buf[q], wj, j == 0);
+        for (int vb = piece * steps_per_unit * step; vb < vb_end; vb += step)
+            combine_step<KT, U>(k, lane, y, rowb, row, w, 0, vb, vb_end, dst);
+    }
+    if (__any_sync(kFull, bad_slot) && lane == 0) atomicOr(a.status, kDevBadSlot);
+}
+
+// The same combine for calls with fewer tokens than warps, where every row is
+// split into pieces and each warp has a few one-step units whose time is
+// memory round trips: the slot rows and gate weights of the warp's next
+// M = 32/k units come in with one warp-wide load (lane l: slot l % k of unit
+// l / k) before any of their gathers, so each unit waits on one round trip
+// instead of two (r8 E128 T256 H5120 top-1: 24.6 against 26.2 us per step).
+// With whole-row units the plain kernel above is faster.
+template <int KT, int U>
+__global__ void __launch_bounds__(256) combine_batched_kernel(const CombineArgs a) {
+    const Geometry &g = a.g;
+    const int k = KT > 0 ? KT : g.k;
+    const int lane = threadIdx.x & 31;
+    const int nv = g.H >> 3;
+    const int step = 32 * U;
+    const uint32_t nsplit = (uint32_t)a.nsplit;
+    const int steps_per_row = (nv + step - 1) / step;
+    const int steps_per_unit = (steps_per_row + (int)nsplit - 1) / (int)nsplit;
+    const uint32_t units = (uint32_t)g.R * (uint32_t)g.T * nsplit;  // < 2^31, as in combine_kernel
+    const uint32_t T = (uint32_t)g.T;
+    const uint32_t nw = (gridDim.x * blockDim.x) >> 5;
+    const uint32_t gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const size_t rowb = (size_t)g.H * 2;
+    const char *y = reinterpret_cast<const char *>(a.y);
+    const int M = 32 / k;
+    const int mi = lane / k, mj = lane - mi * k;
+    bool bad_slot = false;
+    grid_dependency_wait();
+    // the warp's units are gw, gw + nw, ... (token-major, as in combine_kernel);
+    // base + nw*M stays below 2^32 since units < 2^31 and nw*M <= 2048 per SM
+    for (uint32_t base = gw; base < units; base += nw * (uint32_t)M) {
+        int32_t mrow = -1;
+        float mw = 0.f;
+        int mact = 0;
+        if (mi < M && base + (uint32_t)mi * nw < units) {
+            const uint32_t u = (base + (uint32_t)mi * nw) / nsplit;
+            const uint32_t s_tok = u / T;
+            mact = (int)(u - s_tok * T) < active_tokens(a.num_tokens, (int)s_tok, g.T);
+            mrow = __ldg(a.slot_map + (size_t)u * k + mj);
+            mw = __ldg(a.gate + (size_t)u * k + mj);
+            if (mrow >= a.arena_rows) {
+                bad_slot = true;
+                mrow = -1;
             }
         }
-#pragma unroll
-        for (int q = 0; q < U; ++q) {
-            const int v = vb + q * 32 + lane;
-            if (v < vb_end) st_stream_v4(dst + (size_t)v * 16, to_bf16x8(acc[q]));
-        }
+#pragma unroll 1
+        for (int bi = 0; bi < M; ++bi) {
+            const uint32_t un = base + (uint32_t)bi * nw;
+            if (un >= units) break;                   // warp-uniform
+            if (!__shfl_sync(kFull, mact, bi * k)) continue;  // warp-uniform: out row left alone
+            const uint32_t u = un / nsplit;
+            const int piece = (int)(un - u * nsplit);
+            char *dst = reinterpret_cast<char *>(a.out) + (size_t)u * rowb;
+            const int vb_end = min(nv, (piece + 1) * steps_per_unit * step);
+            for (int vb = piece * steps_per_unit * step; vb < vb_end; vb += step)
+                combine_step<KT, U>(k, lane, y, rowb, mrow, mw, bi * k, vb, vb_end, dst);
         }
     }
     if (__any_sync(kFull, bad_slot) && lane == 0) atomicOr(a.status, kDevBadSlot);
@@ -361,26 +429,32 @@ __global__ void __launch_bounds__(256) expert_scale_kernel(const ScaleArgs a) {
 
 using CombineKernel = void (*)(const CombineArgs);
 
-// The instantiated (k, U) pairs; U = 16-byte vectors per lane and step.
+// The instantiated (k, U, batch) triples; U = 16-byte vectors per lane and
+// step, batch = combine_batched_kernel (top-1 and top-2 only).
 struct CombineVariant {
     int k, u;
+    bool batch;
     CombineKernel fn;
 };
 const CombineVariant kCombineVariants[] = {
-    {1, 2, combine_kernel<1, 2>}, {1, 4, combine_kernel<1, 4>}, {1, 8, combine_kernel<1, 8>},
-    {2, 1, combine_kernel<2, 1>}, {2, 2, combine_kernel<2, 2>}, {2, 4, combine_kernel<2, 4>},
-    {4, 1, combine_kernel<4, 1>}, {4, 2, combine_kernel<4, 2>},
-    {8, 1, combine_kernel<8, 1>}, {8, 2, combine_kernel<8, 2>},
-    {0, 1, combine_kernel<0, 1>}, {0, 2, combine_kernel<0, 2>},
+    {1, 2, false, combine_kernel<1, 2>}, {1, 4, false, combine_kernel<1, 4>}, {1, 8, false, combine_kernel<1, 8>},
+    {2, 1, false, combine_kernel<2, 1>}, {2, 2, false, combine_kernel<2, 2>}, {2, 4, false, combine_kernel<2, 4>},
+    {4, 1, false, combine_kernel<4, 1>}, {4, 2, false, combine_kernel<4, 2>},
+    {8, 1, false, combine_kernel<8, 1>}, {8, 2, false, combine_kernel<8, 2>},
+    {0, 1, false, combine_kernel<0, 1>}, {0, 2, false, combine_kernel<0, 2>},
+    {1, 2, true, combine_batched_kernel<1, 2>}, {1, 4, true, combine_batched_kernel<1, 4>},
+    {2, 2, true, combine_batched_kernel<2, 2>},
 };
 
 // Measured on GB300: fewer loads per lane and more resident warps win
 // (k*U of 2 to 8 vectors in flight per lane).  With the packed fp32
 // arithmetic U=2 also wins for top-1 batches of few tokens (r8 T256 H5120:
 // 25.6 vs 26.0 us per step with U=4), where the scalar code had preferred U=4.
-int default_unroll(int k) {
+// With batched metadata (fewer tokens than warps) U=4 wins for top-1 (r8 E128
+// T256 H5120: 24.6 against 24.8 us per step with U=2, 26.2 us unbatched).
+int default_unroll(int k, bool batch) {
     switch (k) {
-        case 1: return 2;
+        case 1: return batch ? 4 : 2;
         case 2: return 2;
         case 4: return 1;
         case 8: return 1;
@@ -388,13 +462,14 @@ int default_unroll(int k) {
     }
 }
 
-// Kernel for this plan's k and requested unroll (nearest instantiated one).
-const CombineVariant *pick_variant(int k, int want_u) {
+// Kernel for this plan's k and requested unroll (nearest instantiated one);
+// nullptr if there is no batched kernel for k.
+const CombineVariant *pick_variant(int k, int want_u, bool batch) {
     const int kk = (k == 1 || k == 2 || k == 4 || k == 8) ? k : 0;
-    const int u = want_u > 0 ? want_u : (kk ? default_unroll(kk) : 2);
+    const int u = want_u > 0 ? want_u : (kk ? default_unroll(kk, batch) : (batch ? 1 : 2));
     const CombineVariant *best = nullptr;
     for (const auto &v : kCombineVariants) {
-        if (v.k != kk) continue;
+        if (v.k != kk || v.batch != batch) continue;
         if (!best || abs(v.u - u) < abs(best->u - u) || (abs(v.u - u) == abs(best->u - u) && v.u < best->u))
             best = &v;
     }
@@ -414,6 +489,7 @@ cudaError_t occupancy_grid(a2av_plan_s &p, const CombineVariant *v) {
     if (ns > steps_per_row) ns = steps_per_row;
     p.comb_nsplit = (int32_t)ns;
     p.comb_unroll = v->u;
+    p.comb_batch = v->batch;
     return e;
 }
 
@@ -464,8 +540,17 @@ cudaError_t configure_combine(a2av_plan_s &p) {
         return e;
     }
     p.combine_tma = 0;
-    e = occupancy_grid(p, pick_variant(p.g.k, p.cfg.combine_unroll));
+    e = occupancy_grid(p, pick_variant(p.g.k, p.cfg.combine_unroll, false));
     if (e != cudaSuccess) return e;
+    // Fewer tokens than warps: the call is latency-bound.  The pack then lets
+    // the combine's CTAs take their SM slots early, and where rows are split
+    // into several pieces the combine batches its metadata loads.
+    p.few_tokens = (long long)p.g.R * p.g.T < (long long)p.combine.grid * 8;
+    const CombineVariant *vb = p.few_tokens ? pick_variant(p.g.k, p.cfg.combine_unroll, true) : nullptr;
+    if (vb && (p.g.H >> 3) > 32 * vb->u) {
+        e = occupancy_grid(p, vb);
+        if (e != cudaSuccess) return e;
+    }
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, expert_scale_kernel, 256, 0);
     p.scale.grid = p.num_sms * (per_sm > 0 ? per_sm : 1);
@@ -483,7 +568,7 @@ cudaError_t launch_combine(const a2av_plan_s &p, const CombineArgs &a, cudaStrea
         return e != cudaSuccess ? e : cudaGetLastError();
     }
     b.nsplit = p.comb_nsplit;
-    e = launch_pdl(pick_variant(p.g.k, p.comb_unroll)->fn, p.combine.grid, 256, 0, s, b);
+    e = launch_pdl(pick_variant(p.g.k, p.comb_unroll, p.comb_batch)->fn, p.combine.grid, 256, 0, s, b);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

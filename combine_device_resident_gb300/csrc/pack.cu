@@ -107,6 +107,12 @@ __host__ __device__ constexpr size_t pack_tail_bytes(int stages) {
 template <bool COUNTED, bool PADDED>
 __global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
+    // Latency-bound calls (few tokens): the combine, a programmatic
+    // dependent, may take its SM slots now; its own grid-dependency wait
+    // still covers every store of this grid.  Not on large calls: there the
+    // early CTAs cost the pack about 4% (r16 E128 T4096 top-2: 661 against
+    // 636 us per step).
+    if (a.trigger_early) grid_launch_dependents();
     const Geometry &g = a.g;
     const int lane = threadIdx.x;
     const int NS = a.stages, CH = a.chunk_bytes, nch = a.nchunks;
@@ -276,6 +282,7 @@ __global__ void __launch_bounds__(256) pack_lsu_kernel(const PackArgs a) {
     const size_t rowb = (size_t)g.H * 2;
     const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
     uint32_t ovf = 0;
+    if (a.trigger_early) grid_launch_dependents();  // as in the TMA pack
     grid_dependency_wait();
     for (long long u = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < ntok; u += nw) {
         const int s_tok = (int)(u / g.T);
@@ -419,6 +426,7 @@ cudaError_t launch_exchange_padded(const a2av_plan_s &p, const ExchangeArgs &a, 
 
 cudaError_t launch_pack(const a2av_plan_s &p, const PackArgs &a, cudaStream_t s) {
     PackArgs b = a;  // b.rows_final: set by the caller from the splits launch that preceded it
+    b.trigger_early = p.few_tokens ? 1 : 0;
     cudaError_t e;
     if (p.pack_tma) {
         b.chunk_bytes = p.pack_chunk_bytes;
