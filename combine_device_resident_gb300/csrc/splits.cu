@@ -400,7 +400,6 @@ __device__ __forceinline__ int ld_dsmem(uint32_t addr) {
 template <bool BY_EXPERT, bool WRITE_REO>
 __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(const HistArgs a) {
     extern __shared__ int smem[];
-    __shared__ int wtot[33];
     grid_launch_dependents();
     const Geometry &g = a.g;
     const int R = g.R, E = g.E, epr = g.epr, ES = E + 1;
@@ -418,6 +417,16 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
     int *xb = wb + R;                    // [E] expert order: rows of expert e on ranks below s
     int *xt = xb + E;                    // [E] expert order: rows of e on all ranks, then e's block start
     constexpr bool by_expert = BY_EXPERT;
+    // the routing loads go out first; the counters are cleared while they fly
+    int vals[kClusterRounds];
+    {
+        const int32_t *idx = a.idx + (size_t)s * A;
+#pragma unroll
+        for (int r = 0; r < kClusterRounds; ++r) {
+            const int ai = a0 + r * 32 + lane;
+            vals[r] = (r * 32 < chunk && ai < A) ? __ldg(idx + ai) : -1;
+        }
+    }
     for (int i = tid; i < kClusterWarps * ES; i += kClusterThreads) cnt[i] = 0;
     if (by_expert)
         for (int i = tid; i < 2 * E; i += kClusterThreads) xb[i] = 0;  // xb and xt
@@ -426,13 +435,6 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
     int key[kClusterRounds], rank[kClusterRounds];
     int *mine = cnt + warp * ES;
     {
-        const int32_t *idx = a.idx + (size_t)s * A;
-        int vals[kClusterRounds];
-#pragma unroll
-        for (int r = 0; r < kClusterRounds; ++r) {
-            const int ai = a0 + r * 32 + lane;
-            vals[r] = (r * 32 < chunk && ai < A) ? __ldg(idx + ai) : -1;
-        }
         bool bad = false;
 #pragma unroll
         for (int r = 0; r < kClusterRounds; ++r) {
@@ -454,18 +456,26 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
         const int v = cnt[lane * ES + e];
         const int incl = warp_inclusive_scan(v, lane);
         cnt[lane * ES + e] = incl - v;
-        if (lane == 31) {
-            so[e] = incl;
-            a.sp.send_counts[(size_t)s * E + e] = incl;
-            const int d = e / epr, le = e - d * epr;
-            a.sp.recv_expert_counts[((size_t)d * R + s) * epr + le] = incl;
-        }
+        if (lane == 31) so[e] = incl;
     }
     __syncthreads();
-    const int total = block_exclusive_scan(so, E, wtot);
-    if (tid == 0) so[E] = total;
-    for (int e = tid; e < E; e += kClusterThreads) a.sp.send_offsets[(size_t)s * E + e] = so[e];
+    if (warp == 0) {  // exclusive scan of the E counts by one warp (one barrier, not four)
+        const int per = (E + 31) / 32;
+        const int lo = min(E, lane * per), hi = min(E, lo + per);
+        int sum = 0;
+        for (int i = lo; i < hi; ++i) sum += so[i];
+        const int incl = warp_inclusive_scan(sum, lane);
+        int run = incl - sum;
+        for (int i = lo; i < hi; ++i) {
+            const int v = so[i];
+            so[i] = run;
+            run += v;
+        }
+        if (lane == 31) so[E] = incl;
+    }
     __syncthreads();
+    // (send_counts, send_offsets and recv_expert_counts are stored after the
+    // cluster barriers: a barrier's release would otherwise wait for them)
 
     // every rank's send offsets are now in its CTA's shared memory
     cluster_barrier();
@@ -552,6 +562,14 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
         }
     }
     if (__any_sync(kFull, ovf) && lane == 0) atomicOr(a.status, (uint32_t)A2AV_DEV_WINDOW_OVERFLOW);
+    // this rank's send counts and offsets (so[] holds the exclusive offsets, so[E] the total)
+    for (int e = tid; e < E; e += kClusterThreads) {
+        const int c = so[e + 1] - so[e];
+        const int d = e / epr, le = e - d * epr;
+        a.sp.send_counts[(size_t)s * E + e] = c;
+        a.sp.send_offsets[(size_t)s * E + e] = so[e];
+        a.sp.recv_expert_counts[((size_t)d * R + s) * epr + le] = c;
+    }
     // first row of each of this rank's (destination, local expert) blocks
     if (WRITE_REO)
         for (int e = tid; e < E; e += kClusterThreads) {
