@@ -263,7 +263,11 @@ __global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
         __syncwarp();
     }
     if (lane == 0) {
-        bulk_wait_all();
+        // Leave once every stage has been read: the stores' writes to the
+        // windows complete before the grid does, which is what the kernels
+        // after it wait for.
+        if (timed_out) bulk_wait_all();
+        else bulk_wait_read<0>();
         if (timed_out) {
             // Leave only after every load this CTA issued has landed (bounded).
             for (long long p = i; p < issued; ++p) mbar_wait_bounded(&bars[p % NS], (uint32_t)((p / NS) & 1));
