@@ -213,14 +213,19 @@ def test_status_read_and_clear():
     assert plan.read_status() == 0
 
 
-def test_graph_replay_with_new_routing_each_time():
+# (4, 1100, 136): a large call; (3, 256, 1032) and (4, 128, 520): few-token
+# calls (fewer tokens than combine warps, rows split into pieces), which take
+# the pack's early launch of the combine and the batched-metadata combine.
+@pytest.mark.parametrize("wid,T,H", [(4, 1100, 136), (3, 256, 1032), (4, 128, 520)],
+                         ids=["large", "few-tokens-top1", "few-tokens-top2"])
+def test_graph_replay_with_new_routing_each_time(wid, T, H):
     # Capture dispatch + combine once; then rewrite topk_idx/gate_w in place and
     # replay.  The counts change with every replay while the graph stays the
     # same, and every replay matches the oracle.
     import torch
     from combine_device_resident_gb300 import Plan
 
-    w = W.WORKLOADS[4].scaled(T=1100, H=136)
+    w = W.WORKLOADS[wid].scaled(T=T, H=H)
     dev = P.device()
     plan = Plan(w.R, w.E, w.T, w.H, w.k, device=dev)
     x = W.make_x(w, 0, device=dev)
