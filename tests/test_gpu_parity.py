@@ -349,7 +349,10 @@ def _counts(w, seed):
     return nt
 
 
-@pytest.mark.parametrize("wid,T,H", [(1, None, None), (2, 1000, 136), (3, 256, 72), (4, 2100, 40), (5, 300, 64)])
+# (3, 256, 1032) and (4, 128, 520): few-token calls with rows split into
+# pieces (the batched-metadata combine and the pack's early launch).
+@pytest.mark.parametrize("wid,T,H", [(1, None, None), (2, 1000, 136), (3, 256, 72), (4, 2100, 40), (5, 300, 64),
+                                     (3, 256, 1032), (4, 128, 520)])
 def test_active_token_counts(wid, T, H):
     w = W.WORKLOADS[wid] if T is None else W.WORKLOADS[wid].scaled(T=T, H=H)
     g = P.full_parity(w, num_tokens=_counts(w, wid))
