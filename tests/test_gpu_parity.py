@@ -204,6 +204,53 @@ def test_fixed_window_overflow_is_flagged_and_bounded():
     assert g["guard_ok"]
 
 
+def test_null_and_misaligned_pointers_are_rejected():
+    # Host-side argument checks of the C ABI: a null or misaligned buffer is
+    # refused with A2AV_ERR_INVALID_ARG before anything is enqueued (the
+    # plan's launch count does not move and the device status stays clear).
+    import ctypes
+
+    import torch
+    from combine_device_resident_gb300 import Plan
+
+    w = W.WORKLOADS[2].scaled(T=64, H=136)
+    dev = P.device()
+    plan = Plan(w.R, w.E, w.T, w.H, w.k, device=dev)
+    L, h = plan.lib, plan.handle
+    x = W.make_x(w, 0, device=dev)
+    idx = torch.zeros((w.R, w.T, w.k), dtype=torch.int32, device=dev)
+    gate = torch.ones((w.R, w.T, w.k), dtype=torch.float32, device=dev)
+    recv, slot_map, out = plan.new_buffers()
+    sp = plan.new_splits()
+    spp = ctypes.byref(sp.ptrs)
+    stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    before = L.a2av_plan_launches(h)
+    p = lambda t, off=0: ctypes.c_void_p(t.data_ptr() + off)  # noqa: E731
+    null = ctypes.c_void_p(0)
+    invalid = 1  # A2AV_ERR_INVALID_ARG
+    bad_dispatch = [
+        (null, p(idx), spp, p(recv), p(slot_map)),          # null x
+        (p(x, 2), p(idx), spp, p(recv), p(slot_map)),       # x not 16-byte aligned
+        (p(x), p(idx), spp, p(recv, 8), p(slot_map)),       # recv not 16-byte aligned
+        (p(x), p(idx, 2), spp, p(recv), p(slot_map)),       # topk_idx not 4-byte aligned
+        (p(x), p(idx), spp, p(recv), null),                 # null slot_map
+    ]
+    for a in bad_dispatch:
+        assert L.a2av_dispatch(h, *a, stream) == invalid
+    bad_combine = [
+        (p(recv, 2), p(gate), p(slot_map), p(out)),         # y not 16-byte aligned
+        (p(recv), null, p(slot_map), p(out)),               # null gate
+        (p(recv), p(gate), p(slot_map), p(out, 4)),         # out not 16-byte aligned
+    ]
+    for a in bad_combine:
+        assert L.a2av_combine(h, *a, stream) == invalid
+    assert L.a2av_dispatch(None, p(x), p(idx), spp, p(recv), p(slot_map), stream) == invalid  # no plan
+    torch.cuda.synchronize()
+    assert L.a2av_plan_launches(h) == before
+    assert plan.read_status() == 0
+    plan.close()
+
+
 def test_status_read_and_clear():
     w = _uniform(2, 4, 100, 8, 1)
     idx = np.full((2, 100, 1), 9, np.int32)
