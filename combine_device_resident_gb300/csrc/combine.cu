@@ -12,7 +12,10 @@
 // vector gathers of 32*U vectors per step.  The kernel is
 // instantiated for k in {1, 2, 4, 8} so that all k*U loads of a unit are in
 // flight before the ordered accumulation; other k use the generic loop.
-// Launched as a programmatic dependent of the pack kernel.
+// Calls with fewer tokens than warps (decode-sized batches, rows split into
+// pieces) run combine_batched_kernel, which loads the slot rows and gates of
+// several units at once.  Launched as a programmatic dependent of the pack
+// kernel.
 //
 // Also here: the expert stand-in of the checkable workload,
 // y = bf16_rne(recv * (1 + e/E)), and its launcher.
