@@ -354,11 +354,11 @@ def main():
     import combine_device_resident_gb300 as A
 
     rank, world, local = dist_env()
+    torch.cuda.set_device(local)  # before the process group, so NCCL binds this rank's GPU
     if world > 1:
         import torch.distributed as dist
 
         dist.init_process_group("nccl", init_method="env://")
-    torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
     padded = args.mode == "padded"
