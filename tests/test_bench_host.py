@@ -18,3 +18,25 @@ def test_kernel_hashes_are_distinct_and_stable():
     hs = {k: bench.kernel_source_hash(k) for k in bench.KERNEL_SOURCES}
     assert len(set(hs.values())) == len(hs)
     assert hs == {k: bench.kernel_source_hash(k) for k in bench.KERNEL_SOURCES}
+
+
+def test_traffic_record_is_keyed_on_workload_and_kernel():
+    w2 = "r8-e16-t1024-h5120-top1-uniform"
+    assert bench.ncu_traffic("pack", "no-such-workload") is None
+    assert bench.ncu_traffic("route", w2) is None  # no capture recorded for the router
+    assert bench.ncu_traffic("no-such-kernel", w2) is None
+
+
+def test_traffic_record_per_launch_bytes_add_up():
+    import json
+    import os
+
+    d = json.load(open(os.path.join(bench.ROOT, "profiles", "ncu_traffic.json")))
+    for name, ent in d["kernels"].items():
+        live = ent["live"]
+        assert ent["dram_bytes_per_launch"] == live["dram_read_bytes"] + live["dram_write_bytes"], name
+        if "per_launch" in live:  # the mean of the captured launches
+            reads = [r for r, _ in live["per_launch"]]
+            writes = [w_ for _, w_ in live["per_launch"]]
+            assert live["dram_read_bytes"] == sum(reads) // len(reads), name
+            assert live["dram_write_bytes"] == sum(writes) // len(writes), name
