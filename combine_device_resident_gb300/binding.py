@@ -40,7 +40,7 @@ EXPORTED = [
     "a2av_read_device_status", "a2av_device_status_ptr", "a2av_plan_launches",
     "a2av_status_string", "a2av_last_error", "a2av_dispatch_static",
     "a2av_dispatch_padded", "a2av_pack_padded", "a2av_exchange_padded", "a2av_set_active_tokens",
-    "a2av_route", "a2av_route_splits",
+    "a2av_route", "a2av_route_splits", "a2av_set_wait_limit",
 ]
 
 
@@ -136,6 +136,8 @@ def load_library(path: Optional[str] = None):
     L.a2av_route.restype = i32
     L.a2av_route_splits.argtypes = [vp, vp, vp, vp, spp, vp, vp]
     L.a2av_route_splits.restype = i32
+    L.a2av_set_wait_limit.argtypes = [vp, ctypes.c_int64]
+    L.a2av_set_wait_limit.restype = i32
     if path is None:
         _lib = L
     return L
@@ -378,6 +380,11 @@ class Plan:
             self.handle, self._rows(recv, "recv"), self._t(topk_idx, torch.int32, (self.R, self.T, self.k), "topk_idx"),
             self._t(slot_map, torch.int32, (self.R, self.T, self.k), "slot_map"), self._rows(y, "y"),
             _stream_ptr(stream, self.device)), "a2av_expert_scale")
+
+    def set_wait_limit(self, polls: int = -1):
+        """Main-loop poll limit of the TMA kernels' bounded waits for later
+        calls (0: give up at once; negative: the default)."""
+        _check(self.lib, self.lib.a2av_set_wait_limit(self.handle, int(polls)), "a2av_set_wait_limit")
 
     def read_status(self, clear: bool = False, stream=None) -> int:
         bits = ctypes.c_uint32(0)

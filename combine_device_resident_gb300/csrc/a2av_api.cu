@@ -428,6 +428,12 @@ a2av_status_t a2av_set_active_tokens(a2av_plan_t p, const int32_t *num_tokens) {
     return A2AV_OK;
 }
 
+a2av_status_t a2av_set_wait_limit(a2av_plan_t p, int64_t polls) {
+    if (!p) return A2AV_ERR_INVALID_ARG;
+    p->wait_polls = polls < 0 ? a2av::kWaitLimit : (polls > a2av::kWaitLimit ? a2av::kWaitLimit : polls);
+    return A2AV_OK;
+}
+
 const void *a2av_device_status_ptr(a2av_plan_t p) { return p ? p->status : nullptr; }
 
 int64_t a2av_plan_launches(a2av_plan_t p) { return p ? p->launches : -1; }

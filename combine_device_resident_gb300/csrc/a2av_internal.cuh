@@ -22,6 +22,9 @@ constexpr int kMaxTopk = 32;
 // Status bit set when a bounded wait gives up (should never happen: every wait
 // in these kernels is on copies this CTA issued itself).
 constexpr uint32_t kDevWaitTimeout = 1u << 31;
+// Polls of a bounded mbarrier wait before it gives up (each poll is a
+// try_wait, which itself blocks for a while): seconds, far beyond any copy.
+constexpr long long kWaitLimit = 1ll << 22;
 
 struct Splits {
     int32_t *send_counts, *send_offsets, *recv_counts, *recv_offsets, *recv_expert_counts, *recv_total,
@@ -76,6 +79,7 @@ struct PackArgs {
     int32_t lag;          // store groups allowed to read a stage before it is refilled
     int64_t padded_tk;    // padded plans: T*k, and `recv` is the padded send buffer
     int32_t trigger_early;  // 1: let the dependent grid launch at once (few tokens: latency-bound call)
+    int64_t wait_polls;     // main-loop mbarrier wait limit (kWaitLimit unless a2av_set_wait_limit)
 };
 
 struct RouteArgs {
@@ -107,6 +111,7 @@ struct CombineArgs {
     int32_t nchunks;      // chunks per row
     int32_t stages;
     int32_t nsplit;       // LSU variant: pieces per row
+    int64_t wait_polls;   // TMA variant: main-loop mbarrier wait limit
 };
 
 struct ScaleArgs {
@@ -152,6 +157,7 @@ struct a2av_plan_s {
     int pack_tma = 1;
     int32_t pack_chunk_bytes = 0, pack_nchunks = 0, pack_stages = 0, pack_lag = 1;
     int64_t launches = 0;
+    int64_t wait_polls = a2av::kWaitLimit;  // main-loop wait limit of the TMA kernels (a2av_set_wait_limit)
     // 1: the last splits launch left final rows in slot_map (cluster kernel);
     // 0: tile ranks (tiled kernels).  The next pack reads it.
     int last_rows_final = 0;
@@ -259,8 +265,6 @@ __device__ __forceinline__ void st_stream_v4(void *p, const uint4 &v) {
 // mbarrier + bulk-copy (TMA) helpers.  Every wait is bounded: a kernel that
 // gives up sets a status bit and returns instead of hanging the GPU.
 // ---------------------------------------------------------------------------
-constexpr long long kWaitLimit = 1ll << 22;  // bounded spin on our own copies
-
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -285,8 +289,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
-    for (long long it = 0; it < kWaitLimit; ++it)
+// At most `limit` polls (0: give up without polling).  Kernels take the
+// main-loop limit from their arguments (a2av_set_wait_limit) and always
+// drain their own copies with kWaitLimit.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, long long limit = kWaitLimit) {
+    for (long long it = 0; it < limit; ++it)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }

@@ -360,13 +360,17 @@ __global__ void __launch_bounds__(32, 1) combine_tma_kernel(const CombineArgs a)
     for (long long i = 0; i < n; ++i) {
         const int st = (int)(i % NS);
         int ok = 1;
-        if (lane == 0) ok = mbar_wait_bounded(&full[st], (uint32_t)((i / NS) & 1));
+        if (lane == 0) ok = mbar_wait_bounded(&full[st], (uint32_t)((i / NS) & 1), a.wait_polls);
         ok = __shfl_sync(kFull, ok, 0);
         if (!ok) {
             timed_out = true;
-            // let every copy this CTA issued land before leaving (bounded)
+            // Let every copy this CTA issued land before leaving: unit i's (the
+            // one the wait gave up on) and those after it.  Full bound, as in
+            // the pack: in-bounds bulk copies complete unless the context is
+            // already lost.
             if (lane == 0)
-                for (long long p = i + 1; p < issued; ++p) mbar_wait_bounded(&full[p % NS], (uint32_t)((p / NS) & 1));
+                for (long long p = i; p < issued; ++p)
+                    mbar_wait_bounded(&full[p % NS], (uint32_t)((p / NS) & 1), kWaitLimit);
             break;
         }
         const long long tok = tb + i / nch;
@@ -567,6 +571,7 @@ cudaError_t launch_combine(const a2av_plan_s &p, const CombineArgs &a, cudaStrea
         b.chunk_bytes = p.comb_chunk_bytes;
         b.nchunks = p.comb_nchunks;
         b.stages = p.comb_stages;
+        b.wait_polls = p.wait_polls;
         e = launch_pdl(combine_tma_kernel, p.combine.grid, p.combine.block, p.combine.smem, s, b);
         return e != cudaSuccess ? e : cudaGetLastError();
     }

@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
         }
         const int st = (int)(i % NS);
         int ok = 1;
-        if (lane == 0) ok = mbar_wait_bounded(&bars[st], (uint32_t)((i / NS) & 1));
+        if (lane == 0) ok = mbar_wait_bounded(&bars[st], (uint32_t)((i / NS) & 1), a.wait_polls);
         ok = __shfl_sync(kFull, ok, 0);
         if (!ok) {
             timed_out = true;
@@ -269,8 +269,15 @@ __global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
         if (timed_out) bulk_wait_all();
         else bulk_wait_read<0>();
         if (timed_out) {
-            // Leave only after every load this CTA issued has landed (bounded).
-            for (long long p = i; p < issued; ++p) mbar_wait_bounded(&bars[p % NS], (uint32_t)((p / NS) & 1));
+            // Leave only after every load this CTA issued has landed, unit i's
+            // included (it is the one the main loop gave up on).  These waits
+            // keep the full bound whatever the main loop's limit: each load is
+            // a bulk copy of in-bounds rows of x, which completes in
+            // microseconds unless the memory system itself has failed (then
+            // the context is already lost), so the bound is never reached in a
+            // live context.
+            for (long long p = i; p < issued; ++p)
+                mbar_wait_bounded(&bars[p % NS], (uint32_t)((p / NS) & 1), kWaitLimit);
             atomicOr(a.status, kDevWaitTimeout);
         }
     }
@@ -431,6 +438,7 @@ cudaError_t launch_exchange_padded(const a2av_plan_s &p, const ExchangeArgs &a, 
 cudaError_t launch_pack(const a2av_plan_s &p, const PackArgs &a, cudaStream_t s) {
     PackArgs b = a;  // b.rows_final: set by the caller from the splits launch that preceded it
     b.trigger_early = p.few_tokens ? 1 : 0;
+    b.wait_polls = p.wait_polls;
     cudaError_t e;
     if (p.pack_tma) {
         b.chunk_bytes = p.pack_chunk_bytes;
