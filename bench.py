@@ -4,7 +4,18 @@
 One step = one pass of the whole path on one batch: splits (histogram + scan),
 pack + exchange into the destination windows, and the top-k combine, replayed
 from one CUDA graph, with the inputs already resident in HBM.  The L2 is
-flushed (a 512 MiB write) between timed steps, outside the step's events.
+flushed between timed steps by reading a 512 MiB buffer, outside the step's
+events (a read leaves only clean lines behind, so no write-back of the flush
+lands inside the next step).
+
+Beside the step figure the line carries the two halves timed apart with the
+same flush before each (``split_flush``: in a MoE layer the expert FFN runs
+between dispatch and combine, so the combine cannot find the pack's rows in
+L2), and, for workloads whose receive arena fits in L2, the step with a warm
+L2 (``l2_warm``).  ``--layers L`` captures L independent dispatch+combine
+pairs (each with its own buffers) back to back in one graph, as a decode step
+over L MoE layers would, and reports the time per pair without the cost of
+launching a graph for every call.
 
 Prints ONE JSON line (rank 0).  ``value`` is dispatch+combine algorithmic
 bytes / step time in GB/s, summed over all GPUs; tokens/s and microseconds per
@@ -37,13 +48,14 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "dispatch+combine HBM GB/s (% of GB300 peak), tokens/s and µs per call at 1 GPU"
-DEFAULT_WORKLOAD = 2
+DEFAULT_WORKLOAD = 5
 FLUSH_BYTES = 512 << 20
+L2_BYTES = 126 << 20  # GB300's L2, if the device properties do not say
 FALLBACK_HBM_GBS = 6800.0
 
 
 # ---------------------------------------------------------------------------
-def parse():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
@@ -72,14 +84,19 @@ def parse():
     ap.add_argument("--combine-unroll", type=int, default=0)
     ap.add_argument("--kernel-steps", type=int, default=300, help="steps of the per-kernel timing pass")
     ap.add_argument("--e2e-steps", type=int, default=30)
-    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline sample budget")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0, help="CPU baseline sample budget (both settings)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--l2", choices=["flush", "warm"], default="flush",
                     help="flush L2 before every step (default) or replay back to back with a warm L2 "
                          "(context for workloads that fit in L2; not the reported default)")
     ap.add_argument("--reference-seconds", type=float, default=90.0, help="reference arm: total budget")
-    return ap.parse_args()
+    ap.add_argument("--layers", type=int, default=0,
+                    help="capture this many independent dispatch+combine pairs (own buffers each) in one graph "
+                         "and report the time per pair (decode over several MoE layers)")
+    ap.add_argument("--cpu-threads", type=int, default=0,
+                    help="threads of the CPU baseline's per-rank setting (0 = min(R, usable cores))")
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -229,8 +246,54 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-def cpu_baseline(w: W.Workload, x_host_bits, idx, gate, budget_s: float):
-    """Time the CPU oracle (as it stands, one thread) on a bounded sample."""
+def _sample(a, T_s):
+    """The first T_s tokens of every rank, as a contiguous array (made
+    before the timed region, so no leg pays for the copy)."""
+    import numpy as np
+
+    return np.ascontiguousarray(a[:, :T_s])
+
+
+def oracle_step_threaded(wl: W.Workload, xb, ix, gt, pool, nthr: int):
+    """One pass of the unchanged oracle functions with the per-rank work on
+    `nthr` threads: the splits (a few integer passes over idx) on the calling
+    thread, then each thread dispatches a contiguous range of source ranks
+    into the shared arena (disjoint rows), applies the expert stand-in to its
+    own assignments and combines its own tokens.  Returns (recv, slot_map,
+    out) so that tests can compare it with the one-thread run."""
+    import numpy as np
+
+    import oracle
+
+    R, T, k, H = wl.R, wl.T, wl.k, wl.H
+    sp = oracle.splits(R, wl.E, ix, wl.window_mode, wl.window_rows)
+    recv = np.zeros((oracle.arena_rows(R, T, k, wl.window_mode, wl.window_rows), H), np.uint16)
+    sm = np.empty((R, T, k), np.int32)
+    bounds = [(R * i // nthr, R * (i + 1) // nthr) for i in range(nthr)]
+    bounds = [b for b in bounds if b[0] < b[1]]
+    for f in [pool.submit(oracle.dispatch, R, wl.E, xb, ix, sp, wl.window_mode, wl.window_rows, recv=recv,
+                          ranks=b, slot_map_out=sm) for b in bounds]:
+        f.result()
+    y = recv
+    if wl.expert == "scale":
+        y = recv.copy()
+        for f in [pool.submit(oracle.expert_scale, wl.E, recv, ix[s0:s1], sm[s0:s1], y) for s0, s1 in bounds]:
+            f.result()
+    out = np.empty((R * T, H), np.uint16)
+    futs = [(s0, s1, pool.submit(oracle.combine, y, gt, sm, np.arange(s0 * T, s1 * T, dtype=np.int64)))
+            for s0, s1 in bounds]
+    for s0, s1, f in futs:
+        out[s0 * T:s1 * T] = f.result()
+    return recv, sm, out.reshape(R, T, H)
+
+
+def cpu_baseline(w: W.Workload, x_host_bits, idx, gate, budget_s: float, threads: int = 0):
+    """Time the CPU oracle on a bounded sample of the workload, in two
+    settings: (i) as it stands, one thread (oracle.run_all); (ii) one thread
+    per emulated rank, capped at the usable cores: the same oracle functions
+    on disjoint source-rank ranges (oracle_step_threaded)."""
+    import concurrent.futures
+
     import oracle
 
     def run(wl, xb, ix, gt):
@@ -241,20 +304,46 @@ def cpu_baseline(w: W.Workload, x_host_bits, idx, gate, budget_s: float):
     # probe with a small slice of tokens, then size the sample to the budget
     probe_T = max(1, min(w.T, 64))
     wp = w.scaled(T=probe_T)
-    tp = run(wp, x_host_bits[:, :probe_T], idx[:, :probe_T], gate[:, :probe_T])
+    tp = run(wp, _sample(x_host_bits, probe_T), _sample(idx, probe_T), _sample(gate, probe_T))
     per_token = tp / probe_T
-    T_s = int(min(w.T, max(probe_T, budget_s / 2 / max(per_token, 1e-9))))
+    leg_s = budget_s / 4  # each leg: about a quarter for the sample, the rest for reps
+    T_s = int(min(w.T, max(probe_T, leg_s / max(per_token, 1e-9))))
     ws = w.scaled(T=T_s)
-    xs, ixs, gs = x_host_bits[:, :T_s], idx[:, :T_s], gate[:, :T_s]
+    xs, ixs, gs = _sample(x_host_bits, T_s), _sample(idx, T_s), _sample(gate, T_s)
     reps, spent = 0, 0.0
-    while spent < budget_s / 2 or reps == 0:
+    while spent < leg_s or reps == 0:
         spent += run(ws, xs, ixs, gs)
         reps += 1
     value = ws.algorithmic_bytes() * reps / spent / 1e9
     sample = (f"oracle (splits, dispatch, combine) on the first {T_s} of {w.T} tokens per rank "
               f"of every rank, {reps} rep(s), {spent:.1f} s")
-    return {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
-            "tokens_per_s": round(ws.R * ws.T * reps / spent, 1), "host": host_cpu()}
+    res = {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
+           "tokens_per_s": round(ws.R * ws.T * reps / spent, 1), "host": host_cpu()}
+
+    # (ii) per-rank threads (source order: the rank ranges of the dispatch)
+    usable = len(os.sched_getaffinity(0))
+    nthr = min(w.R, usable) if threads <= 0 else min(threads, w.R)
+    if w.recv_order != "source" or nthr < 2:
+        res.update({"threads": 1, "value_threaded": None})
+        return res
+    T_t = int(min(w.T, max(probe_T, T_s * nthr)))
+    wt = w.scaled(T=T_t)
+    xt, ixt, gtt = _sample(x_host_bits, T_t), _sample(idx, T_t), _sample(gate, T_t)
+    reps_t, spent_t = 0, 0.0
+    with concurrent.futures.ThreadPoolExecutor(max_workers=nthr) as pool:
+        oracle_step_threaded(wp, _sample(x_host_bits, probe_T), _sample(idx, probe_T), _sample(gate, probe_T),
+                             pool, nthr)
+        while spent_t < leg_s or reps_t == 0:
+            t = time.perf_counter()
+            oracle_step_threaded(wt, xt, ixt, gtt, pool, nthr)
+            spent_t += time.perf_counter() - t
+            reps_t += 1
+    res.update({"threads": nthr, "value_threaded": round(wt.algorithmic_bytes() * reps_t / spent_t / 1e9, 4),
+                "tokens_per_s_threaded": round(wt.R * wt.T * reps_t / spent_t, 1),
+                "sample_threaded": (f"the same oracle functions, one thread per emulated rank (capped at the "
+                                    f"{usable} usable cores: {nthr} threads; splits on one), first {T_t} of "
+                                    f"{w.T} tokens per rank, {reps_t} rep(s), {spent_t:.1f} s")})
+    return res
 
 
 def host_cpu() -> dict:
@@ -317,7 +406,7 @@ def run_reference(args, w: W.Workload):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": steps, "warmup": warm, "ms_per_step": round(dt * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_block(w, "none (host memory)"),
+        "config": config_block(w, args),
         "tokens_per_s": round(ws.R * ws.T / dt, 2), "us_per_call": round(dt * 1e6, 2),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
                          "host": host_cpu()},
@@ -329,15 +418,169 @@ def run_reference(args, w: W.Workload):
     return 0
 
 
-def config_block(w: W.Workload, l2: str):
-    return {"workload": w.name, "R": w.R, "E": w.E, "T": w.T, "H": w.H, "k": w.k, "routing": w.routing,
-            "gate": w.gate, "window": w.window_mode, "recv_order": w.recv_order, "l2": l2, "accumulate": "fp32",
-            "parallelism": "replicas"}
+def l2_protocol(args) -> str:
+    """How the L2 is handled between timed steps (the same text in both arms,
+    so that their ``config`` blocks compare equal)."""
+    if args.l2 == "flush":
+        return (f"GPU arm: L2 flushed before every step by reading a {FLUSH_BYTES >> 20} MiB buffer; "
+                "CPU arm: host memory")
+    return "GPU arm: steps back to back with a warm L2; CPU arm: host memory"
+
+
+def config_block(w: W.Workload, args) -> dict:
+    c = {"workload": w.name, "R": w.R, "E": w.E, "T": w.T, "H": w.H, "k": w.k, "routing": w.routing,
+         "gate": w.gate, "window": w.window_mode, "recv_order": w.recv_order, "l2": l2_protocol(args),
+         "accumulate": "fp32", "parallelism": "replicas"}
+    if getattr(args, "layers", 0) > 0:
+        c["layers"] = args.layers
+    return c
+
+
+def make_plan(args, w: W.Workload, dev):
+    import combine_device_resident_gb300 as A
+
+    return A.Plan(w.R, w.E, w.T, w.H, w.k, w.window_mode, w.window_rows, device=dev,
+                  flags=args.flags | (A.FLAG_ROUTE_FUSED if args.router and args.router_fused else 0),
+                  pack_ctas_per_sm=args.pack_ctas_per_sm, pack_stage_bytes=args.pack_stage_bytes,
+                  pack_store_lag=args.pack_store_lag, combine_ctas_per_sm=args.combine_ctas_per_sm,
+                  combine_stage_bytes=args.combine_stage_bytes, combine_unroll=args.combine_unroll,
+                  recv_order=w.recv_order)
+
+
+# ---------------------------------------------------------------------------
+def run_layers(args, w: W.Workload, dev, rank: int, world: int, local: int):
+    """L independent dispatch+combine pairs captured back to back in one
+    graph, each with its own inputs, splits and buffers (routing drawn with
+    seed = layer index), replayed after an L2 flush: the per-pair time of a
+    decode step over L MoE layers, without a graph launch per call.  Nested
+    graphs of the first 1, 2, 3 stages of every layer give the per-stage
+    time per layer."""
+    import torch
+
+    L = args.layers
+    plan = make_plan(args, w, dev)
+    flush = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_out = torch.zeros((), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    x0 = W.make_x(w, 0, device=dev)
+    layers = []
+    for i in range(L):
+        rg = W.make_routing_gate(w, i)
+        recv, slot_map, out = plan.new_buffers()
+        layers.append(dict(x=x0.clone(), idx=torch.from_numpy(rg["topk_idx"]).to(dev),
+                           gate=torch.from_numpy(rg["gate_w"]).to(dev), sp=plan.new_splits(), recv=recv,
+                           slot=slot_map, out=out))
+    del x0
+
+    def stage_fns(b):
+        return [lambda s: plan.splits(b["idx"], b["sp"], b["slot"], stream=s),
+                lambda s: plan.pack(b["x"], b["idx"], b["sp"], b["recv"], b["slot"], stream=s),
+                lambda s: plan.combine(b["recv"], b["gate"], b["slot"], b["out"], stream=s)]
+
+    with torch.cuda.stream(stream):
+        for b in layers:
+            for fn in stage_fns(b):
+                fn(stream)
+    torch.cuda.synchronize(dev)
+    if plan.read_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    def capture(n_stages):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            s_ = torch.cuda.current_stream(dev)
+            for b in layers:
+                for fn in stage_fns(b)[:n_stages]:
+                    fn(s_)
+        return g
+
+    launches0 = plan.launches
+    graph = capture(3)
+    kernels_per_step = plan.launches - launches0
+    nested = [capture(1), capture(2), graph]
+    g_null = torch.cuda.CUDAGraph()
+    null_t = torch.zeros(1, dtype=torch.int32, device=dev)
+    with torch.cuda.graph(g_null, stream=stream):
+        null_t.add_(1)
+
+    def flush_l2():
+        if args.l2 == "flush":
+            torch.sum(flush, dim=0, out=flush_out)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            for gr in nested:
+                flush_l2()
+                gr.replay()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(local, enabled=not args.no_clocks)
+    time.sleep(0.15 if sampler.proc else 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush_l2()
+            starts[i].record(stream)
+            graph.replay()
+            ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    t_wall1 = time.time()
+    sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms = max_over_ranks(sum(step_ms) / K)
+    if plan.read_status() != 0:
+        raise RuntimeError("device status word set during the timed region")
+
+    KK = max(1, min(K, args.kernel_steps))
+    timed = nested + [g_null]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(timed))] for _ in range(KK)]
+    with torch.cuda.stream(stream):
+        for i in range(KK):
+            for j, gr in enumerate(timed):
+                flush_l2()
+                ev[i][2 * j].record(stream)
+                gr.replay()
+                ev[i][2 * j + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    t_ms = [sum(ev[i][2 * j].elapsed_time(ev[i][2 * j + 1]) for i in range(KK)) / KK for j in range(len(timed))]
+    per_stage = {"splits": 1e3 * (t_ms[0] - t_ms[3]) / L, "pack": 1e3 * (t_ms[1] - t_ms[0]) / L,
+                 "combine": 1e3 * (t_ms[2] - t_ms[1]) / L}
+    bytes_pair = w.algorithmic_bytes()
+    job = whole_job(bytes_pair * L, w.R * w.T * L, ms, world)
+    peak, peak_kind = read_peaks()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(job["gbs"], 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_block(w, args), "layers": L,
+            "us_per_pair": round(1e3 * ms / L, 3), "tokens_per_s": round(job["tokens_per_s"], 1),
+            "pct_of_peak": round(100 * job["gbs"] / world / peak, 2), "peak_gbs": peak, "peak_kind": peak_kind,
+            "per_layer_stage_us": {n: round(v, 3) for n, v in per_stage.items()},
+            "graph_floor_us": round(1e3 * t_ms[3], 3),
+            "timing": (f"one graph of {L} x [splits, pack, combine], each layer with its own buffers; "
+                       f"{K} replays; stages from nested graphs of the first 1..3 stages of every layer, "
+                       f"{KK} replays each, minus the graph-launch floor for the first"),
+            "gpu_launches": int(kernels_per_step * K), "kernels_per_step": int(kernels_per_step),
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    plan.close()
+    return 0
 
 
 # ---------------------------------------------------------------------------
 def main():
-    args = parse()
+    args = parse_args()
     w = W.WORKLOADS[args.workload]
     if args.tokens:
         w = w.scaled(T=args.tokens)
@@ -348,10 +591,7 @@ def main():
     if args.impl == "reference":
         return run_reference(args, w)
 
-    import numpy as np
     import torch
-
-    import combine_device_resident_gb300 as A
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)  # before the process group, so NCCL binds this rank's GPU
@@ -360,6 +600,11 @@ def main():
 
         dist.init_process_group("nccl", init_method="env://")
     dev = torch.device("cuda", local)
+    if args.layers > 0:
+        rc = run_layers(args, w, dev, rank, world, local)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return rc
 
     padded = args.mode == "padded"
     if padded:
@@ -378,12 +623,7 @@ def main():
     x = W.make_x(w, 0, device=dev)
     idx = torch.from_numpy(idx_h).to(dev)
     gate = torch.from_numpy(gate_h).to(dev)
-    plan = A.Plan(w.R, w.E, w.T, w.H, w.k, w.window_mode, w.window_rows, device=dev,
-                  flags=args.flags | (A.FLAG_ROUTE_FUSED if args.router and args.router_fused else 0),
-                  pack_ctas_per_sm=args.pack_ctas_per_sm, pack_stage_bytes=args.pack_stage_bytes,
-                  pack_store_lag=args.pack_store_lag, combine_ctas_per_sm=args.combine_ctas_per_sm,
-                  combine_stage_bytes=args.combine_stage_bytes, combine_unroll=args.combine_unroll,
-                  recv_order=w.recv_order)
+    plan = make_plan(args, w, dev)
     recv, slot_map, out = plan.new_buffers()
     sp = plan.new_splits()
     sendbuf = plan.new_send_buffer() if padded else None
@@ -499,8 +739,12 @@ def main():
         raise RuntimeError(f"device status word set during the timed region: {status:#x}")
 
     # ---- per-kernel durations (same stream, same flush) ------------------------------
+    # Also the combine on its own (graph [combine]): with the flush before it,
+    # its rows come from DRAM, as they would after an expert FFN between the
+    # two halves (the split-flush figures).
+    g_comb = capture(stages[-1:])
     KK = max(1, min(K, args.kernel_steps))
-    timed = prefixes + [g_null]
+    timed = prefixes + [g_null, g_comb]
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(timed))] for _ in range(KK)]
     with torch.cuda.stream(stream):
         for i in range(KK):
@@ -511,6 +755,7 @@ def main():
                 ev[i][2 * j + 1].record(stream)
     torch.cuda.synchronize(dev)
     prefix_ms = [sum(ev[i][2 * j].elapsed_time(ev[i][2 * j + 1]) for i in range(KK)) / KK for j in range(len(timed))]
+    comb_alone_ms = prefix_ms.pop()
     names = [n for n, _ in stages]
     mean = {"+".join(names[:j + 1]): prefix_ms[j] for j in range(len(stages))}
     mean["null"] = prefix_ms[-1]
@@ -554,6 +799,52 @@ def main():
                 "timing": (f"marginal: nested graphs of the first 1..{len(stages)} kernels, "
                            f"{KK} steps each, L2 flushed before each replay"),
                 "nested_us": {n: round(1e3 * v, 3) for n, v in mean.items()}}
+
+    # ---- the two halves apart, each after its own flush ------------------------------
+    # dispatch = every stage but the combine (one graph), combine = its own
+    # graph; the sum is what a MoE layer pays when its expert FFN evicts the
+    # pack's rows between the halves.  Per kernel: the last dispatch kernel's
+    # marginal over the graph before it, and the combine graph minus the
+    # graph-launch floor (an empty-work graph timed the same way).
+    disp_ms = prefix_ms[len(stages) - 2]
+    floor_ms = mean["null"]
+    sf_kus = {names[-2]: 1e3 * (disp_ms - (prefix_ms[len(stages) - 3] if len(stages) >= 3 else floor_ms)),
+              names[-1]: 1e3 * (comb_alone_ms - floor_ms)}
+    sf_gbs = {n: kbytes[n] / (v * 1e-6) / 1e9 for n, v in sf_kus.items() if v > 0}
+    split_flush = {
+        "dispatch_us": round(1e3 * disp_ms, 3), "combine_us": round(1e3 * comb_alone_ms, 3),
+        "total_us": round(1e3 * (disp_ms + comb_alone_ms), 3), "graph_floor_us": round(1e3 * floor_ms, 3),
+        "gbs": round(bytes_step / ((disp_ms + comb_alone_ms) * 1e-3) / 1e9, 1),
+        "pct_of_peak": round(100 * bytes_step / ((disp_ms + comb_alone_ms) * 1e-3) / 1e9 / peak, 2),
+        "kernel_us": {n: round(v, 3) for n, v in sf_kus.items()},
+        "kernel_gbs": {n: round(v, 1) for n, v in sf_gbs.items()},
+        "kernel_frac": {n: round(v / peak, 4) for n, v in sf_gbs.items()},
+        "timing": (f"graphs [{', '.join(names[:-1])}] and [{names[-1]}] replayed {KK} times each, "
+                   "L2 flushed before each replay; the sum counts two graph launches"),
+    }
+    if traffic and dom in sf_kus and sf_kus[dom] > 0:
+        split_flush["traffic_frac"] = {dom: round(traffic / (sf_kus[dom] * 1e-6) / 1e9 / peak, 4)}
+
+    # ---- warm L2, for workloads whose receive arena fits in L2 ---------------------
+    l2_warm = None
+    arena_bytes = plan.arena_rows * w.H * 2
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or L2_BYTES)
+    if args.l2 == "flush" and arena_bytes <= l2_bytes:
+        KW = max(10, min(K, 1000))
+        ws_, we_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for _ in range(10):
+                graph.replay()
+            ws_.record(stream)
+            for _ in range(KW):
+                graph.replay()
+            we_.record(stream)
+        torch.cuda.synchronize(dev)
+        warm_ms = max_over_ranks(ws_.elapsed_time(we_) / KW)
+        l2_warm = {"ms_per_step": round(warm_ms, 5), "us_per_call": round(1e3 * warm_ms, 3),
+                   "gbs": round(whole_job(bytes_step, w.R * t_active, warm_ms, world)["gbs"], 1),
+                   "pct_of_peak": round(100 * bytes_step / (warm_ms * 1e-3) / 1e9 / peak, 2), "steps": KW,
+                   "timing": "graph replayed back to back, no flush (each step pays the previous one's write-back)"}
 
     # ---- end to end through host buffers ----------------------------------------
     # Inputs come from pinned host memory and the result goes back to pinned
@@ -679,7 +970,7 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and not padded and t_active == w.T and not args.router:
-        cpu = cpu_baseline(w, W.bf16_bits(x), idx_h, gate_h, args.cpu_seconds)
+        cpu = cpu_baseline(w, W.bf16_bits(x), idx_h, gate_h, args.cpu_seconds, args.cpu_threads)
 
     if rank == 0:
         line = {
@@ -687,13 +978,12 @@ def main():
             "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5), "ms_median_per_step": round(ms_median, 5),
             "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": config_block(w, f"flushed between steps (read of a {FLUSH_BYTES >> 20} MiB buffer)"
-                                   if args.l2 == "flush" else "warm: steps back to back, no flush"),
+            "config": config_block(w, args),
             "mode": args.mode, "active_tokens_per_rank": t_active,
             "router": (("fused" if args.router_fused else "separate") if args.router else False),
             "pct_of_peak": round(100 * gbs / world / peak, 2), "peak_gbs": peak,
             "tokens_per_s": round(job["tokens_per_s"], 1), "us_per_call": round(job["us_per_call"], 3),
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roofline, "split_flush": split_flush, "l2_warm": l2_warm, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(kernels_per_step * K), "kernels_per_step": int(kernels_per_step),
             "clocks": clocks, "variant": {"flags": args.flags, "pack_ctas_per_sm": args.pack_ctas_per_sm,
                                           "pack_stage_bytes": args.pack_stage_bytes,

@@ -77,6 +77,8 @@ def bind(L):
     L.oracle_dispatch.restype = ctypes.c_uint32
     L.oracle_dispatch.argtypes = [ci, ci, ci, ci, ci, ci, ci64, vp, u16p, i32p, i32p, i32p, i32p, i32p,
                                   u16p, i32p]
+    L.oracle_dispatch_ranks.restype = ctypes.c_uint32
+    L.oracle_dispatch_ranks.argtypes = L.oracle_dispatch.argtypes + [ci, ci]
     L.oracle_expert_scale.restype = None
     L.oracle_expert_scale.argtypes = [ci, ci, ci64, u16p, i32p, i32p, u16p]
     L.oracle_combine.restype = None
@@ -193,9 +195,14 @@ def arena_rows(R: int, T: int, k: int, window_mode="packed", window_rows: int = 
 
 
 def dispatch(R: int, E: int, x: np.ndarray, idx: np.ndarray, sp: dict, window_mode="packed",
-             window_rows: int = 0, recv: Optional[np.ndarray] = None, num_tokens=None, recv_order="source"):
+             window_rows: int = 0, recv: Optional[np.ndarray] = None, num_tokens=None, recv_order="source",
+             ranks=None, slot_map_out: Optional[np.ndarray] = None):
     """(recv uint16 [rows][H], slot_map, status).  x uint16 bf16 bits [R][T][H].
-    Rows no assignment reaches keep their prior contents (zeros if recv is None)."""
+    Rows no assignment reaches keep their prior contents (zeros if recv is None).
+
+    ``ranks=(s0, s1)``: only source ranks s0 <= s < s1 (source order only),
+    writing their rows into ``recv`` and their slots into ``slot_map_out``
+    (both shared by callers that run disjoint ranges, e.g. one per thread)."""
     x = np.ascontiguousarray(x, dtype=np.uint16)
     idx = np.ascontiguousarray(idx, dtype=np.int32)
     _, T, H = x.shape
@@ -203,11 +210,19 @@ def dispatch(R: int, E: int, x: np.ndarray, idx: np.ndarray, sp: dict, window_mo
     rows = arena_rows(R, T, k, window_mode, window_rows)
     if recv is None:
         recv = np.zeros((rows, H), np.uint16)
-    sm = np.empty((R, T, k), np.int32)
+    sm = np.empty((R, T, k), np.int32) if slot_map_out is None else slot_map_out
     nt, _keep = _counts_ptr(num_tokens)
-    st = lib().oracle_dispatch(R, E, T, H, k, _mode(window_mode, recv_order), int(window_rows), nt, x, idx,
-                               sp["send_counts"], sp["send_offsets"], sp["recv_offsets"],
-                               sp["window_base"], recv, sm)
+    args = (R, E, T, H, k, _mode(window_mode, recv_order), int(window_rows), nt, x, idx,
+            sp["send_counts"], sp["send_offsets"], sp["recv_offsets"], sp["window_base"], recv, sm)
+    if ranks is None:
+        st = lib().oracle_dispatch(*args)
+    else:
+        if recv_order not in (0, "source"):
+            raise ValueError("a source-rank range is defined for the source order only")
+        s0, s1 = (int(v) for v in ranks)
+        if not 0 <= s0 <= s1 <= R:
+            raise ValueError(f"rank range {ranks} outside [0, {R}]")
+        st = lib().oracle_dispatch_ranks(*args, s0, s1)
     return recv, sm, int(st)
 
 

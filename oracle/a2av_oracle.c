@@ -322,6 +322,17 @@ static uint32_t dispatch_expert_order(int R, int E, int T, int H, int k, int lay
                                       const int32_t *recv_offsets, const int32_t *window_base,
                                       uint16_t *recv, int32_t *slot_map);
 
+/* The source-order dispatch of source ranks s_begin <= s < s_end only (each
+ * source's send buffer and segments are its own; the splits are those of
+ * every rank).  oracle_dispatch runs it over all ranks; a caller that splits
+ * the ranks into disjoint ranges and runs each range on its own thread gets
+ * the same recv and slot_map (the ranges write disjoint rows and slots). */
+uint32_t oracle_dispatch_ranks(int R, int E, int T, int H, int k, int window_mode, int64_t window_rows,
+                               const int32_t *num_tokens, const uint16_t *x, const int32_t *idx,
+                               const int32_t *send_counts, const int32_t *send_offsets,
+                               const int32_t *recv_offsets, const int32_t *window_base,
+                               uint16_t *recv, int32_t *slot_map, int s_begin, int s_end);
+
 uint32_t oracle_dispatch(int R, int E, int T, int H, int k, int window_mode, int64_t window_rows,
                          const int32_t *num_tokens, const uint16_t *x, const int32_t *idx,
                          const int32_t *send_counts, const int32_t *send_offsets,
@@ -331,13 +342,25 @@ uint32_t oracle_dispatch(int R, int E, int T, int H, int k, int window_mode, int
     if (window_mode & ORACLE_ORDER_EXPERT)
         return dispatch_expert_order(R, E, T, H, k, ORACLE_LAYOUT(window_mode), window_rows, num_tokens, x, idx,
                                      send_counts, send_offsets, recv_offsets, window_base, recv, slot_map);
+    return oracle_dispatch_ranks(R, E, T, H, k, window_mode, window_rows, num_tokens, x, idx, send_counts,
+                                 send_offsets, recv_offsets, window_base, recv, slot_map, 0, R);
+}
+
+uint32_t oracle_dispatch_ranks(int R, int E, int T, int H, int k, int window_mode, int64_t window_rows,
+                               const int32_t *num_tokens, const uint16_t *x, const int32_t *idx,
+                               const int32_t *send_counts, const int32_t *send_offsets,
+                               const int32_t *recv_offsets, const int32_t *window_base,
+                               uint16_t *recv, int32_t *slot_map, int s_begin, int s_end)
+{
+    if (window_mode & ORACLE_ORDER_EXPERT)
+        return 0xffffffffu; /* source order only */
     uint32_t status = 0;
     int epr = E / R;
     size_t row_bytes = sizeof(uint16_t) * (size_t)H;
     int32_t *running = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
     int32_t *pos = (int32_t *)malloc(sizeof(int32_t) * (size_t)T * k + 4);
     uint16_t *sendbuf = (uint16_t *)malloc(row_bytes * (size_t)T * k + 16);
-    for (int s = 0; s < R; ++s) {
+    for (int s = s_begin; s < s_end; ++s) {
         const int32_t *idx_s = idx + (size_t)s * T * k;
         const int32_t *so = send_offsets + (size_t)s * E;
         const int32_t *sc = send_counts + (size_t)s * E;

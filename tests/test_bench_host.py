@@ -40,3 +40,36 @@ def test_traffic_record_per_launch_bytes_add_up():
             writes = [w_ for _, w_ in live["per_launch"]]
             assert live["dram_read_bytes"] == sum(reads) // len(reads), name
             assert live["dram_write_bytes"] == sum(writes) // len(writes), name
+
+
+def test_threaded_oracle_step_equals_one_thread_run():
+    # CPU baseline setting (ii): the same oracle functions on disjoint
+    # source-rank ranges, one thread each, give the one-thread results.
+    import concurrent.futures
+
+    import numpy as np
+
+    import oracle
+    import workloads as W
+
+    for wid, T, H, nthr in [(4, 40, 16, 5), (5, 10, 8, 16), (2, 30, 8, 3)]:
+        w = W.WORKLOADS[wid].scaled(T=T, H=H)
+        x = W.bf16_bits(W.make_x(w, 0))
+        rg = W.make_routing_gate(w, 0)
+        ref = oracle.run_all(w.R, w.E, x, rg["topk_idx"], rg["gate_w"], w.window_mode, w.window_rows, w.expert)
+        with concurrent.futures.ThreadPoolExecutor(max_workers=nthr) as pool:
+            recv, sm, out = bench.oracle_step_threaded(w, x, rg["topk_idx"], rg["gate_w"], pool, nthr)
+        np.testing.assert_array_equal(sm, ref["slot_map"])
+        np.testing.assert_array_equal(recv, ref["recv"])
+        np.testing.assert_array_equal(out, ref["out"])
+
+
+def test_cpu_baseline_reports_both_settings():
+    import workloads as W
+
+    w = W.WORKLOADS[5].scaled(T=16, H=64)
+    x = W.bf16_bits(W.make_x(w, 0))
+    rg = W.make_routing_gate(w, 0)
+    cb = bench.cpu_baseline(w, x, rg["topk_idx"], rg["gate_w"], budget_s=0.5, threads=4)
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] > 0
+    assert cb["threads"] == 4 and cb["value_threaded"] > 0 and "4 threads" in cb["sample_threaded"]

@@ -87,7 +87,14 @@ def test_reference_arm_prints_one_line_on_cpu():
     assert d["value"] > 0 and d["steps"] == 2 and d["warmup"] == 1
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
-    assert d["config"]["workload"].startswith("r8-e16-t1024-h5120")
+    # the largest single-GPU workload by default, with the GPU arm's config block
+    assert d["config"]["workload"].startswith("r32-e256-t2048-h7168")
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+
+    args = bench.parse_args([])
+    assert d["config"] == bench.config_block(W.WORKLOADS[bench.DEFAULT_WORKLOAD], args)
 
 
 def test_reference_arm_nonzero_ranks_exit_quietly():

@@ -22,7 +22,7 @@ import numpy as np
 import pytest
 
 import oracle
-from tests.bf16util import bits_to_f32, f32_to_bits_torch, ulp_diff
+from tests.bf16util import bits_to_f32, f32_to_bits_torch, is_nan, ulp_diff
 
 SPLIT_KEYS = ["send_counts", "send_offsets", "recv_counts", "recv_offsets",
               "recv_expert_counts", "recv_total", "window_base"]
@@ -557,6 +557,83 @@ def test_combine_rounds_product_and_sum_hand_case():
     y = np.repeat(SLOT_PAIR_Y[:, None], H, axis=1)
     out = oracle.combine(y, SLOT_PAIR_W.reshape(1, 1, 2), np.array([[[0, 1]]], np.int32))
     assert (out == SLOT_PAIR_SEPARATE).all(), out
+
+
+@pytest.mark.parametrize("wid,T,H,nthr", [(2, 40, 16, 3), (3, 64, 8, 8), (4, 50, 8, 5), (5, 12, 8, 7)])
+def test_dispatch_by_rank_ranges_equals_whole_dispatch(wid, T, H, nthr):
+    # The per-rank CPU setting runs disjoint source-rank ranges of the same
+    # dispatch; together they must place every row and slot as one call does
+    # (fixed windows with overflow included).
+    import workloads as W
+
+    w = W.WORKLOADS[wid].scaled(T=T, H=H)
+    x = W.bf16_bits(W.make_x(w, 3))
+    idx = W.make_routing_gate(w, 3)["topk_idx"]
+    window_rows = w.window_rows if w.window_mode != "fixed" else max(1, w.window_rows // 9)
+    sp = oracle.splits(w.R, w.E, idx, w.window_mode, window_rows)
+    recv, sm, st = oracle.dispatch(w.R, w.E, x, idx, sp, w.window_mode, window_rows)
+    recv2 = np.zeros_like(recv)
+    sm2 = np.full_like(sm, -7)
+    st2 = 0
+    for i in range(nthr):
+        s0, s1 = w.R * i // nthr, w.R * (i + 1) // nthr
+        _, _, sti = oracle.dispatch(w.R, w.E, x, idx, sp, w.window_mode, window_rows, recv=recv2, ranks=(s0, s1),
+                                    slot_map_out=sm2)
+        st2 |= sti
+    np.testing.assert_array_equal(sm2, sm)
+    np.testing.assert_array_equal(recv2, recv)
+    assert st2 == st
+    with pytest.raises(ValueError):
+        oracle.dispatch(w.R, w.E, x, idx, sp, ranks=(0, 1), recv_order="expert")
+
+
+def test_combine_non_finite_values_follow_ieee():
+    # Reading: infinities and NaNs in the expert outputs go through the
+    # combine's fp32 products and sums as IEEE 754 defines them (a zero gate
+    # times an infinity is NaN, +inf plus -inf is NaN, a NaN stays NaN).  Pinned
+    # against numpy's float32 arithmetic, which shares nothing with the oracle,
+    # on every pair of special and ordinary values under every pair of gates.
+    vals = np.array([0x7F80, 0xFF80, 0x7FC1, 0xFFA0, 0x3FC0, 0xC000, 0x0000, 0x8000, 0x4040], np.uint16)
+    gates = np.array([0.0, 1.0, 0.5, -1.0, -0.0, np.inf], np.float32)
+    ys, ws = [], []
+    for a in vals:
+        for b in vals:
+            for g0 in gates:
+                for g1 in gates:
+                    ys.append((a, b))
+                    ws.append((g0, g1))
+    n = len(ys)
+    H = 2  # column 1 holds a finite control value
+    y = np.zeros((2 * n, H), np.uint16)
+    y[:, 0] = np.array(ys, np.uint16).reshape(-1)
+    y[:, 1] = 0x3F80
+    gate = np.array(ws, np.float32).reshape(1, n, 2)
+    sm = np.arange(2 * n, dtype=np.int32).reshape(1, n, 2)
+    out = oracle.combine(y, gate, sm)
+    yf = bits_to_f32(np.array(ys, np.uint16))
+    wf = np.array(ws, np.float32)
+    with np.errstate(invalid="ignore", over="ignore"):
+        acc = np.float32(0.0) + (wf[:, 0] * yf[:, 0]).astype(np.float32)
+        acc = (acc + (wf[:, 1] * yf[:, 1]).astype(np.float32)).astype(np.float32)
+        ctrl = ((np.float32(0.0) + wf[:, 0]).astype(np.float32) + wf[:, 1]).astype(np.float32)
+    for col, want_f in ((0, acc), (1, ctrl)):
+        got = out[:, col]
+        nan = np.isnan(want_f)
+        assert is_nan(got[nan]).all(), "a NaN result must come out as a NaN"
+        assert not is_nan(got[~nan]).any()
+        np.testing.assert_array_equal(got[~nan], f32_to_bits_torch(want_f[~nan]))
+    # the cases the reading names, spelled out
+    index = {(int(a), int(b), float(g0), float(g1)): i for i, ((a, b), (g0, g1)) in enumerate(zip(ys, ws))}
+
+    def one(a, b, g0, g1):
+        return int(out[index[(a, b, g0, g1)], 0])
+
+    assert is_nan(one(0x7F80, 0x3FC0, 0.0, 1.0))       # 0 * inf
+    assert one(0x7F80, 0x3FC0, 1.0, 1.0) == 0x7F80      # inf + 1.5
+    assert is_nan(one(0x7F80, 0xFF80, 1.0, 0.5))       # inf + -inf
+    assert is_nan(one(0x7FC1, 0x3FC0, 1.0, 1.0))       # NaN in, NaN out
+    assert one(0x7F80, 0x3FC0, -1.0, 1.0) == 0xFF80     # the sign of the gate
+    assert one(0x3FC0, 0x4040, np.inf, 0.0) == 0x7F80   # an infinite gate on a finite row
 
 
 def test_scaled_experts_closed_form_numpy_f32():
