@@ -10,8 +10,33 @@ def ordered(bits: np.ndarray) -> np.ndarray:
     return np.where(b & 0x8000, -mag, mag)
 
 
+# Distance reported for a pair that must match exactly and does not.
+MISMATCH = 1 << 16
+
+
+def is_nan(bits: np.ndarray) -> np.ndarray:
+    b = np.asarray(bits).astype(np.int32)
+    return ((b & 0x7F80) == 0x7F80) & ((b & 0x7F) != 0)
+
+
+def is_inf(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits).astype(np.int32) & 0x7FFF) == 0x7F80
+
+
 def ulp_diff(a: np.ndarray, b: np.ndarray) -> np.ndarray:
-    return np.abs(ordered(a) - ordered(b))
+    """bf16 ulp distance of finite values (+0 == -0).  Non-finite values are
+    compared by what they are: a NaN matches any NaN (sign and payload are not
+    fixed by the arithmetic: the oracle keeps a quiet payload, the GPU's
+    conversion returns one canonical NaN) and nothing else; an infinity
+    matches only the same infinity.  A mismatch counts as MISMATCH ulps."""
+    a, b = np.asarray(a), np.asarray(b)
+    d = np.abs(ordered(a) - ordered(b))
+    an, bn = is_nan(a), is_nan(b)
+    d = np.where(an | bn, np.where(an & bn, 0, MISMATCH), d)
+    ai, bi = is_inf(a), is_inf(b)
+    special_inf = (ai | bi) & ~(an | bn)
+    same = np.asarray(a).astype(np.int32) == np.asarray(b).astype(np.int32)
+    return np.where(special_inf, np.where(same, 0, MISMATCH), d)
 
 
 def bits_to_f32(bits: np.ndarray) -> np.ndarray:

@@ -10,7 +10,7 @@ import pytest
 import oracle
 import workloads as W
 from tests import parity as P
-from tests.bf16util import ulp_diff
+from tests.bf16util import is_inf, is_nan, ulp_diff
 
 pytestmark = pytest.mark.gpu
 
@@ -202,6 +202,40 @@ def test_fixed_window_overflow_is_flagged_and_bounded():
     assert g["status"] & A.DEV_WINDOW_OVERFLOW
     assert (g["slot_map"] >= 0).sum() == 2 * 900
     assert g["guard_ok"]
+
+
+@pytest.mark.parametrize("wid,T,H,flags", [(4, 300, 72, 0), (4, 300, 72, 4), (5, 60, 136, 0), (3, 256, 264, 0)],
+                         ids=["top2", "top2-tma-combine", "top8", "top1-fixed"])
+def test_non_finite_payloads(wid, T, H, flags):
+    # Reading on non-finite values: the dispatch copies NaN and infinity bits
+    # unchanged (bit-exact, as every recv row); the combine follows IEEE fp32
+    # (a zero gate times an infinity is NaN, +inf plus -inf is NaN, a NaN stays
+    # NaN); a NaN output matches any NaN, an infinity only the same infinity.
+    import torch
+
+    w = W.WORKLOADS[wid].scaled(T=T, H=H)
+    dev = P.device()
+    x = W.make_x(w, 0, device=dev)
+    rg = W.make_routing_gate(w, 0)
+    idx, gate = rg["topk_idx"], rg["gate_w"].copy()
+    xb = x.view(torch.int16)
+    PINF, NINF, QNAN, SNAN = 0x7F80, -0x80, 0x7FC1, -0x60  # bf16 +inf, -inf, quiet NaN, 0xFFA0 (signalling, negative)
+    xb[0, 0, :] = PINF
+    xb[0, 1, :] = NINF
+    xb[0, 2, 3] = QNAN
+    xb[0, 3, 0::2] = PINF
+    xb[0, 3, 1::2] = NINF
+    xb[1, 4, 7] = SNAN
+    xb[1, 5, :] = PINF
+    gate[0, 0, -1] = 0.0   # a zero gate on an infinite row: NaN (top-1: the only slot)
+    gate[1, 5, 0] = -gate[1, 5, 0]  # opposite infinities in one sum when k > 1
+    g = P.full_parity(w, x=x, idx=idx, gate=gate, flags=flags)
+    ref = g["ref"]["out"].reshape(w.R * w.T, w.H)
+    out = g["out"].reshape(w.R * w.T, w.H)
+    assert is_nan(ref).any() and is_inf(ref).any()  # the case is not vacuous
+    np.testing.assert_array_equal(is_nan(out), is_nan(ref))
+    fin = ~is_nan(ref)
+    np.testing.assert_array_equal(out[fin], ref[fin])  # everything else bit for bit
 
 
 def test_null_and_misaligned_pointers_are_rejected():
