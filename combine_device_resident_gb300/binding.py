@@ -397,26 +397,64 @@ class Plan:
         return int(self.lib.a2av_plan_launches(self.handle))
 
 
+def _static_shape_checks(L, cfg, x, topk_idx, splits, recv, slot_map, dev_status, R, E, T, H, k):
+    """Shapes a2av_dispatch_static's kernels rely on (the C ABI only sees
+    pointers): x (R,T,H), topk_idx and slot_map (R,T,k), recv with at least
+    the arena's rows of H values, a dev_status element, and split arrays
+    made for R ranks and E experts.  Raises A2avError before anything is
+    enqueued."""
+    rc = L.a2av_config_check(ctypes.byref(cfg))
+    if rc != A2AV_OK:
+        raise A2avError(f"a2av_dispatch_static: invalid configuration R={R} E={E} T={T} H={H} k={k}")
+    want = {"x": (x, (R, T, H)), "topk_idx": (topk_idx, (R, T, k)), "slot_map": (slot_map, (R, T, k))}
+    for name, (t, shape) in want.items():
+        if tuple(t.shape) != shape:
+            raise A2avError(f"{name} has shape {tuple(t.shape)}, expected {shape}")
+    rows = int(L.a2av_recv_arena_rows(ctypes.byref(cfg)))
+    if recv.dim() != 2 or recv.shape[1] != H or recv.shape[0] < rows:
+        raise A2avError(f"recv has shape {tuple(recv.shape)}, expected at least ({rows}, {H})")
+    if dev_status.numel() < 1:
+        raise A2avError("dev_status needs one element")
+    epr = E // R
+    shapes = {"send_counts": (R, E), "send_offsets": (R, E), "recv_counts": (R, R), "recv_offsets": (R, R),
+              "recv_expert_counts": (R, R, epr), "recv_total": (R,), "window_base": (R,),
+              "recv_expert_offsets": (R, R, epr)}
+    for name in splits.names:
+        t = getattr(splits, name)
+        if tuple(t.shape) != shapes[name]:
+            raise A2avError(f"splits.{name} has shape {tuple(t.shape)}, expected {shapes[name]} (R={R}, E={E})")
+    if cfg.recv_order == ORDER_EXPERT and "recv_expert_offsets" not in splits.names:
+        raise A2avError("the expert-grouped receive order needs splits.recv_expert_offsets")
+
+
 def dispatch_static(x, topk_idx, splits: Splits, recv, slot_map, dev_status, R, E, T, H, k,
                     window_mode="packed", window_rows=0, flags=0, stream=None, recv_order="source"):
     """Dispatch without a plan and without any allocation (a2av_dispatch_static).
 
-    For callers that cannot allocate device memory at the point of dispatch:
-    the kernels' scratch lives in a static device array of the library (1 MiB
-    per GPU), so shapes are bounded; ``dev_status`` is a caller-owned int32
-    device tensor of one element that receives the A2AV_DEV_* bits.  The first
-    call on a device does a one-time set-up, so make it before any graph
-    capture; calls that overlap on the GPU share the array and race.
+    For callers that cannot allocate device memory where they dispatch (a
+    framework whose caching allocator owns all device memory, a spent
+    device-memory budget, a loop that cannot take cudaMalloc's implicit
+    synchronisation): the kernels' scratch lives in a static device array of
+    the library (1 MiB per GPU), so shapes are bounded; ``dev_status`` is a
+    caller-owned int32 device tensor of one element that receives the
+    A2AV_DEV_* bits.  The first call on a device (and the first with each
+    configuration) does a one-time set-up, so make it before any stream
+    capture; calls that overlap on the GPU share the array and race.  Every
+    shape is checked here before anything is enqueued.
     """
     import torch
 
     L = load_library()
     dev = x.device
-    cfg = make_config(R, E, T, H, k, window_mode, window_rows, dev.index, flags, recv_order=recv_order)
-    for t, dt, name in ((x, torch.bfloat16, "x"), (topk_idx, torch.int32, "topk_idx"), (recv, torch.bfloat16, "recv"),
-                        (slot_map, torch.int32, "slot_map"), (dev_status, torch.int32, "dev_status")):
-        if t.device != dev or t.dtype != dt or not t.is_contiguous():
-            raise A2avError(f"{name}: expected a contiguous {dt} tensor on {dev}")
+    cfg = make_config(R, E, T, H, k, window_mode, window_rows, dev.index if dev.index is not None else 0, flags,
+                      recv_order=recv_order)
+    _static_shape_checks(L, cfg, x, topk_idx, splits, recv, slot_map, dev_status, R, E, T, H, k)
+    tensors = [(x, torch.bfloat16, "x"), (topk_idx, torch.int32, "topk_idx"), (recv, torch.bfloat16, "recv"),
+               (slot_map, torch.int32, "slot_map"), (dev_status, torch.int32, "dev_status")]
+    tensors += [(getattr(splits, n), torch.int32, f"splits.{n}") for n in splits.names]
+    for t, dt, name in tensors:
+        if t.device != dev or dev.type != "cuda" or t.dtype != dt or not t.is_contiguous():
+            raise A2avError(f"{name}: expected a contiguous {dt} tensor on the CUDA device of x ({dev})")
     rc = L.a2av_dispatch_static(ctypes.byref(cfg), ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(topk_idx.data_ptr()),
                                 ctypes.byref(splits.ptrs), ctypes.c_void_p(recv.data_ptr()),
                                 ctypes.c_void_p(slot_map.data_ptr()), ctypes.c_void_p(dev_status.data_ptr()),

@@ -1,19 +1,22 @@
 // Dispatch without any allocation: a2av_dispatch_static.
 //
-// Some callers cannot call cudaMalloc: code that runs while a CUDA graph is
-// being captured in a mode that forbids allocation, code inside a framework
-// whose caching allocator owns all device memory and must not be bypassed,
-// or processes with a fixed device-memory budget that is exhausted by the
-// time this library runs.  For them this entry point keeps its scratch (the
-// per-tile histogram bases, the per-rank totals and the completion counters
-// the splits kernel needs) in one file-scope __device__
-// array, so the only device memory it touches besides the caller's buffers
-// is memory the library already owns from the moment it is loaded.
+// Some callers cannot call cudaMalloc where they dispatch: code inside a
+// framework whose caching allocator owns all device memory and must not be
+// bypassed, processes that run under a fixed device-memory budget that is
+// spent by the time this library runs, and latency-critical loops that must
+// not take cudaMalloc's implicit device synchronisation.  For them this entry
+// point keeps its scratch (the per-tile histogram bases, the per-rank totals
+// and the completion counters the splits kernel needs) in one file-scope
+// __device__ array, so the only device memory it touches besides the
+// caller's buffers is memory the library already owns from the moment it is
+// loaded.
 //
 // The same splits and pack kernels as a2av_dispatch run; only where their
 // scratch lives differs.  The array is shared by every call in the process,
 // and every GPU that loads the library holds a copy of it until the process
-// exits.
+// exits.  Per device, the first call does the set-up (the array's device
+// address, the kernels' shared-memory attributes); per configuration, the
+// first call computes the launch shapes; both are kept for later calls.
 #include <stdio.h>
 
 #include <mutex>
@@ -30,20 +33,84 @@ static __device__ __align__(256) int32_t g_dispatch_scratch[kStaticScratchInts];
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 int32_t *g_scratch_addr[kMaxDevices];  // device address of the array, per device
+int g_num_sms[kMaxDevices];
 
 size_t round64(size_t n) { return (n + 63) / 64 * 64; }
 
-// Address of the array on `dev`, looked up once per device with `dev` current.
-cudaError_t scratch_on(int dev, int32_t **out) {
+// Launch shapes of one configuration on one device, computed by the first
+// call that uses them (configure_hist / configure_pack: kernel attributes,
+// occupancy and cluster-residency queries) and reused by later calls.
+struct ShapeEntry {
+    bool used = false;
+    a2av_config_t cfg{};
+    a2av::LaunchShape hist, pack;
+    int splits_small = 0;
+    int32_t pack_chunk_bytes = 0, pack_nchunks = 0, pack_stages = 0, pack_lag = 1;
+};
+constexpr int kShapeCache = 32;
+ShapeEntry g_shapes[kShapeCache];
+int g_next_shape = 0;  // round-robin replacement once the cache is full
+
+bool same_config(const a2av_config_t &a, const a2av_config_t &b) {
+    return a.num_ranks == b.num_ranks && a.num_experts == b.num_experts && a.tokens_per_rank == b.tokens_per_rank &&
+           a.hidden == b.hidden && a.topk == b.topk && a.window_mode == b.window_mode &&
+           a.window_rows == b.window_rows && a.device == b.device && a.flags == b.flags &&
+           a.pack_ctas_per_sm == b.pack_ctas_per_sm && a.pack_stage_bytes == b.pack_stage_bytes &&
+           a.pack_store_lag == b.pack_store_lag && a.combine_ctas_per_sm == b.combine_ctas_per_sm &&
+           a.combine_stage_bytes == b.combine_stage_bytes && a.combine_unroll == b.combine_unroll &&
+           a.recv_order == b.recv_order;
+}
+
+// One-time set-up of `dev` (with `dev` current): the array's device address
+// and the SM count.  A later cudaDeviceReset is not supported: the address
+// would belong to the destroyed context.
+cudaError_t device_setup_locked(int dev) {
+    if (g_scratch_addr[dev]) return cudaSuccess;
+    void *ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_dispatch_scratch);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = static_cast<int32_t *>(ptr);
+    return cudaSuccess;
+}
+
+// Fills p's device fields (scratch address, SM count) and launch shapes for
+// p.cfg, doing the device set-up and the shape configuration only the first
+// time they are needed.
+cudaError_t prepare(a2av_plan_s &p, int32_t **scratch) {
+    const int dev = p.cfg.device;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_addr[dev]) {
-        void *ptr = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&ptr, g_dispatch_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = static_cast<int32_t *>(ptr);
+    cudaError_t e = device_setup_locked(dev);
+    if (e != cudaSuccess) return e;
+    *scratch = g_scratch_addr[dev];
+    p.num_sms = g_num_sms[dev];
+    for (const ShapeEntry &s : g_shapes) {
+        if (s.used && same_config(s.cfg, p.cfg)) {
+            p.hist = s.hist;
+            p.pack = s.pack;
+            p.splits_small = s.splits_small;
+            p.pack_chunk_bytes = s.pack_chunk_bytes;
+            p.pack_nchunks = s.pack_nchunks;
+            p.pack_stages = s.pack_stages;
+            p.pack_lag = s.pack_lag;
+            return cudaSuccess;
+        }
     }
-    *out = g_scratch_addr[dev];
+    e = a2av::configure_hist(p);
+    if (e == cudaSuccess) e = a2av::configure_pack(p);
+    if (e != cudaSuccess) return e;
+    ShapeEntry &s = g_shapes[g_next_shape];
+    g_next_shape = (g_next_shape + 1) % kShapeCache;
+    s.used = true;
+    s.cfg = p.cfg;
+    s.hist = p.hist;
+    s.pack = p.pack;
+    s.splits_small = p.splits_small;
+    s.pack_chunk_bytes = p.pack_chunk_bytes;
+    s.pack_nchunks = p.pack_nchunks;
+    s.pack_stages = p.pack_stages;
+    s.pack_lag = p.pack_lag;
     return cudaSuccess;
 }
 
@@ -112,16 +179,13 @@ extern "C" a2av_status_t a2av_dispatch_static(const a2av_config_t *cfg, const vo
     cudaError_t e = cudaGetDevice(&prev);
     if (e == cudaSuccess && prev != cfg->device) e = cudaSetDevice(cfg->device);
     int32_t *scratch = nullptr;
-    if (e == cudaSuccess) e = scratch_on(cfg->device, &scratch);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p.num_sms, cudaDevAttrMultiProcessorCount, cfg->device);
+    if (e == cudaSuccess) e = prepare(p, &scratch);
     if (e == cudaSuccess) {
         p.tile_base = scratch;
         p.rank_total = scratch + n_tile;
         p.counters = reinterpret_cast<uint32_t *>(scratch + n_tile + n_tot);
         p.status = dev_status;
-        e = a2av::configure_hist(p);
     }
-    if (e == cudaSuccess) e = a2av::configure_pack(p);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // The completion counters must start at zero; the previous call leaves them
     // at zero, but clear them anyway so that nothing depends on earlier calls.

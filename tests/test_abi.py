@@ -125,3 +125,35 @@ def test_product_package_does_not_import_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 src = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in re.sub(r"#.*|//.*", "", src).replace("the oracle", ""), f
+
+
+def test_static_dispatch_checks_every_shape_on_the_host():
+    # a2av_dispatch_static's binding checks shapes before any device work, so
+    # a wrong shape fails here without a GPU (host tensors, never enqueued).
+    import torch
+
+    import combine_device_resident_gb300 as A
+    from combine_device_resident_gb300.binding import dispatch_static
+
+    R, E, T, H, k = 4, 16, 50, 64, 2
+    good = dict(x=torch.zeros((R, T, H), dtype=torch.bfloat16), topk_idx=torch.zeros((R, T, k), dtype=torch.int32),
+                splits=A.Splits(R, E, "cpu"), recv=torch.zeros((R * T * k, H), dtype=torch.bfloat16),
+                slot_map=torch.zeros((R, T, k), dtype=torch.int32), dev_status=torch.zeros(1, dtype=torch.int32))
+    bad = {"x": torch.zeros((R, T, H - 8), dtype=torch.bfloat16),
+           "topk_idx": torch.zeros((R, T - 1, k), dtype=torch.int32),
+           "splits": A.Splits(R, 2 * E, "cpu"),
+           "recv": torch.zeros((R * T * k - 1, H), dtype=torch.bfloat16),
+           "slot_map": torch.zeros((R, T, 1), dtype=torch.int32),
+           "dev_status": torch.zeros(0, dtype=torch.int32)}
+    for name, t in bad.items():
+        args = dict(good, **{name: t})
+        with pytest.raises(A.A2avError, match="shape|element"):
+            dispatch_static(args["x"], args["topk_idx"], args["splits"], args["recv"], args["slot_map"],
+                            args["dev_status"], R, E, T, H, k)
+    # right shapes, host tensors: refused for the device, still before any call
+    with pytest.raises(A.A2avError, match="CUDA device"):
+        dispatch_static(*good.values(), R, E, T, H, k)
+    expert = A.Splits(R, E, "cpu", expert_offsets=False)
+    with pytest.raises(A.A2avError, match="expert"):
+        dispatch_static(good["x"], good["topk_idx"], expert, good["recv"], good["slot_map"], good["dev_status"],
+                        R, E, T, H, k, recv_order="expert")

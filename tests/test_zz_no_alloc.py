@@ -1,8 +1,9 @@
 """a2av_dispatch_static: the dispatch for callers that cannot allocate device
-memory where they dispatch (for instance while a graph is captured in a mode
-that forbids allocation, or inside a framework whose allocator owns all device
-memory).  It keeps its kernels' scratch in a static device array of the
-library instead of a plan's workspace.
+memory where they dispatch (inside a framework whose caching allocator owns
+all device memory, under a device-memory budget that is already spent, or in
+a loop that cannot take cudaMalloc's implicit synchronisation).  It keeps its
+kernels' scratch in a static device array of the library instead of a plan's
+workspace.
 
 Checked through the C ABI against the plan-based a2av_dispatch on the same
 inputs, on two calls in a row with different routings (so contents the first
@@ -91,3 +92,32 @@ def test_static_dispatch_rejects_shapes_beyond_its_scratch():
         dispatch_static(x, idx, sp, recv, sm, status, R, E, T, H, k)
     torch.cuda.synchronize()
     assert int(sp.recv_total.sum().item()) == 0  # nothing was enqueued
+
+
+def test_static_dispatch_rejects_wrong_shapes_before_enqueueing():
+    import torch
+
+    import combine_device_resident_gb300 as A
+    from combine_device_resident_gb300.binding import dispatch_static
+
+    dev = torch.device("cuda", 0)
+    R, E, T, H, k = 4, 16, 50, 64, 2
+    good = dict(x=torch.zeros((R, T, H), dtype=torch.bfloat16, device=dev),
+                topk_idx=torch.zeros((R, T, k), dtype=torch.int32, device=dev),
+                splits=A.Splits(R, E, dev),
+                recv=torch.full((R * T * k, H), 5.0, dtype=torch.bfloat16, device=dev),
+                slot_map=torch.full((R, T, k), -9, dtype=torch.int32, device=dev),
+                dev_status=torch.zeros(1, dtype=torch.int32, device=dev))
+    bad = {"x": torch.zeros((R, T, H - 8), dtype=torch.bfloat16, device=dev),
+           "topk_idx": torch.zeros((R, T - 1, k), dtype=torch.int32, device=dev),
+           "splits": A.Splits(R, 2 * E, dev),
+           "recv": torch.zeros((R * T * k - 1, H), dtype=torch.bfloat16, device=dev),
+           "slot_map": torch.zeros((R, T, 1), dtype=torch.int32, device=dev),
+           "dev_status": torch.zeros(0, dtype=torch.int32, device=dev)}
+    for name, t in bad.items():
+        args = dict(good, **{name: t})
+        with pytest.raises(A.A2avError):
+            dispatch_static(args["x"], args["topk_idx"], args["splits"], args["recv"], args["slot_map"],
+                            args["dev_status"], R, E, T, H, k)
+    torch.cuda.synchronize()
+    assert (good["slot_map"] == -9).all() and (good["recv"] == 5.0).all()  # nothing ran
