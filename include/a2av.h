@@ -38,8 +38,9 @@
  *     (rows move as 16-byte vectors); integer/float arrays 4-byte aligned.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Enqueueing calls are asynchronous: they return after
- *     launching, never synchronise, allocate, or read device memory back, and
- *     can be captured into a CUDA graph.  A returned A2AV_OK means "enqueued".
+ *     launching and never synchronise, allocate, or read device memory back.
+ *     Those that take a plan can be captured into a CUDA graph (the plan is
+ *     made outside capture).  A returned A2AV_OK means "enqueued".
  *   - Host-side argument errors are returned synchronously
  *     (A2AV_ERR_INVALID_ARG) and nothing is enqueued.  Data errors found on
  *     the device (expert id out of range, fixed window too small) set sticky
@@ -221,23 +222,29 @@ a2av_status_t a2av_expert_scale(a2av_plan_t plan, const void *recv, const int32_
                                 const int32_t *slot_map, void *y, void *stream);
 
 /* Dispatch that allocates nothing (no plan, no cudaMalloc, no allocating
- * library call).  The paper has no counterpart; it exists for callers that
- * cannot allocate device memory where they dispatch -- for example code that
- * runs while a graph is captured in a mode that forbids allocation, or inside
- * a framework whose allocator owns all device memory.  Same inputs, outputs
- * and results as a2av_dispatch on a plan made from `cfg`; the scratch the
- * splits and pack kernels need lives in one static device array of the
- * library (1 MiB per GPU that loads the library, held until process exit),
- * which bounds the shapes it accepts: R*ceil(T*k/2048)*E + R + (R + 1) int32
- * (each term rounded up to 64) must fit in 262144, else A2AV_ERR_INVALID_ARG
- * with the sizes in a2av_last_error().  `dev_status` is a caller-owned device
+ * library call).  The paper has no counterpart.  It is for callers that
+ * cannot allocate device memory where they dispatch: code inside a framework
+ * whose caching allocator owns all device memory and must not be bypassed,
+ * processes under a fixed device-memory budget that is spent by the time
+ * this library runs, and latency-critical loops that cannot take the
+ * implicit device synchronisation of cudaMalloc.  Same inputs, outputs and
+ * results as a2av_dispatch on a plan made from `cfg`; the scratch the splits
+ * and pack kernels need lives in one static device array of the library
+ * (1 MiB per GPU that loads the library, held until process exit), which
+ * bounds the shapes it accepts: R*ceil(T*k/2048)*E + R + (R + 1) int32 (each
+ * term rounded up to 64) must fit in 262144, else A2AV_ERR_INVALID_ARG with
+ * the sizes in a2av_last_error().  `dev_status` is a caller-owned device
  * uint32 that the kernels OR the A2AV_DEV_* bits into (the caller clears it).
- * The first call on each device looks up the array's device address (a
- * synchronous runtime call), so make that first call before any stream
- * capture.  Every call uses the same array and leaves its last contents there
- * (the counters that must start at zero are cleared on the stream by each
- * call): calls that overlap on the GPU -- on different streams, or from
- * different threads without ordering -- race on it. */
+ * The first call on each device does a one-time set-up with that device
+ * current (it looks up the array's device address, a synchronous runtime
+ * call, and sets the kernels' attributes), and the first call with each
+ * configuration computes its launch shapes; both are kept for later calls,
+ * so make the first call before any stream capture.  cudaDeviceReset after
+ * the first call is not supported (the address looked up would belong to the
+ * destroyed context).  Every call uses the same array and leaves its last
+ * contents there (the counters that must start at zero are cleared on the
+ * stream by each call): calls that overlap on the GPU -- on different
+ * streams, or from different threads without ordering -- race on it. */
 a2av_status_t a2av_dispatch_static(const a2av_config_t *cfg, const void *x, const int32_t *topk_idx,
                                    const a2av_splits_t *splits, void *recv, int32_t *slot_map,
                                    uint32_t *dev_status, void *stream);
