@@ -112,6 +112,7 @@ struct CombineArgs {
     int32_t stages;
     int32_t nsplit;       // LSU variant: pieces per row
     int64_t wait_polls;   // TMA variant: main-loop mbarrier wait limit
+    int32_t trigger_early;  // 1: let the next kernel (a programmatic dependent) launch at once (few tokens)
 };
 
 struct ScaleArgs {
@@ -151,7 +152,7 @@ struct a2av_plan_s {
     int splits_small = 0;  // 1: one-CTA splits kernel that writes final rows
     const int32_t *num_tokens = nullptr;  // a2av_set_active_tokens
     int combine_tma = 1;
-    int32_t comb_chunk_bytes = 0, comb_nchunks = 0, comb_stages = 0, comb_nsplit = 1, comb_unroll = 2;
+    int32_t comb_chunk_bytes = 0, comb_nchunks = 0, comb_stages = 0, comb_nsplit = 1, comb_unroll = 2, comb_group = 1;
     bool comb_batch = false;  // combine_batched_kernel (set with few_tokens where rows split into pieces)
     bool few_tokens = false;  // R*T below the combine's warps: the pack triggers the combine's launch early
     int pack_tma = 1;
@@ -255,6 +256,9 @@ __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepco
 __device__ __forceinline__ void grid_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+
+// Bring the line holding p into L2 (no value is read; nothing waits on it).
+__device__ __forceinline__ void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
 __device__ __forceinline__ void st_stream_v4(void *p, const uint4 &v) {
     asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)

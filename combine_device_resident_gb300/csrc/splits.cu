@@ -129,6 +129,10 @@ __global__ void __launch_bounds__(NW * 32) hist_scan_kernel(const HistArgs a) {
     int *cnt = smem + warp * ES;
     for (int e = lane; e < E; e += 32) cnt[e] = 0;
     __syncwarp();
+    // Launched as a programmatic dependent of whatever kernel came before
+    // (the previous call's combine, a router): nothing global is read or
+    // written before its grid has completed.
+    grid_dependency_wait();
     const int w0 = tile * kHistTile + warp * (32 * ROUNDS);
     int key[ROUNDS], rank[ROUNDS];
     int vals[ROUNDS];
@@ -417,19 +421,28 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
     int *xb = wb + R;                    // [E] expert order: rows of expert e on ranks below s
     int *xt = xb + E;                    // [E] expert order: rows of e on all ranks, then e's block start
     constexpr bool by_expert = BY_EXPERT;
-    // the routing loads go out first; the counters are cleared while they fly
-    int vals[kClusterRounds];
-    {
-        const int32_t *idx = a.idx + (size_t)s * A;
+    // Launched as a programmatic dependent of the kernel before it (the
+    // previous call's combine, a router): it is resident early and reads or
+    // writes nothing global before that grid has completed.  Meanwhile it
+    // asks L2 for its routing lines (a prefetch only warms L2, which stays
+    // coherent with the predecessor's writes; the values are loaded after the
+    // wait) and clears its counters.
+    const int32_t *idx = a.idx + (size_t)s * A;
 #pragma unroll
-        for (int r = 0; r < kClusterRounds; ++r) {
-            const int ai = a0 + r * 32 + lane;
-            vals[r] = (r * 32 < chunk && ai < A) ? __ldg(idx + ai) : -1;
-        }
+    for (int r = 0; r < kClusterRounds; ++r) {
+        const int ai = a0 + r * 32 + lane;
+        if (r * 32 < chunk && ai < A && (lane & 31) == 0) prefetch_l2(idx + ai);
     }
     for (int i = tid; i < kClusterWarps * ES; i += kClusterThreads) cnt[i] = 0;
     if (by_expert)
         for (int i = tid; i < 2 * E; i += kClusterThreads) xb[i] = 0;  // xb and xt
+    grid_dependency_wait();
+    int vals[kClusterRounds];
+#pragma unroll
+    for (int r = 0; r < kClusterRounds; ++r) {
+        const int ai = a0 + r * 32 + lane;
+        vals[r] = (r * 32 < chunk && ai < A) ? __ldg(idx + ai) : -1;
+    }
     __syncthreads();
 
     int key[kClusterRounds], rank[kClusterRounds];
@@ -492,7 +505,9 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
                 if (src < s) atomicAdd(&xb[e], c);
             }
         }
-    // no CTA may leave (or reuse) its shared memory until every peer has read it
+    // no CTA may leave (or reuse) its shared memory until every peer has read
+    // it; the barrier also orders this CTA's own threads (rc is written by
+    // some warps above and read by others below)
     cluster_barrier();
 
     // one warp per window: this rank's receive offset and the window total
@@ -607,7 +622,9 @@ SplitsKernel hist_kernel_for(bool write_reo, int route_epl = 0) {
     }
 }
 
-cudaLaunchConfig_t cluster_launch_config(const a2av_plan_s &p, cudaLaunchAttribute *at, cudaStream_t s) {
+// `at` holds two attributes: the cluster shape and (when `pdl`) the
+// programmatic stream serialization the kernels' grid_dependency_wait needs.
+cudaLaunchConfig_t cluster_launch_config(const a2av_plan_s &p, cudaLaunchAttribute *at, cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(p.g.R);
     lc.blockDim = dim3(kClusterThreads);
@@ -617,9 +634,28 @@ cudaLaunchConfig_t cluster_launch_config(const a2av_plan_s &p, cudaLaunchAttribu
     at[0].val.clusterDim.x = p.g.R;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = at;
+    lc.numAttrs = pdl ? 2 : 1;
+    return lc;
+}
+
+// The tiled kernels' launch: grid (tiles, R), programmatic dependent of the
+// kernel before it.
+cudaError_t launch_tiled(SplitsKernel k, const a2av_plan_s &p, int threads, size_t smem, const HistArgs &a,
+                         cudaStream_t s) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(p.g.tiles, p.g.R);
+    lc.blockDim = dim3(threads);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = at;
     lc.numAttrs = 1;
-    return lc;
+    return cudaLaunchKernelEx(&lc, k, a);
 }
 
 }  // namespace
@@ -659,8 +695,8 @@ cudaError_t configure_hist(a2av_plan_s &p) {
         if (e != cudaSuccess) return e;
         const auto kern = cluster_kernel_for(p.g, true);
         // Can a cluster of R such CTAs be resident at all on this device?
-        cudaLaunchAttribute at[1];
-        cudaLaunchConfig_t lc = cluster_launch_config(p, at, nullptr);
+        cudaLaunchAttribute at[2];
+        cudaLaunchConfig_t lc = cluster_launch_config(p, at, nullptr, false);
         int clusters = 0;
         e = cudaOccupancyMaxActiveClusters(&clusters, kern, &lc);
         if (e == cudaSuccess && clusters >= 1) {
@@ -681,16 +717,15 @@ cudaError_t configure_hist(a2av_plan_s &p) {
 
 cudaError_t launch_hist(const a2av_plan_s &p, const HistArgs &a, cudaStream_t s) {
     const bool reo = a.sp.recv_expert_offsets != nullptr;
+    cudaError_t e;
     if (p.splits_small) {
-        cudaLaunchAttribute at[1];
-        cudaLaunchConfig_t lc = cluster_launch_config(p, at, s);
-        cudaError_t e = cudaLaunchKernelEx(&lc, cluster_kernel_for(p.g, reo), a);
-        if (e != cudaSuccess) return e;
+        cudaLaunchAttribute at[2];
+        cudaLaunchConfig_t lc = cluster_launch_config(p, at, s, true);
+        e = cudaLaunchKernelEx(&lc, cluster_kernel_for(p.g, reo), a);
     } else {
-        dim3 grid(p.g.tiles, p.g.R);
-        hist_kernel_for(reo)<<<grid, kHistThreads, hist_smem_bytes(p.g, reo, kHistWarps), s>>>(a);
+        e = launch_tiled(hist_kernel_for(reo), p, kHistThreads, hist_smem_bytes(p.g, reo, kHistWarps), a, s);
     }
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace a2av
@@ -705,9 +740,9 @@ cudaError_t launch_routed_hist(const a2av_plan_s &p, const HistArgs &a, cudaStre
     const int epl = routed_epl(p.g);
     if (!epl) return cudaErrorInvalidValue;
     const bool reo = a.sp.recv_expert_offsets != nullptr;
-    dim3 grid(p.g.tiles, p.g.R);
-    hist_kernel_for(reo, epl)<<<grid, kRoutedWarps * 32, hist_smem_bytes(p.g, reo, kRoutedWarps), s>>>(a);
-    return cudaGetLastError();
+    cudaError_t e =
+        launch_tiled(hist_kernel_for(reo, epl), p, kRoutedWarps * 32, hist_smem_bytes(p.g, reo, kRoutedWarps), a, s);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace a2av

@@ -140,10 +140,11 @@ typedef struct {
                                  (0 = 2 KiB for k >= 4, else min(row, 16 KiB)) */
     int32_t pack_store_lag;   /* TMA pack: row stores that may still read a stage before its refill, 1..8
                                  (0 = 6 for k >= 4, else 2) */
-    int32_t combine_ctas_per_sm;  /* TMA combine: resident CTAs per SM, 1..8 (0 = 4) */
+    int32_t combine_ctas_per_sm;  /* TMA combine: CTAs per SM (1 producer + 8 consumer warps each), 1..8 (0 = 2) */
     int32_t combine_stage_bytes;  /* TMA combine: bytes of the k row chunks per stage, multiple of 16 (0 = 16 KiB) */
     int32_t combine_unroll;       /* vector combine: 16-byte loads per lane and slot per step, 1..8
-                                     (0 = 2 for k <= 2, else 1) */
+                                     (0 = 2 for k <= 2, 1 for k = 4, 4 for k = 8; the slots are then taken
+                                     in groups sized for about 4 loads per lane) */
     int32_t recv_order;           /* A2AV_ORDER_SOURCE (0) or A2AV_ORDER_EXPERT */
 } a2av_config_t;
 
