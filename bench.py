@@ -824,6 +824,41 @@ def main():
     }
     if traffic and dom in sf_kus and sf_kus[dom] > 0:
         split_flush["traffic_frac"] = {dom: round(traffic / (sf_kus[dom] * 1e-6) / 1e9 / peak, 4)}
+    if args.l2 == "flush":
+        # Write-back charged: rows a half leaves dirty in L2 are written back
+        # during the next flush, outside the half's events.  Time [half, then
+        # a flush] and subtract a flush of a clean L2: what remains is the
+        # half plus the write-back of its dirty lines.
+        pre_g = prefixes[len(stages) - 3] if len(stages) >= 3 else g_null
+        wb_graphs = [pre_g, prefixes[len(stages) - 2], g_comb, g_null, None]
+        ev_wb = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(wb_graphs))] for _ in range(KK)]
+        with torch.cuda.stream(stream):
+            for i in range(KK):
+                for j, gr in enumerate(wb_graphs):
+                    flush_l2()
+                    ev_wb[i][2 * j].record(stream)
+                    if gr is not None:
+                        gr.replay()
+                    flush_l2()
+                    ev_wb[i][2 * j + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        wb = [sum(ev_wb[i][2 * j].elapsed_time(ev_wb[i][2 * j + 1]) for i in range(KK)) / KK
+              for j in range(len(wb_graphs))]
+        clean = wb[-1]
+        pre_c, disp_c, comb_c, null_c = (v - clean for v in wb[:4])
+        wb_kus = {names[-2]: 1e3 * (disp_c - pre_c), names[-1]: 1e3 * (comb_c - null_c)}
+        wb_gbs = {n: kbytes[n] / (v * 1e-6) / 1e9 for n, v in wb_kus.items() if v > 0}
+        split_flush["writeback_charged"] = {
+            "dispatch_us": round(1e3 * disp_c, 3), "combine_us": round(1e3 * comb_c, 3),
+            "total_us": round(1e3 * (disp_c + comb_c), 3),
+            "pct_of_peak": round(100 * bytes_step / ((disp_c + comb_c) * 1e-3) / 1e9 / peak, 2),
+            "kernel_us": {n: round(v, 3) for n, v in wb_kus.items()},
+            "kernel_gbs": {n: round(v, 1) for n, v in wb_gbs.items()},
+            "kernel_frac": {n: round(v / peak, 4) for n, v in wb_gbs.items()},
+            "clean_flush_us": round(1e3 * clean, 3),
+            "timing": ("each graph timed together with the flush after it, minus a flush of a clean L2 "
+                       "(the dirty lines a half leaves are written back during that flush)"),
+        }
 
     # ---- warm L2, for workloads whose receive arena fits in L2 ---------------------
     l2_warm = None
