@@ -173,12 +173,13 @@ def ncu_traffic(kernel: str, workload: str):
         d = json.load(open(p))
     except Exception:
         return None
-    ent = d.get("kernels", {}).get(kernel, {})
-    if kernel not in KERNEL_SOURCES or ent.get("source_sha") != kernel_source_hash(kernel):
+    if kernel not in KERNEL_SOURCES:
         return None
-    if ent.get("workload") != workload:
-        return None
-    return ent.get("dram_bytes_per_launch")
+    for ent in d.get("records", []):
+        if (ent.get("kernel") == kernel and ent.get("workload") == workload
+                and ent.get("source_sha") == kernel_source_hash(kernel)):
+            return ent.get("dram_bytes_per_launch")
+    return None
 
 
 # ---------------------------------------------------------------------------

@@ -21,25 +21,31 @@ def test_kernel_hashes_are_distinct_and_stable():
 
 
 def test_traffic_record_is_keyed_on_workload_and_kernel():
-    w2 = "r8-e16-t1024-h5120-top1-uniform"
+    w5 = "r32-e256-t2048-h7168-top8-hot0-zipf1.1-softmax"
     assert bench.ncu_traffic("pack", "no-such-workload") is None
-    assert bench.ncu_traffic("route", w2) is None  # no capture recorded for the router
-    assert bench.ncu_traffic("no-such-kernel", w2) is None
+    assert bench.ncu_traffic("route", w5) is None  # no capture recorded for the router
+    assert bench.ncu_traffic("no-such-kernel", w5) is None
 
 
-def test_traffic_record_per_launch_bytes_add_up():
+def test_traffic_records_add_up_and_match_the_workload():
     import json
     import os
 
+    import workloads as W
+
     d = json.load(open(os.path.join(bench.ROOT, "profiles", "ncu_traffic.json")))
-    for name, ent in d["kernels"].items():
-        live = ent["live"]
-        assert ent["dram_bytes_per_launch"] == live["dram_read_bytes"] + live["dram_write_bytes"], name
-        if "per_launch" in live:  # the mean of the captured launches
-            reads = [r for r, _ in live["per_launch"]]
-            writes = [w_ for _, w_ in live["per_launch"]]
-            assert live["dram_read_bytes"] == sum(reads) // len(reads), name
-            assert live["dram_write_bytes"] == sum(writes) // len(writes), name
+    by_name = {w.name: w for w in W.WORKLOADS.values()}
+    for ent in d["records"]:
+        assert ent["dram_bytes_per_launch"] == ent["dram_read_bytes"] + ent["dram_write_bytes"], ent["kernel"]
+        reads = [r for r, _ in ent["per_launch"]]
+        writes = [w_ for _, w_ in ent["per_launch"]]
+        assert ent["dram_read_bytes"] == sum(reads) // len(reads), ent["kernel"]
+        assert ent["dram_write_bytes"] == sum(writes) // len(writes), ent["kernel"]
+        w = by_name[ent["workload"]]
+        A = w.R * w.T * w.k
+        assert ent["algorithmic_bytes_per_launch"] == w.R * w.T * w.H * 2 * (1 + w.k) + 8 * A
+        # measured DRAM bytes of a full-size launch: within a few % of the algorithmic bytes
+        assert 0.95 < ent["dram_bytes_per_launch"] / ent["algorithmic_bytes_per_launch"] < 1.02, ent["kernel"]
 
 
 def test_threaded_oracle_step_equals_one_thread_run():
