@@ -935,7 +935,10 @@ def main():
     ev_out = [torch.cuda.Event() for _ in range(2)]
     n_pipe = args.e2e_steps
 
-    def pipelined(n):
+    def pipelined(n, compute=True):
+        """Time per step of the double-buffered loop; compute=False leaves the
+        graph replays out (the same copies, streams and events: the host
+        link's floor for a step)."""
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
         t0.record(s_in)
@@ -952,7 +955,8 @@ def main():
                 stream.wait_event(ev_in[b])
                 if i >= 2:
                     stream.wait_event(ev_out[b])  # step i-2's result has left this set
-                gr.replay()
+                if compute:
+                    gr.replay()
                 ev_comp[b].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_comp[b])
@@ -968,27 +972,8 @@ def main():
     pipelined(4)  # warm-up
     pipe_ms = max_over_ranks(pipelined(n_pipe))
 
-    def copies_only(n):
-        """The same per-step copies with no kernels: inputs in on s_in, the
-        result out on s_out, concurrently -- the host link's floor for a step."""
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        t0.record(s_in)
-        s_out.wait_stream(s_in)
-        for i in range(n):
-            ins, ob, _ = sets[i % 2]
-            with torch.cuda.stream(s_in):
-                for dst, src in zip(ins, in_pins):
-                    dst.copy_(src, non_blocking=True)
-            with torch.cuda.stream(s_out):
-                outs_pin[i % 2].copy_(ob, non_blocking=True)
-        s_in.wait_stream(s_out)
-        t1.record(s_in)
-        t1.synchronize()
-        return t0.elapsed_time(t1) / n
-
-    copies_only(2)
-    link_ms = max_over_ranks(copies_only(n_pipe))
+    pipelined(2, compute=False)
+    link_ms = max_over_ranks(pipelined(n_pipe, compute=False))
     serial_t = max_over_ranks(sum(serial_ms) / len(serial_ms))
     e2e = {"value": round(whole_job(bytes_step, w.R * t_active, pipe_ms, world)["gbs"], 2), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(pipe_ms, 4),

@@ -347,6 +347,65 @@ def test_graph_replay_with_new_routing_each_time(wid, T, H):
     assert plan.read_status() == 0
 
 
+@pytest.mark.parametrize("wid,T,H,flags,graph", [(3, 256, 1032, 0, False), (1, None, None, 0, True),
+                                                 (2, 700, 264, 2, False), (5, 90, 136, 0, True),
+                                                 (4, 300, 136, 4, False)],
+                         ids=["cluster", "cluster-graph", "tiled", "tiled-top8-graph", "tma-combine"])
+def test_back_to_back_calls_reusing_buffers(wid, T, H, flags, graph):
+    # Consecutive dispatch+combine calls on one stream, with no host sync
+    # between them, reuse the splits arrays, slot_map and the arena.  Each
+    # splits kernel is a programmatic dependent of the previous call's combine
+    # and may be resident before it ends; nothing it writes may reach the
+    # buffers the combine still reads.  Each call has its own routing and its
+    # own out, and every out must match the oracle.
+    import torch
+    from combine_device_resident_gb300 import Plan
+
+    w = W.WORKLOADS[wid] if T is None else W.WORKLOADS[wid].scaled(T=T, H=H)
+    dev = P.device()
+    plan = Plan(w.R, w.E, w.T, w.H, w.k, w.window_mode, w.window_rows, device=dev, flags=flags)
+    x = W.make_x(w, 0, device=dev)
+    recv, slot_map, _ = plan.new_buffers()
+    sp = plan.new_splits()
+    n = 6
+    rgs = [W.make_routing_gate(w, 200 + i) for i in range(n)]
+    idx = [torch.from_numpy(r["topk_idx"]).to(dev) for r in rgs]
+    gate = [torch.from_numpy(r["gate_w"]).to(dev) for r in rgs]
+    outs = [torch.full((w.R, w.T, w.H), 7.0, dtype=torch.bfloat16, device=dev) for _ in range(n)]
+    plan.read_status(clear=True)
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+
+    def calls():
+        for i in range(n):
+            plan.dispatch(x, idx[i], sp, recv, slot_map, stream=s)
+            plan.combine(recv, gate[i], slot_map, outs[i], stream=s)
+
+    if graph:
+        with torch.cuda.stream(s):
+            calls()  # warm-up outside capture
+        torch.cuda.synchronize()
+        for o in outs:
+            o.fill_(7.0)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            calls()
+        g.replay()
+    else:
+        with torch.cuda.stream(s):
+            calls()
+    torch.cuda.synchronize()
+    xh = P.bits(x)
+    for i in range(n):
+        ref = oracle.run_all(w.R, w.E, xh, rgs[i]["topk_idx"], rgs[i]["gate_w"], w.window_mode, w.window_rows)
+        np.testing.assert_array_equal(P.bits(outs[i]), ref["out"], err_msg=f"call {i}")
+    np.testing.assert_array_equal(slot_map.cpu().numpy(), ref["slot_map"])  # the last call's
+    P.check_splits(sp.to_numpy(), ref["splits"])
+    assert plan.read_status() == 0
+    plan.close()
+
+
 def test_plans_with_different_shapes_coexist():
     # Kernel attributes are per kernel, not per plan: a plan made later with a
     # small row must not break an earlier plan with a large one.
