@@ -157,6 +157,7 @@ struct a2av_plan_s {
     bool few_tokens = false;  // R*T below the combine's warps: the pack triggers the combine's launch early
     int pack_tma = 1;
     int32_t pack_chunk_bytes = 0, pack_nchunks = 0, pack_stages = 0, pack_lag = 1;
+    int pack_stream_rows = 0;  // the pack stores its rows evict-first (see configure_pack)
     int64_t launches = 0;
     int64_t wait_polls = a2av::kWaitLimit;  // main-loop wait limit of the TMA kernels (a2av_set_wait_limit)
     // 1: the last splits launch left final rows in slot_map (cluster kernel);
@@ -321,6 +322,12 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
+}
+// bulk_store with an L2 cache policy for the destination lines.
+__device__ __forceinline__ void bulk_store_hint(void *dst, const void *src_smem, uint32_t bytes, uint64_t policy) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+                 "r"(smem_u32(src_smem)), "r"(bytes), "l"(policy)
+                 : "memory");
 }
 // bulk_load with an L2 cache policy for the source lines.
 __device__ __forceinline__ void bulk_load_hint(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar,

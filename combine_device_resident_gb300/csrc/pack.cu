@@ -101,10 +101,13 @@ __host__ __device__ constexpr size_t pack_tail_bytes(int stages) {
 // stores of every chunk, the lanes compute the destination rows of the next
 // batch of BT = 32/k tokens (lane l: token l / k, slot l % k).  COUNTED:
 // per-rank active token counts (a.num_tokens); PADDED: stores go to the
-// padded send buffer.  Both are compile-time, so the plain instantiation
-// keeps the shortest issue loop (measured: the issuing lane's scalar work
-// between copy-engine waits shows up directly in the kernel's time).
-template <bool COUNTED, bool PADDED>
+// padded send buffer; STREAM: the row stores carry an evict-first L2 policy
+// (plans whose rows cannot stay in L2 until the combine and whose pack is
+// write-dominated, see configure_pack).  All compile-time, so the plain
+// instantiation keeps the shortest issue loop (measured: the issuing lane's
+// scalar work between copy-engine waits shows up directly in the kernel's
+// time).
+template <bool COUNTED, bool PADDED, bool STREAM>
 __global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     // Latency-bound calls (few tokens): the combine, a programmatic
@@ -249,7 +252,12 @@ __global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
         if (lane == 0) fence_proxy_async_smem();
         for (int j = 0; j < g.k; ++j) {
             const int32_t rj = __shfl_sync(kFull, cur, lb * g.k + j);
-            if (lane == 0 && rj >= 0) bulk_store(recv + (size_t)rj * rowb + off, smem + (size_t)st * CH, bytes);
+            if (lane == 0 && rj >= 0) {
+                if (STREAM)
+                    bulk_store_hint(recv + (size_t)rj * rowb + off, smem + (size_t)st * CH, bytes, x_policy);
+                else
+                    bulk_store(recv + (size_t)rj * rowb + off, smem + (size_t)st * CH, bytes);
+            }
         }
         if (lane == 0) {
             bulk_commit();
@@ -370,6 +378,19 @@ __global__ void __launch_bounds__(256) exchange_padded_kernel(const ExchangeArgs
 cudaError_t configure_pack(a2av_plan_s &p) {
     const size_t rowb = (size_t)p.g.H * 2;
     {
+        // Evict-first row stores: when the rows a call writes cannot stay in
+        // L2 until the combine and the pack is write-dominated (k >= 4).
+        // Measured, L2 flushed: r32 E256 T2048 H7168 top-8 pack 1,346 ->
+        // 1,326 us, step 2,652 -> 2,627 us; r16 E128 T4096 top-2 pack
+        // unchanged (317 us) while the combine in the step lost 4.5 us (it
+        // finds fewer of the last rows in L2); the hinted store with the
+        // normal policy on L2-sized calls cost r8 E128 T256 0.15 us.
+        int l2 = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, p.cfg.device);
+        if (e != cudaSuccess) return e;
+        p.pack_stream_rows = p.g.k >= 4 && (double)p.g.R * p.g.T * p.g.k * (double)rowb > (double)l2 ? 1 : 0;
+    }
+    {
         int per_sm = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, exchange_padded_kernel, 256, 0);
         if (e != cudaSuccess) return e;
@@ -421,8 +442,10 @@ cudaError_t configure_pack(a2av_plan_s &p) {
     p.pack.grid = p.num_sms * ctas_per_sm;
     // The attribute is a per-kernel cap shared by every plan: raise it to the
     // device maximum (never lower it to this plan's size).
-    for (auto kern : {pack_tma_kernel<false, false>, pack_tma_kernel<false, true>, pack_tma_kernel<true, false>,
-                      pack_tma_kernel<true, true>}) {
+    for (auto kern : {pack_tma_kernel<false, false, false>, pack_tma_kernel<false, true, false>,
+                      pack_tma_kernel<true, false, false>, pack_tma_kernel<true, true, false>,
+                      pack_tma_kernel<false, false, true>, pack_tma_kernel<false, true, true>,
+                      pack_tma_kernel<true, false, true>, pack_tma_kernel<true, true, true>}) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
         if (e != cudaSuccess) return e;
     }
@@ -446,8 +469,12 @@ cudaError_t launch_pack(const a2av_plan_s &p, const PackArgs &a, cudaStream_t s)
         b.stages = p.pack_stages;
         b.lag = p.pack_lag;
         const bool counted = b.num_tokens != nullptr, padded = b.padded_tk != 0;
-        auto kern = counted ? (padded ? pack_tma_kernel<true, true> : pack_tma_kernel<true, false>)
-                            : (padded ? pack_tma_kernel<false, true> : pack_tma_kernel<false, false>);
+        auto kern = p.pack_stream_rows
+                        ? (counted ? (padded ? pack_tma_kernel<true, true, true> : pack_tma_kernel<true, false, true>)
+                                   : (padded ? pack_tma_kernel<false, true, true> : pack_tma_kernel<false, false, true>))
+                        : (counted ? (padded ? pack_tma_kernel<true, true, false> : pack_tma_kernel<true, false, false>)
+                                   : (padded ? pack_tma_kernel<false, true, false>
+                                             : pack_tma_kernel<false, false, false>));
         e = launch_pdl(kern, p.pack.grid, p.pack.block, p.pack.smem, s, b);
     } else {
         e = launch_pdl(pack_lsu_kernel<kLsuUnroll>, p.pack.grid, p.pack.block, 0, s, b);

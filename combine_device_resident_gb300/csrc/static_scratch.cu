@@ -46,6 +46,7 @@ struct ShapeEntry {
     a2av::LaunchShape hist, pack;
     int splits_small = 0;
     int32_t pack_chunk_bytes = 0, pack_nchunks = 0, pack_stages = 0, pack_lag = 1;
+    int pack_stream_rows = 0;
 };
 constexpr int kShapeCache = 32;
 ShapeEntry g_shapes[kShapeCache];
@@ -94,6 +95,7 @@ cudaError_t prepare(a2av_plan_s &p, int32_t **scratch) {
             p.pack_nchunks = s.pack_nchunks;
             p.pack_stages = s.pack_stages;
             p.pack_lag = s.pack_lag;
+            p.pack_stream_rows = s.pack_stream_rows;
             return cudaSuccess;
         }
     }
@@ -111,6 +113,7 @@ cudaError_t prepare(a2av_plan_s &p, int32_t **scratch) {
     s.pack_nchunks = p.pack_nchunks;
     s.pack_stages = p.pack_stages;
     s.pack_lag = p.pack_lag;
+    s.pack_stream_rows = p.pack_stream_rows;
     return cudaSuccess;
 }
 
