@@ -33,6 +33,15 @@ def test_workload_parity(wid, T, H):
     P.full_parity(w)
 
 
+@pytest.mark.parametrize("wid,T,H", [(5, 160, 2056)])
+def test_rows_beyond_l2_parity(wid, T, H):
+    # Top-8 calls whose rows exceed the L2 (168 MB here) run the
+    # pack with evict-first row stores and the combine with evict-first
+    # gathers; element-by-element parity on every row and output.
+    g = P.full_parity(W.WORKLOADS[wid].scaled(T=T, H=H))
+    np.testing.assert_array_equal(g["out"], g["ref"]["out"])
+
+
 @pytest.mark.parametrize("wid", [2, 3])
 def test_workload_parity_full_hidden(wid):
     # the real row sizes (H=5120) on a few hundred tokens per rank
