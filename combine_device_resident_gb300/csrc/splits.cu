@@ -12,11 +12,14 @@
 //
 // Cluster kernel (R <= 16 ranks, T*k <= 8192): one CTA per rank, the R CTAs
 // form one thread-block cluster.  CTA s counts rank s, scans its counts in
-// shared memory, and after a cluster barrier reads every other rank's send
-// offsets straight out of that rank's shared memory (distributed shared
-// memory) to get the received counts, receive offsets and window bases.  It
-// then writes the final arena row of each of its assignments into slot_map.
-// No global atomics, fences, or waits beyond the hardware cluster barrier.
+// shared memory, and writes its count to every window straight into the
+// shared memory of every other CTA (distributed shared memory); after the
+// next cluster barrier each CTA holds all R x R counts and derives the
+// receive offsets and window bases itself.  (The expert receive order also
+// needs every rank's per-expert counts, which it reads from the peers'
+// shared memory instead.)  It then writes the final arena row of each of its
+// assignments into slot_map.  No global atomics, fences, or waits beyond the
+// hardware cluster barrier.
 //
 // Tiled kernel (any shape): grid (tiles, R), one tile of kHistTile
 // assignments per CTA.  The last CTA of a rank to finish (atomic ticket, no
@@ -397,6 +400,9 @@ __device__ __forceinline__ int ld_dsmem(uint32_t addr) {
     asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
+__device__ __forceinline__ void st_dsmem(uint32_t addr, int v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 
 // BY_EXPERT: the expert-grouped receive order; WRITE_REO: fill
 // splits.recv_expert_offsets.  Both compile-time, so the plain source-order
@@ -490,13 +496,28 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
     // (send_counts, send_offsets and recv_expert_counts are stored after the
     // cluster barriers: a barrier's release would otherwise wait for them)
 
-    // every rank's send offsets are now in its CTA's shared memory
-    cluster_barrier();
-    for (int p = tid; p < R * R; p += kClusterThreads) {
-        const int d = p / R, src = p - d * R;
-        rc[p] = ld_dsmem(peer_smem(so + (d + 1) * epr, src)) - ld_dsmem(peer_smem(so + d * epr, src));
-    }
-    if (by_expert)  // one (source, expert) pair per thread, summed with shared-memory atomics
+    if (!by_expert) {
+        // Push: this rank's count to every window d goes into rc[d][s] of
+        // every peer CTA, so no remote load sits between the two barriers.
+        // The first makes sure every peer CTA has started (its shared memory
+        // may be written); nothing reads a peer's shared memory after the
+        // second.
+        cluster_barrier();
+        for (int p = tid; p < R * R; p += kClusterThreads) {
+            const int peer = p / R, d = p - peer * R;
+            st_dsmem(peer_smem(rc + d * R + s, peer), so[(d + 1) * epr] - so[d * epr]);
+        }
+        // the release makes the pushes visible to every peer's acquire; it
+        // also orders this CTA's own threads (rc is read by other warps below)
+        cluster_barrier();
+    } else {
+        // every rank's send offsets are now in its CTA's shared memory
+        cluster_barrier();
+        for (int p = tid; p < R * R; p += kClusterThreads) {
+            const int d = p / R, src = p - d * R;
+            rc[p] = ld_dsmem(peer_smem(so + (d + 1) * epr, src)) - ld_dsmem(peer_smem(so + d * epr, src));
+        }
+        // one (source, expert) pair per thread, summed with shared-memory atomics
         for (int p = tid; p < R * E; p += kClusterThreads) {
             const int src = p / E, e = p - src * E;
             const int c = ld_dsmem(peer_smem(so + e + 1, src)) - ld_dsmem(peer_smem(so + e, src));
@@ -505,10 +526,10 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
                 if (src < s) atomicAdd(&xb[e], c);
             }
         }
-    // no CTA may leave (or reuse) its shared memory until every peer has read
-    // it; the barrier also orders this CTA's own threads (rc is written by
-    // some warps above and read by others below)
-    cluster_barrier();
+        // no CTA may leave (or reuse) its shared memory until every peer has
+        // read it; the barrier also orders this CTA's own threads
+        cluster_barrier();
+    }
 
     // one warp per window: this rank's receive offset and the window total
     if (warp < R) {
