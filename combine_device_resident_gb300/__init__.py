@@ -18,6 +18,7 @@ from .binding import (  # noqa: F401
     FLAG_SPLITS_TILED,
     FLAG_COMBINE_TMA,
     FLAG_ROUTE_FUSED,
+    FLAG_ROUTE_WARP,
     ORDER_EXPERT,
     ORDER_SOURCE,
     Plan,

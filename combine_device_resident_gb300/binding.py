@@ -32,6 +32,7 @@ FLAG_PACK_LSU = 1 << 0
 FLAG_SPLITS_TILED = 1 << 1
 FLAG_COMBINE_TMA = 1 << 2
 FLAG_ROUTE_FUSED = 1 << 3
+FLAG_ROUTE_WARP = 1 << 4
 
 # Every function the header declares, for load checks.
 EXPORTED = [

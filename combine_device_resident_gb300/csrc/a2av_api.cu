@@ -87,7 +87,7 @@ a2av_status_t a2av_config_check(const a2av_config_t *c) {
     }
     if (c->device < 0) return A2AV_ERR_INVALID_ARG;
     if (c->flags & ~(uint32_t)(A2AV_FLAG_PACK_LSU | A2AV_FLAG_SPLITS_TILED | A2AV_FLAG_COMBINE_TMA |
-                               A2AV_FLAG_ROUTE_FUSED))
+                               A2AV_FLAG_ROUTE_FUSED | A2AV_FLAG_ROUTE_WARP))
         return A2AV_ERR_INVALID_ARG;
     if (c->pack_store_lag < 0 || c->pack_store_lag > 8) return A2AV_ERR_INVALID_ARG;
     if (c->combine_ctas_per_sm < 0 || c->combine_ctas_per_sm > 8) return A2AV_ERR_INVALID_ARG;
@@ -380,6 +380,9 @@ a2av_status_t a2av_route(a2av_plan_t p, const float *logits, int32_t *topk_idx, 
     a.logits = logits;
     a.idx = topk_idx;
     a.gate = gate_w;
+    a.status = p->status;
+    a.wait_polls = p->wait_polls;
+    a.rsw = 0;  // set by launch_route for the lane-per-token kernel
     cudaError_t e = a2av::launch_route(*p, a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "route kernel launch");
     p->launches += 1;

@@ -88,6 +88,9 @@ struct RouteArgs {
     const float *logits;  // [R][T][E]
     int32_t *idx;         // [R][T][k]
     float *gate;          // [R][T][k]
+    uint32_t *status;     // device status word (wait give-up bit)
+    int64_t wait_polls;   // mbarrier wait limit of the lane-per-token kernel
+    int32_t rsw;          // its padded shared-memory row stride, in floats
 };
 
 struct ExchangeArgs {
@@ -148,7 +151,7 @@ struct a2av_plan_s {
     int32_t *rank_total = nullptr;
     uint32_t *counters = nullptr;
     uint32_t *status = nullptr;
-    a2av::LaunchShape hist, pack, combine, scale, exchange, route;
+    a2av::LaunchShape hist, pack, combine, scale, exchange, route, route_lane;
     int splits_small = 0;  // 1: one-CTA splits kernel that writes final rows
     const int32_t *num_tokens = nullptr;  // a2av_set_active_tokens
     int combine_tma = 1;
@@ -158,6 +161,8 @@ struct a2av_plan_s {
     int pack_tma = 1;
     int32_t pack_chunk_bytes = 0, pack_nchunks = 0, pack_stages = 0, pack_lag = 1;
     int pack_stream_rows = 0;  // the pack stores its rows evict-first (see configure_pack)
+    int route_lane_kmax = 0;   // lane-per-token router instantiation (0: the warp-per-token kernel)
+    int32_t route_lane_rsw = 0;  // its padded row stride in floats
     int64_t launches = 0;
     int64_t wait_polls = a2av::kWaitLimit;  // main-loop wait limit of the TMA kernels (a2av_set_wait_limit)
     // 1: the last splits launch left final rows in slot_map (cluster kernel);

@@ -123,6 +123,8 @@ enum {
     A2AV_FLAG_COMBINE_TMA = 1u << 2,  /* combine through TMA bulk copies into shared memory (default: vector gathers) */
     A2AV_FLAG_ROUTE_FUSED = 1u << 3,  /* a2av_route_splits: the router inside the tiled histogram kernel (default: the
                                          router kernel, then the splits kernel -- measured faster, see the call) */
+    A2AV_FLAG_ROUTE_WARP = 1u << 4,   /* a2av_route: one warp per token on every shape (default: one lane per token
+                                         where E % 4 == 0, k <= 8 and the logits are 16-byte aligned; same results) */
 };
 
 typedef struct {

@@ -57,11 +57,12 @@ def _cfg(**kw):
 def test_config_check_host_only(lib):
     ok = [_cfg(), _cfg(R=1, E=1, T=1, H=8, k=1), _cfg(R=64, E=2048, T=3, H=8, k=32),
           _cfg(window_mode="fixed", window_rows=100), _cfg(window_mode="padded"), _cfg(recv_order="expert"),
-          _cfg(window_mode="fixed", window_rows=100, recv_order="expert"), _cfg(flags=1 << 3)]
+          _cfg(window_mode="fixed", window_rows=100, recv_order="expert"), _cfg(flags=1 << 3), _cfg(flags=1 << 4),
+          _cfg(flags=(1 << 3) | (1 << 4))]
     bad = [_cfg(R=0), _cfg(R=65, E=130), _cfg(E=12, R=8), _cfg(E=4096, R=8), _cfg(H=12), _cfg(H=0), _cfg(k=0),
            _cfg(k=33), _cfg(T=0), _cfg(window_mode=3), _cfg(window_mode="fixed", window_rows=-1),
            _cfg(R=64, E=64, T=65536, k=8, window_mode="padded"),
-           _cfg(R=64, E=64, T=1 << 20, k=32), _cfg(flags=1 << 7), _cfg(flags=1 << 4), _cfg(pack_stage_bytes=24),
+           _cfg(R=64, E=64, T=1 << 20, k=32), _cfg(flags=1 << 7), _cfg(flags=1 << 5), _cfg(pack_stage_bytes=24),
            _cfg(pack_ctas_per_sm=9), _cfg(recv_order=2), _cfg(recv_order=-1),
            _cfg(window_mode="padded", recv_order="expert")]
     for c in ok:

@@ -658,6 +658,78 @@ def test_router_then_dispatch_and_combine(wid, T, H):
     assert plan.read_status() == 0
 
 
+def _adversarial_logits(w, seed, dev):
+    """Seeded Gaussian logits with rows built to reach every path of the
+    lane-per-token router: ties across the k-th place, exactly 32 and 33
+    logits at the top (the candidate list holds 32), infinities, NaN, -0 and
+    denormals, and rows where a group of 16-byte units holds only -inf."""
+    import torch
+
+    lg = W.make_logits(w, seed, device=dev)
+    E, T = w.E, w.T
+    rows = [lg[0, t] for t in range(min(T, 9))]
+    if len(rows) > 0:
+        rows[0][:] = 3.0                               # all equal
+    if len(rows) > 1:
+        rows[1][: min(E, 32)] = 7.0                    # 32 at the top: a full list
+    if len(rows) > 2:
+        rows[2][: min(E, 33)] = 7.0                    # 33: one over, whole-row fallback
+    if len(rows) > 3:
+        rows[3][::3] = 1.5                             # ties straddling the k-th place
+    if len(rows) > 4:
+        rows[4][E // 2] = float("inf")
+        rows[4][E - 1] = float("inf")                  # two +inf
+    if len(rows) > 5:
+        rows[5][::2] = float("nan")                    # NaN counts as -inf
+    if len(rows) > 6:
+        rows[6][:] = float("-inf")
+        rows[6][E - 1] = -0.0                          # one finite logit
+    if len(rows) > 7:
+        rows[7][:] = 1e-40                             # denormals and signed zeros
+        rows[7][1::4] = -0.0
+        rows[7][2::4] = 0.0
+    if len(rows) > 8 and E >= 8:
+        rows[8][: E // 2] = float("-inf")              # half the groups' units start -inf
+    return lg
+
+
+@pytest.mark.parametrize("R,T,E,k", [(2, 300, 4, 1), (8, 512, 16, 1), (16, 257, 128, 2), (4, 130, 256, 8),
+                                     (4, 70, 8, 8), (2, 65, 12, 4), (2, 40, 512, 8), (1, 33, 64, 3),
+                                     (4, 31, 256, 7)])
+def test_router_lane_kernel_equals_warp_kernel(R, T, E, k):
+    # The lane-per-token router (the default on these shapes) against the
+    # warp-per-token one (A2AV_FLAG_ROUTE_WARP) and against the oracle: same
+    # ids, same gate bits.  A logits array 4 bytes off a 16-byte boundary
+    # makes the default plan take the warp kernel too.
+    import torch
+    from combine_device_resident_gb300 import FLAG_ROUTE_WARP, Plan
+
+    dev = P.device()
+    w = W.Workload("router", R=R, E=E, T=T, H=8, k=k)
+    logits = _adversarial_logits(w, 11 + E, dev)
+    outs = []
+    for flags, shift in ((0, 0), (FLAG_ROUTE_WARP, 0), (0, 1)):
+        plan = Plan(R, E, T, 8, k, device=dev, flags=flags)
+        if shift:
+            buf = torch.empty(logits.numel() + 4, dtype=torch.float32, device=dev)
+            lg = buf[shift:shift + logits.numel()].view(R, T, E)
+            lg.copy_(logits)
+            assert lg.data_ptr() % 16 != 0
+        else:
+            lg = logits
+        idx = torch.full((R, T, k), -9, dtype=torch.int32, device=dev)
+        gate = torch.zeros((R, T, k), dtype=torch.float32, device=dev)
+        plan.route(lg, idx, gate)
+        torch.cuda.synchronize()
+        assert plan.read_status() == 0
+        outs.append((idx.cpu().numpy(), gate.cpu().numpy().view(np.uint32)))
+    for i in (1, 2):
+        np.testing.assert_array_equal(outs[0][0], outs[i][0])
+        np.testing.assert_array_equal(outs[0][1], outs[i][1])
+    ridx, _ = oracle.route(logits.cpu().numpy(), k)
+    np.testing.assert_array_equal(outs[0][0], ridx)
+
+
 def test_router_leaves_inactive_tokens_alone():
     import torch
     from combine_device_resident_gb300 import Plan
