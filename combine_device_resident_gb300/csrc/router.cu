@@ -7,27 +7,28 @@
 //
 // Two kernels, the plan picks one (A2AV_FLAG_ROUTE_WARP: always the second).
 //
-// Lane-per-token kernel (E a multiple of 4, k <= 8, rows that fit shared
-// memory; the default): a warp takes 32 consecutive tokens and brings their
-// logit rows into shared memory, one bulk copy per row, rows padded so that
-// lane i reading row i with 16-byte loads touches distinct banks.  Each lane
-// then selects its own token's k largest in three passes over its row:
-//   1. the maxima of 2*KMAX disjoint groups of the row (16-byte unit j in
-//      group j % (2*KMAX)), KMAX >= k.  tau, the KMAX-th largest of them,
-//      bounds the k-th largest logit from below: the group maxima are
-//      distinct elements, KMAX of them >= tau.  (Sort both halves of the
-//      maxima; the KMAX-th largest of all is min_i max(A_i, B_{KMAX-1-i}),
-//      the first step of a bitonic merge.)
-//   2. the ids of the logits >= tau, in ascending id order, into the lane's
-//      candidate list (about 10 per token on Gaussian logits with E = 256,
-//      k = 8, at most 16 in a warp; with KMAX groups and their minimum it
-//      was 21, and 8% of the lanes overflowed the list);
+// Lane kernel (E a multiple of 4, k <= 8, rows that fit shared memory; the
+// default): P lanes per token (4; 2 for k = 2), 32/P tokens per warp task,
+// four independent warps per CTA.  A task's logit rows come into shared
+// memory by one bulk copy each, padded so that the 8 lanes of a quarter warp
+// read 8 distinct bank groups; lane share r of a token holds 16-byte units
+// r, r+P, ... of its row.  Per share, in three passes over it:
+//   1. a lower bound tau of the k-th largest logit: the (KMAX/P)-th largest
+//      of the share's 2*KMAX/P group maxima, then the smallest over the
+//      token's P shares -- KMAX >= k distinct elements are >= tau.  (For
+//      k = 1, P > KMAX: the row's maximum.)
+//   2. the ids of the share's logits >= tau, ascending, into a candidate
+//      list (about 4 per share on Gaussian logits with E = 256, k = 8: 16
+//      per token; a bound from the minimum of KMAX group maxima let 21 per
+//      token through, and 8% of the lists overflowed);
 //   3. a sorted insertion of the candidates into KMAX registers, where only
-//      a strictly greater key moves up: of equal logits the lower id stays
-//      ahead, as it arrived first.
-// A lane whose list overflows, or whose tau is -infinity (a group of only
-// -infinity or NaN logits), inserts every logit of its row instead.  Gates
-// are computed as in route_token, so both kernels give the same bits.
+//      a strictly greater key moves up (of equal logits the lower id, which
+//      arrived first, stays ahead).
+// A share whose list overflows, or whose tau is -infinity (a group of only
+// -infinity or NaN logits), inserts every logit it holds instead.  Bitonic
+// merges over xor shuffles then give every lane of the token the token's
+// best KMAX, by key and then lower id.  Gates are computed as in
+// route_token, so the two kernels give the same bits.
 //
 // Warp-per-token kernel (any shape): route_token in route_select.cuh, one
 // warp per token, grid-stride over all R*T tokens.
@@ -109,86 +110,153 @@ __device__ __forceinline__ void sort_desc(float (&v)[N]) {
         }
 }
 
-// Row stride in floats: a multiple of 4 with an odd number of 16-byte units,
-// so lanes reading the same unit of their own rows hit distinct banks.
-int lane_row_stride(int E) {
-    const int u = E / 4;
-    return 4 * (u + ((u & 1) ? 2 : 1));
+// Composite order of the selection: a larger key first, of equal keys the
+// lower id.
+__device__ __forceinline__ bool ranks_before(uint32_t ka, int ia, uint32_t kb, int ib) {
+    return ka > kb || (ka == kb && ia < ib);
 }
-size_t lane_smem_bytes(int E) {
-    return (size_t)32 * lane_row_stride(E) * sizeof(float) + (size_t)(kLaneCap + 1) * 32 * sizeof(uint16_t) +
-           sizeof(uint64_t);
+
+// Merge this lane's sorted list with that of lane ^ mask, keeping the best
+// KMAX in order; both lanes end with the same list.  The better of a[j] and
+// b[KMAX-1-j] for every j are the best KMAX of the two (a bitonic
+// sequence); half-cleaners then sort them.
+template <int KMAX>
+__device__ __forceinline__ void merge_lists(uint32_t (&kk)[KMAX], int (&ii)[KMAX], int mask) {
+    uint32_t bk[KMAX];
+    int bi[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        bk[j] = __shfl_xor_sync(kAllLanes, kk[j], mask);
+        bi[j] = __shfl_xor_sync(kAllLanes, ii[j], mask);
+    }
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        const uint32_t ok = bk[KMAX - 1 - j];
+        const int oi = bi[KMAX - 1 - j];
+        if (!ranks_before(kk[j], ii[j], ok, oi)) {
+            kk[j] = ok;
+            ii[j] = oi;
+        }
+    }
+#pragma unroll
+    for (int d = KMAX / 2; d >= 1; d >>= 1)
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+            if ((j & d) == 0 && ranks_before(kk[j + d], ii[j + d], kk[j], ii[j])) {
+                const uint32_t tk = kk[j];
+                const int ti = ii[j];
+                kk[j] = kk[j + d];
+                ii[j] = ii[j + d];
+                kk[j + d] = tk;
+                ii[j + d] = ti;
+            }
+}
+
+// Lanes per token: KMAX >= P lets every lane bound its share with its own
+// group maxima (k = 1 takes the maximum over the token's lanes instead).
+__host__ __device__ constexpr int lanes_per_token(int kmax) { return kmax >= 4 ? 4 : kmax == 2 ? 2 : 4; }
+constexpr int kRouteWarps = 4;  // warps per CTA, each on its own tasks and shared memory
+
+// Row stride in 16-byte units: at least E/4 and congruent to P mod 2P, so
+// the 8 lanes of a quarter warp (8/P tokens, P lanes each on consecutive
+// units of its row) read 8 distinct bank groups.
+int lane_row_units(int E, int P) {
+    int S = E / 4;
+    while (S % (2 * P) != P) ++S;
+    return S;
+}
+// One warp's shared memory: 32/P rows, the candidate lists, the barrier.
+size_t lane_warp_bytes(int E, int P) {
+    return (size_t)(32 / P) * lane_row_units(E, P) * 16 + (size_t)(kLaneCap + 1) * 32 * sizeof(uint16_t) + 16;
 }
 
 template <int KMAX>
-__global__ void __launch_bounds__(32) route_lane_kernel(const RouteArgs a) {
+__global__ void __launch_bounds__(32 * kRouteWarps) route_lane_kernel(const RouteArgs a) {
+    constexpr int P = lanes_per_token(KMAX);
+    constexpr int TPW = 32 / P;  // tokens per warp task
     extern __shared__ __align__(16) unsigned char sm[];
     const Geometry &g = a.g;
-    const int E = g.E, k = g.k, lane = threadIdx.x, rsw = a.rsw;
-    float *stage = reinterpret_cast<float *>(sm);                            // [32][rsw]
-    uint16_t *lst = reinterpret_cast<uint16_t *>(stage + (size_t)32 * rsw);  // [kLaneCap + 1][32]
-    uint64_t *bar = reinterpret_cast<uint64_t *>(lst + (kLaneCap + 1) * 32);
+    const int E = g.E, k = g.k, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S4 = a.rsw;  // row stride in floats
+    const size_t wbytes = (size_t)TPW * S4 * 4 + (size_t)(kLaneCap + 1) * 32 * sizeof(uint16_t) + 16;
+    unsigned char *base = sm + warp * wbytes;
+    float *stage = reinterpret_cast<float *>(base);                                // [TPW][S4]
+    uint16_t *lst = reinterpret_cast<uint16_t *>(base + (size_t)TPW * S4 * 4);   // [kLaneCap + 1][32]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(base + wbytes - 16);
     if (lane == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
     }
     __syncwarp();
-    const float *row = stage + (size_t)lane * rsw;
-    const float4 *row4 = reinterpret_cast<const float4 *>(row);
+    const int t = lane / P, r = lane - t * P;  // this lane: token t of the task, share r of its row
+    const float4 *row4 = reinterpret_cast<const float4 *>(stage + (size_t)t * S4);
+    const float *row = stage + (size_t)t * S4;
     uint16_t *mine = lst + lane;
     const int nu = E / 4;
     const uint32_t rowb = (uint32_t)E * 4;
     const int ntok = g.R * g.T;
-    const int ntask = (ntok + 31) / 32;
+    const int ntask = (ntok + TPW - 1) / TPW;
     uint32_t phase = 0;
-    for (int task = blockIdx.x; task < ntask; task += gridDim.x) {
-        const int u = task * 32 + lane;
+    for (int task = blockIdx.x * kRouteWarps + warp; task < ntask; task += gridDim.x * kRouteWarps) {
+        const int u = task * TPW + t;
         bool act = u < ntok;
         if (act) {
             const int s = u / g.T;
             act = u - s * g.T < active_tokens(a.num_tokens, s, g.T);
         }
-        const uint32_t am = __ballot_sync(kAllLanes, act);
-        if (!am) continue;
-        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(am) * rowb);
+        const uint32_t lead = __ballot_sync(kAllLanes, act && r == 0);  // one copy per active token
+        if (!lead) continue;
+        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(lead) * rowb);
         __syncwarp();
-        if (act) bulk_load(stage + (size_t)lane * rsw, a.logits + (size_t)u * E, rowb, bar);
+        if (act && r == 0) bulk_load(stage + (size_t)t * S4, a.logits + (size_t)u * E, rowb, bar);
         if (!__all_sync(kAllLanes, mbar_wait_bounded(bar, phase, a.wait_polls))) {
-            // give up: let this CTA's copies land (full bound), flag, leave
+            // give up: let this warp's copies land (full bound), flag, leave
             mbar_wait_bounded(bar, phase, kWaitLimit);
             if (lane == 0) atomicOr(a.status, kDevWaitTimeout);
             return;
         }
         phase ^= 1;
 
-        // 1. maxima of 2*KMAX disjoint groups (NaN ignored: fmaxf returns the
-        // other operand; a group of only NaN stays -infinity), then the
-        // KMAX-th largest of them
-        constexpr int G = 2 * KMAX;
-        float ga[KMAX], gb[KMAX];
+        // 1. the bound.  Lane share r holds units r, r+P, ... of the row.
+        float tau;
+        if constexpr (KMAX >= P) {
+            // KMAX/P-th largest of this share's 2*KMAX/P group maxima (NaN
+            // ignored by fmaxf; an all-NaN group stays -infinity), then the
+            // smallest over the token's P lanes: KMAX distinct elements >= tau
+            constexpr int RK = KMAX / P, GL = 2 * RK;
+            float gm[GL];
 #pragma unroll
-        for (int q = 0; q < KMAX; ++q) ga[q] = gb[q] = -INFINITY;
-        for (int j0 = 0; j0 < nu; j0 += G) {
+            for (int q = 0; q < GL; ++q) gm[q] = -INFINITY;
+            for (int j0 = r; j0 < nu; j0 += P * GL) {
 #pragma unroll
-            for (int q = 0; q < G; ++q)
-                if (j0 + q < nu) {
-                    const float4 v = row4[j0 + q];
-                    const float m = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-                    if (q < KMAX) ga[q] = fmaxf(ga[q], m);
-                    else gb[q - KMAX] = fmaxf(gb[q - KMAX], m);
+                for (int q = 0; q < GL; ++q) {
+                    const int j = j0 + P * q;
+                    if (j < nu) {
+                        const float4 v = row4[j];
+                        gm[q] = fmaxf(gm[q], fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+                    }
                 }
-        }
-        sort_desc<KMAX>(ga);
-        sort_desc<KMAX>(gb);
-        float tau = fmaxf(ga[0], gb[KMAX - 1]);
+            }
+            sort_desc<GL>(gm);
+            tau = gm[RK - 1];
 #pragma unroll
-        for (int i = 1; i < KMAX; ++i) tau = fminf(tau, fmaxf(ga[i], gb[KMAX - 1 - i]));
+            for (int m = 1; m < P; m <<= 1) tau = fminf(tau, __shfl_xor_sync(kAllLanes, tau, m));
+        } else {
+            // k = 1: the row's maximum
+            tau = -INFINITY;
+            for (int j = r; j < nu; j += P) {
+                const float4 v = row4[j];
+                tau = fmaxf(tau, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+            }
+#pragma unroll
+            for (int m = 1; m < P; m <<= 1) tau = fmaxf(tau, __shfl_xor_sync(kAllLanes, tau, m));
+        }
 
-        // 2. candidates: ids of the logits >= tau, ascending (NaN never is;
-        // with tau = -infinity the lane scans its whole row below instead)
+        // 2. this share's candidates: ids of the logits >= tau, ascending
+        // (NaN never is; with tau = -infinity the share is scanned whole below)
         int cnt = 0;
 #pragma unroll 4
-        for (int j = 0; j < nu; ++j) {
+        for (int j = r; j < nu; j += P) {
             const float4 v = row4[j];
             const int e = 4 * j;
             if (v.x >= tau) mine[min(cnt++, kLaneCap) * 32] = (uint16_t)e;
@@ -198,7 +266,7 @@ __global__ void __launch_bounds__(32) route_lane_kernel(const RouteArgs a) {
         }
         const bool scan_all = act && (tau == -INFINITY || cnt > kLaneCap);
 
-        // 3. sorted insertion, candidates in ascending id order
+        // 3. sorted insertion of the share's candidates, ascending ids
         uint32_t kk[KMAX];
         int ii[KMAX];
 #pragma unroll
@@ -218,7 +286,17 @@ __global__ void __launch_bounds__(32) route_lane_kernel(const RouteArgs a) {
             insert_sorted<KMAX>(kk, ii, xk, xi);
         }
         if (__any_sync(kAllLanes, scan_all))
-            for (int e = 0; e < E; ++e) insert_sorted<KMAX>(kk, ii, scan_all ? order_key(logit_key(row[e])) : 0u, e);
+            for (int j = r; j < nu; j += P) {
+                const float4 v = row4[j];
+                const int e = 4 * j;
+                insert_sorted<KMAX>(kk, ii, scan_all ? order_key(logit_key(v.x)) : 0u, e);
+                insert_sorted<KMAX>(kk, ii, scan_all ? order_key(logit_key(v.y)) : 0u, e + 1);
+                insert_sorted<KMAX>(kk, ii, scan_all ? order_key(logit_key(v.z)) : 0u, e + 2);
+                insert_sorted<KMAX>(kk, ii, scan_all ? order_key(logit_key(v.w)) : 0u, e + 3);
+            }
+        // the token's P shares: every lane of it ends with the token's list
+#pragma unroll
+        for (int m = 1; m < P; m <<= 1) merge_lists<KMAX>(kk, ii, m);
 
         if (act) {
             // gates: softmax of the selected logits, summed in slot order
@@ -239,7 +317,7 @@ __global__ void __launch_bounds__(32) route_lane_kernel(const RouteArgs a) {
             }
 #pragma unroll
             for (int j = 0; j < KMAX; ++j)
-                if (j < k) {
+                if (j < k && j % P == r) {
                     a.idx[(size_t)u * k + j] = ii[j];
                     a.gate[(size_t)u * k + j] = w[j];
                 }
@@ -270,17 +348,19 @@ cudaError_t configure_route(a2av_plan_s &p) {
     if (p.cfg.flags & A2AV_FLAG_ROUTE_WARP) return cudaSuccess;
     const int k = p.g.k, E = p.g.E;
     const int kmax = k <= 1 ? 1 : k <= 2 ? 2 : k <= 4 ? 4 : k <= 8 ? 8 : 0;
-    const size_t smem = lane_smem_bytes(E);
-    if (kmax == 0 || E % 4 != 0 || E > 65535 || smem > kLaneSmemMax) return cudaSuccess;
+    if (kmax == 0 || E % 4 != 0 || E > 65535) return cudaSuccess;
+    const int P = lanes_per_token(kmax);
+    const size_t smem = kRouteWarps * lane_warp_bytes(E, P);
+    if (smem > kLaneSmemMax) return cudaSuccess;
     RouteKernel kern = route_lane_kernel_for(kmax);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32, smem);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * kRouteWarps, smem);
     if (e != cudaSuccess) return e;
     if (per_sm <= 0) return cudaSuccess;
     p.route_lane_kmax = kmax;
-    p.route_lane_rsw = lane_row_stride(E);
+    p.route_lane_rsw = 4 * lane_row_units(E, P);
     p.route_lane.grid = p.num_sms * per_sm;
-    p.route_lane.block = 32;
+    p.route_lane.block = 32 * kRouteWarps;
     p.route_lane.smem = smem;
     return cudaSuccess;
 }
@@ -291,7 +371,7 @@ cudaError_t launch_route(const a2av_plan_s &p, const RouteArgs &a, cudaStream_t 
     if (p.route_lane_kmax > 0 && reinterpret_cast<uintptr_t>(a.logits) % 16 == 0) {
         RouteArgs b = a;
         b.rsw = p.route_lane_rsw;
-        route_lane_kernel_for(p.route_lane_kmax)<<<p.route_lane.grid, 32, p.route_lane.smem, s>>>(b);
+        route_lane_kernel_for(p.route_lane_kmax)<<<p.route_lane.grid, p.route_lane.block, p.route_lane.smem, s>>>(b);
     } else {
         route_kernel_for(p.g.E)<<<p.route.grid, p.route.block, 0, s>>>(a);
     }
