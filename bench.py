@@ -74,8 +74,11 @@ def parse_args(argv=None):
                     help="tokens taking part per rank, as a fraction of T (read from device memory)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="run the workload with this many tokens per rank (small cases for profiling)")
+    ap.add_argument("--hidden", type=int, default=0,
+                    help="run the workload with this row width H (small cases for profiling the router)")
     ap.add_argument("--flags", type=int, default=0,
-                    help="a2av_config_t.flags (1 LSU pack, 2 tiled splits, 4 TMA combine)")
+                    help="a2av_config_t.flags (1 LSU pack, 2 tiled splits, 4 TMA combine, 8 fused router, "
+                         "16 warp-per-token router)")
     ap.add_argument("--pack-ctas-per-sm", type=int, default=0)
     ap.add_argument("--pack-stage-bytes", type=int, default=0)
     ap.add_argument("--pack-store-lag", type=int, default=0)
@@ -583,8 +586,8 @@ def run_layers(args, w: W.Workload, dev, rank: int, world: int, local: int):
 def main():
     args = parse_args()
     w = W.WORKLOADS[args.workload]
-    if args.tokens:
-        w = w.scaled(T=args.tokens)
+    if args.tokens or args.hidden:
+        w = w.scaled(T=args.tokens or None, H=args.hidden or None)
     if args.recv_order != "source":
         import dataclasses
 

@@ -298,28 +298,49 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_lane_kernel(const Rout
 #pragma unroll
         for (int m = 1; m < P; m <<= 1) merge_lists<KMAX>(kk, ii, m);
 
-        if (act) {
-            // gates: softmax of the selected logits, summed in slot order
+        // Gates: softmax of the selected logits, summed in slot order.  Share
+        // r computes and stores slots r, r+P, ...; the sum gathers every
+        // slot's exponential from its share (all of a token's lanes see the
+        // same list, so the same top and the same sum).
+        {
+            constexpr int SL = (KMAX + P - 1) / P;  // slots per share
             const float top = order_value(kk[0]);
-            float w[KMAX];
-            if (top == -INFINITY) {
+            const bool flat = top == -INFINITY;      // every selected logit -infinity
+            // this share's slots, picked with static indices (a register
+            // array indexed by the lane's share would go to local memory)
+            uint32_t sk[SL];
+            int si[SL];
 #pragma unroll
-                for (int j = 0; j < KMAX; ++j) w[j] = __fdiv_rn(1.0f, (float)k);
-            } else {
-                float sum = 0.f;
+            for (int q = 0; q < SL; ++q) {
+                sk[q] = 0u;
+                si[q] = -1;
 #pragma unroll
-                for (int j = 0; j < KMAX; ++j) {
-                    w[j] = j < k ? expf(order_value(kk[j]) - top) : 0.f;
-                    if (j < k) sum = __fadd_rn(sum, w[j]);
-                }
-#pragma unroll
-                for (int j = 0; j < KMAX; ++j) w[j] = __fdiv_rn(w[j], sum);
+                for (int d = 0; d < P; ++d)
+                    if (q * P + d < KMAX && d == r) {
+                        sk[q] = kk[q * P + d];
+                        si[q] = ii[q * P + d];
+                    }
             }
+            float ex[SL];
 #pragma unroll
-            for (int j = 0; j < KMAX; ++j)
-                if (j < k && j % P == r) {
-                    a.idx[(size_t)u * k + j] = ii[j];
-                    a.gate[(size_t)u * k + j] = w[j];
+            for (int q = 0; q < SL; ++q) {
+                const int j = q * P + r;
+                ex[q] = (j < k && !flat) ? expf(order_value(sk[q]) - top) : 0.f;
+            }
+            float sum = 0.f;
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                const float ej = __shfl_sync(kAllLanes, ex[j / P], (lane & ~(P - 1)) | (j % P));
+                if (j < k) sum = __fadd_rn(sum, ej);
+            }
+            if (act)
+#pragma unroll
+                for (int q = 0; q < SL; ++q) {
+                    const int j = q * P + r;
+                    if (j < k) {
+                        a.idx[(size_t)u * k + j] = si[q];
+                        a.gate[(size_t)u * k + j] = flat ? __fdiv_rn(1.0f, (float)k) : __fdiv_rn(ex[q], sum);
+                    }
                 }
         }
         __syncwarp();  // every lane is done with the rows before the next copies land
