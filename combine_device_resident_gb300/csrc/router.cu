@@ -13,14 +13,15 @@
 // memory by one bulk copy each, padded so that the 8 lanes of a quarter warp
 // read 8 distinct bank groups; lane share r of a token holds 16-byte units
 // r, r+P, ... of its row.  Per share, in three passes over it:
-//   1. a lower bound tau of the k-th largest logit: the (KMAX/P)-th largest
-//      of the share's 2*KMAX/P group maxima, then the smallest over the
-//      token's P shares -- KMAX >= k distinct elements are >= tau.  (For
-//      k = 1, P > KMAX: the row's maximum.)
+//   1. a lower bound tau of the k-th largest logit: the KMAX-th largest of
+//      2*KMAX group maxima of the row, 2*KMAX/P of them per share, found by
+//      merging the shares' sorted maxima over shuffles -- KMAX >= k distinct
+//      elements are >= tau.  (For k = 1, P > KMAX: the row's maximum.)
 //   2. the ids of the share's logits >= tau, ascending, into a candidate
-//      list (about 4 per share on Gaussian logits with E = 256, k = 8: 16
-//      per token; a bound from the minimum of KMAX group maxima let 21 per
-//      token through, and 8% of the lists overflowed);
+//      list (on Gaussian logits with E = 256, k = 8: 10.4 per token, 2.6
+//      per share, at most 6 in a warp on average; a bound from each share's
+//      own maxima let 16 per token through, and the minimum of KMAX group
+//      maxima 21, with 8% of one-lane-per-token lists overflowing);
 //   3. a sorted insertion of the candidates into KMAX registers, where only
 //      a strictly greater key moves up (of equal logits the lower id, which
 //      arrived first, stays ahead).
@@ -108,6 +109,47 @@ __device__ __forceinline__ void sort_desc(float (&v)[N]) {
             v[j] = hi;
             v[j + 1] = lo;
         }
+}
+
+// Sort a bitonic sequence of floats in descending order (half-cleaners).
+template <int L>
+__device__ __forceinline__ void bitonic_desc(float (&v)[L]) {
+#pragma unroll
+    for (int d = L / 2; d >= 1; d >>= 1)
+#pragma unroll
+        for (int j = 0; j < L; ++j)
+            if ((j & d) == 0) {
+                const float hi = fmaxf(v[j], v[j + d]), lo = fminf(v[j], v[j + d]);
+                v[j] = hi;
+                v[j + d] = lo;
+            }
+}
+
+// The K-th largest of the 2K values held by the P lanes of a token, each
+// lane holding 2K/P of them sorted in descending order (P = 2 or 4).  The
+// last step uses that of two sorted lists A and B of K, the K-th largest of
+// both is min_i max(A_i, B_{K-1-i}).
+template <int K, int P>
+__device__ __forceinline__ float token_kth(float (&g)[2 * K / P]) {
+    if constexpr (P == 2) {
+        float t = INFINITY;
+#pragma unroll
+        for (int i = 0; i < K; ++i) t = fminf(t, fmaxf(g[i], __shfl_xor_sync(kAllLanes, g[K - 1 - i], 1)));
+        return t;
+    } else {
+        constexpr int L = 2 * K / P;  // K / 2
+        float c[2 * L];               // this pair's values, sorted: mine then the partner's reversed
+#pragma unroll
+        for (int i = 0; i < L; ++i) {
+            c[i] = g[i];
+            c[2 * L - 1 - i] = __shfl_xor_sync(kAllLanes, g[i], 1);
+        }
+        bitonic_desc<2 * L>(c);
+        float t = INFINITY;
+#pragma unroll
+        for (int i = 0; i < K; ++i) t = fminf(t, fmaxf(c[i], __shfl_xor_sync(kAllLanes, c[K - 1 - i], 2)));
+        return t;
+    }
 }
 
 // Composite order of the selection: a larger key first, of equal keys the
@@ -220,9 +262,9 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_lane_kernel(const Rout
         // 1. the bound.  Lane share r holds units r, r+P, ... of the row.
         float tau;
         if constexpr (KMAX >= P) {
-            // KMAX/P-th largest of this share's 2*KMAX/P group maxima (NaN
-            // ignored by fmaxf; an all-NaN group stays -infinity), then the
-            // smallest over the token's P lanes: KMAX distinct elements >= tau
+            // the KMAX-th largest of the token's 2*KMAX group maxima, 2*KMAX/P
+            // of them per share (NaN ignored by fmaxf; an all-NaN group stays
+            // -infinity): KMAX distinct elements are >= tau
             constexpr int RK = KMAX / P, GL = 2 * RK;
             float gm[GL];
 #pragma unroll
@@ -238,9 +280,7 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_lane_kernel(const Rout
                 }
             }
             sort_desc<GL>(gm);
-            tau = gm[RK - 1];
-#pragma unroll
-            for (int m = 1; m < P; m <<= 1) tau = fminf(tau, __shfl_xor_sync(kAllLanes, tau, m));
+            tau = token_kth<KMAX, P>(gm);
         } else {
             // k = 1: the row's maximum
             tau = -INFINITY;
