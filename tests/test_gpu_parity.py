@@ -730,26 +730,35 @@ def test_router_lane_kernel_equals_warp_kernel(R, T, E, k):
     np.testing.assert_array_equal(outs[0][0], ridx)
 
 
-def test_router_leaves_inactive_tokens_alone():
+@pytest.mark.parametrize("wid,T", [(4, 100), (5, 37), (2, 45)])
+def test_router_leaves_inactive_tokens_alone(wid, T):
+    # T not a multiple of a warp task's tokens: tasks straddle ranks and mix
+    # active and inactive tokens (top-2: 2 lanes per token, top-8 and top-1: 4)
     import torch
     from combine_device_resident_gb300 import Plan
 
-    w = W.WORKLOADS[4].scaled(T=100, H=8)
+    from combine_device_resident_gb300 import FLAG_ROUTE_WARP
+
+    w = W.WORKLOADS[wid].scaled(T=T, H=8)
     dev = P.device()
-    plan = Plan(w.R, w.E, w.T, w.H, w.k, device=dev)
     nt = _counts(w, 9)
-    plan.set_active_tokens(torch.from_numpy(nt).to(dev))
     logits = W.make_logits(w, 1, device=dev)
-    idx = torch.full((w.R, w.T, w.k), -9, dtype=torch.int32, device=dev)
-    gate = torch.full((w.R, w.T, w.k), -1.0, dtype=torch.float32, device=dev)
-    plan.route(logits, idx, gate)
-    torch.cuda.synchronize()
     ridx, _ = oracle.route(logits.cpu().numpy(), w.k, num_tokens=nt)
-    got = idx.cpu().numpy()
-    for s_ in range(w.R):
-        np.testing.assert_array_equal(got[s_, :nt[s_]], ridx[s_, :nt[s_]])
-        assert (got[s_, nt[s_]:] == -9).all()
-        assert (gate.cpu().numpy()[s_, nt[s_]:] == -1.0).all()
+    runs = []
+    for flags in (0, FLAG_ROUTE_WARP):  # the lane kernel, then the warp kernel
+        plan = Plan(w.R, w.E, w.T, w.H, w.k, device=dev, flags=flags)
+        plan.set_active_tokens(torch.from_numpy(nt).to(dev))
+        idx = torch.full((w.R, w.T, w.k), -9, dtype=torch.int32, device=dev)
+        gate = torch.full((w.R, w.T, w.k), -1.0, dtype=torch.float32, device=dev)
+        plan.route(logits, idx, gate)
+        torch.cuda.synchronize()
+        got, g = idx.cpu().numpy(), gate.cpu().numpy()
+        for s_ in range(w.R):
+            np.testing.assert_array_equal(got[s_, :nt[s_]], ridx[s_, :nt[s_]])
+            assert (got[s_, nt[s_]:] == -9).all()
+            assert (g[s_, nt[s_]:] == -1.0).all()
+        runs.append(g.view(np.uint32))
+    np.testing.assert_array_equal(runs[0], runs[1])
 
 
 # ---------------------------------------------------------------------------
