@@ -221,7 +221,10 @@ __global__ void __launch_bounds__(32, 1) pack_tma_kernel(const PackArgs a) {
         for (long long p = 0; p < pre; ++p) issue_load(p);
     long long issued = pre;  // loads issued so far (units 0..issued-1)
 
-    // x does not depend on the splits kernel; everything below does.
+    // x does not depend on the splits kernel; everything below does.  (The
+    // splits kernels let this grid launch only once the kernel before them
+    // has completed, so these loads never race with a kernel writing x: the
+    // previous call's combine, when its out is this call's x.)
     grid_dependency_wait();
 
     uint32_t ovf = 0;

@@ -33,8 +33,9 @@
 // assignments per round; the lanes holding the same expert find each other
 // with one ballot per bit of the expert id, their group does one
 // shared-memory update, and each lane gets its stable rank in the group.
-// Both let the pack kernel begin launching at once (programmatic dependent
-// launch); the pack kernel waits for this grid before reading its output.
+// Both let the pack kernel begin launching as soon as the kernel before
+// them has completed (programmatic dependent launch), so the pack streams x
+// in while they work; it waits for this grid before reading their output.
 //
 // Compile-time variants: with or without the code that fills
 // recv_expert_offsets (the first row of each (source, local expert) block;
@@ -120,13 +121,11 @@ __global__ void __launch_bounds__(NW * 32) hist_scan_kernel(const HistArgs a) {
     extern __shared__ int smem[];
     __shared__ int wtot[33];
     __shared__ int last;
-    grid_launch_dependents();
     const Geometry &g = a.g;
     const int E = g.E, R = g.R, epr = g.epr, ES = E + 1;  // ES: padded row stride
     const int s = blockIdx.y, tile = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int A = g.T * g.k;  // assignments of one rank
-    const int As = active_tokens(a.num_tokens, s, g.T) * g.k;  // of them taking part
 
     // ---- per-warp counts of this tile --------------------------------------
     int *cnt = smem + warp * ES;
@@ -134,8 +133,13 @@ __global__ void __launch_bounds__(NW * 32) hist_scan_kernel(const HistArgs a) {
     __syncwarp();
     // Launched as a programmatic dependent of whatever kernel came before
     // (the previous call's combine, a router): nothing global is read or
-    // written before its grid has completed.
+    // written before its grid has completed, num_tokens included.
     grid_dependency_wait();
+    // The pack kernel (a programmatic dependent) may launch now.  Not
+    // earlier: the pack loads x before its own dependency wait, and x may be
+    // the output of the kernel just waited for (the previous call's out).
+    grid_launch_dependents();
+    const int As = active_tokens(a.num_tokens, s, g.T) * g.k;  // assignments taking part
     const int w0 = tile * kHistTile + warp * (32 * ROUNDS);
     int key[ROUNDS], rank[ROUNDS];
     int vals[ROUNDS];
@@ -410,12 +414,10 @@ __device__ __forceinline__ void st_dsmem(uint32_t addr, int v) {
 template <bool BY_EXPERT, bool WRITE_REO>
 __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(const HistArgs a) {
     extern __shared__ int smem[];
-    grid_launch_dependents();
     const Geometry &g = a.g;
     const int R = g.R, E = g.E, epr = g.epr, ES = E + 1;
     const int A = g.T * g.k;
     const int s = blockIdx.x;  // == rank of this CTA in the cluster
-    const int As = active_tokens(a.num_tokens, s, g.T) * g.k;  // assignments taking part
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chunk = ((A + kClusterWarps - 1) / kClusterWarps + 31) / 32 * 32;
     const int a0 = warp * chunk;
@@ -443,6 +445,8 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
     if (by_expert)
         for (int i = tid; i < 2 * E; i += kClusterThreads) xb[i] = 0;  // xb and xt
     grid_dependency_wait();
+    grid_launch_dependents();  // the pack may launch now (as in hist_scan_kernel)
+    const int As = active_tokens(a.num_tokens, s, g.T) * g.k;  // assignments taking part
     int vals[kClusterRounds];
 #pragma unroll
     for (int r = 0; r < kClusterRounds; ++r) {

@@ -415,6 +415,70 @@ def test_back_to_back_calls_reusing_buffers(wid, T, H, flags, graph):
     plan.close()
 
 
+@pytest.mark.parametrize("wid,T,H,graph", [(3, 256, 5120, False), (3, 256, 5120, True), (1, None, None, False),
+                                           (2, 512, 1032, True), (4, 2048, 520, False)])
+def test_chained_calls_out_feeds_next_dispatch(wid, T, H, graph):
+    # Each call's out is the next call's x (layer after layer with nothing in
+    # between), on one stream and without a host sync: the next call's pack
+    # loads x before its own dependency wait, so it must not be launched
+    # before this call's combine has completed.  out is filled with a
+    # sentinel on the stream before the combine that writes it; every
+    # received row of the next call must be its out row bit for bit.
+    import torch
+    from combine_device_resident_gb300 import Plan
+
+    w = W.WORKLOADS[wid] if T is None else W.WORKLOADS[wid].scaled(T=T, H=H)
+    dev = P.device()
+    plan = Plan(w.R, w.E, w.T, w.H, w.k, w.window_mode, w.window_rows, device=dev)
+    n = 4
+    xs = [W.make_x(w, 0, device=dev)] + [torch.empty((w.R, w.T, w.H), dtype=torch.bfloat16, device=dev)
+                                          for _ in range(n)]
+    bufs = [plan.new_buffers()[:2] for _ in range(2)]  # double-buffered arenas
+    sps = [plan.new_splits() for _ in range(2)]
+    rgs = [W.make_routing_gate(w, 300 + i) for i in range(n)]
+    idx = [torch.from_numpy(r["topk_idx"]).to(dev) for r in rgs]
+    gate = [torch.from_numpy(r["gate_w"]).to(dev) for r in rgs]
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+
+    def calls():
+        for i in range(n):
+            recv, slot_map = bufs[i % 2]
+            plan.dispatch(xs[i], idx[i], sps[i % 2], recv, slot_map, stream=s)
+            xs[i + 1].fill_(-3.0)  # sentinel, on the stream, right before the combine writes it
+            plan.combine(recv, gate[i], slot_map, xs[i + 1], stream=s)
+
+    if graph:
+        with torch.cuda.stream(s):
+            calls()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            calls()
+        for _ in range(3):
+            g.replay()
+    else:
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                calls()
+    torch.cuda.synchronize()
+    for i in range(n):
+        xh = P.bits(xs[i])
+        ref = oracle.run_all(w.R, w.E, xh, rgs[i]["topk_idx"], rgs[i]["gate_w"], w.window_mode, w.window_rows)
+        np.testing.assert_array_equal(P.bits(xs[i + 1]), ref["out"], err_msg=f"call {i}")
+    recv, slot_map = bufs[(n - 1) % 2]
+    sm = slot_map.cpu().numpy()
+    rb = P.bits(recv)
+    xl = P.bits(xs[n - 1])
+    for s_ in range(w.R):
+        for t in range(0, w.T, max(1, w.T // 64)):
+            for j in range(w.k):
+                if sm[s_, t, j] >= 0:
+                    np.testing.assert_array_equal(rb[sm[s_, t, j]], xl[s_, t])
+    assert plan.read_status() == 0
+    plan.close()
+
+
 def test_plans_with_different_shapes_coexist():
     # Kernel attributes are per kernel, not per plan: a plan made later with a
     # small row must not break an earlier plan with a large one.
