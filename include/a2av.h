@@ -317,14 +317,16 @@ a2av_status_t a2av_route_splits(a2av_plan_t plan, const float *logits, int32_t *
 a2av_status_t a2av_set_active_tokens(a2av_plan_t plan, const int32_t *num_tokens);
 
 /* Diagnostic hook for the failure path of the bounded waits (not part of
- * the method).  The TMA pack (default) and the TMA combine
- * (A2AV_FLAG_COMBINE_TMA) wait on mbarriers for the bulk copies they issued
+ * the method).  The TMA pack (default), the TMA combine
+ * (A2AV_FLAG_COMBINE_TMA) and the lane-per-token router (a2av_route's
+ * default) wait on mbarriers for the bulk copies they issued
  * themselves; each wait gives up after a bounded number of polls, sets
  * A2AV_DEV_WAIT_TIMEOUT in the status word and ends the CTA in order (it
  * first lets every copy it issued land, with the full bound).  This call sets
  * the main-loop limit of those waits for later enqueues on `plan`: polls >= 0
  * polls at most that many times (0 gives up at once, which makes the
- * give-up path run on purpose; the rows of that call are then incomplete),
+ * give-up path run on purpose; the rows, or the routing, of that call are
+ * then incomplete),
  * polls < 0 restores the default (2^22 polls, seconds: never reached while
  * the copies work).  Values above the default are clamped to it.  Host call,
  * no device work.  [No counterpart on the pages: the pages' collectives

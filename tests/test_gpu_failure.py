@@ -1,7 +1,7 @@
 """Failure detection on the GPU without a fault: the bounded waits give up.
 
-The TMA pack (default) and the TMA combine wait on mbarriers for the bulk
-copies they issued themselves.  Every such wait is bounded: when it runs out
+The TMA pack (default), the TMA combine and the lane-per-token router wait
+on mbarriers for the bulk copies they issued themselves.  Every such wait is bounded: when it runs out
 the kernel sets A2AV_DEV_WAIT_TIMEOUT in the plan's status word, lets every
 copy it issued land (with the full bound) and returns, so the context stays
 usable.  ``a2av_set_wait_limit(plan, 0)`` makes the main-loop wait give up at
@@ -76,6 +76,41 @@ def test_tma_combine_wait_gives_up_then_next_call_is_exact(wid, T, H):
     assert g["status"] == 0
     np.testing.assert_array_equal(g["out"], g["ref"]["out"])
     plan.close()
+
+
+@pytest.mark.parametrize("wid,T", [(4, 300), (5, 100), (2, 200)])
+def test_router_wait_gives_up_then_next_call_is_exact(wid, T):
+    import torch
+
+    import combine_device_resident_gb300 as A
+    from oracle import route as oracle_route
+
+    w = W.WORKLOADS[wid].scaled(T=T, H=8)
+    dev = P.device()
+    plan = A.Plan(w.R, w.E, w.T, w.H, w.k, device=dev)
+    warp = A.Plan(w.R, w.E, w.T, w.H, w.k, device=dev, flags=A.FLAG_ROUTE_WARP)
+    logits = W.make_logits(w, 3, device=dev)
+    idx = torch.full((w.R, w.T, w.k), -9, dtype=torch.int32, device=dev)
+    gate = torch.zeros((w.R, w.T, w.k), dtype=torch.float32, device=dev)
+    plan.read_status(clear=True)
+    plan.set_wait_limit(0)
+    plan.route(logits, idx, gate)
+    torch.cuda.synchronize()
+    st = plan.read_status(clear=True)
+    assert st & A.DEV_WAIT_TIMEOUT, f"status {st:#x}"
+    plan.set_wait_limit(-1)
+    plan.route(logits, idx, gate)
+    widx = torch.empty_like(idx)
+    wgate = torch.empty_like(gate)
+    warp.route(logits, widx, wgate)  # the warp-per-token kernel waits on nothing
+    torch.cuda.synchronize()
+    assert plan.read_status() == 0 and warp.read_status() == 0
+    ridx, _ = oracle_route(logits.cpu().numpy(), w.k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+    np.testing.assert_array_equal(widx.cpu().numpy(), ridx)
+    np.testing.assert_array_equal(gate.cpu().numpy().view(np.uint32), wgate.cpu().numpy().view(np.uint32))
+    plan.close()
+    warp.close()
 
 
 def test_wait_limit_is_per_plan():
