@@ -666,10 +666,10 @@ cudaLaunchConfig_t cluster_launch_config(const a2av_plan_s &p, cudaLaunchAttribu
     return lc;
 }
 
-// The tiled kernels' launch: grid (tiles, R), programmatic dependent of the
-// kernel before it.
+// The tiled kernels' launch: grid (tiles, R), a programmatic dependent of
+// the kernel before it when `pdl`.
 cudaError_t launch_tiled(SplitsKernel k, const a2av_plan_s &p, int threads, size_t smem, const HistArgs &a,
-                         cudaStream_t s) {
+                         cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(p.g.tiles, p.g.R);
     lc.blockDim = dim3(threads);
@@ -679,9 +679,19 @@ cudaError_t launch_tiled(SplitsKernel k, const a2av_plan_s &p, int threads, size
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = at;
-    lc.numAttrs = 1;
+    lc.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&lc, k, a);
 }
+
+// Whether a splits kernel starts as a programmatic dependent of the kernel
+// before it.  Only on few-token calls, where the overlap is worth a
+// microsecond or two of a ~20 us step.  On large calls it is worth nothing,
+// and it has a cost: its CTAs, placed while that kernel still holds most
+// SMs, crowd onto the few SMs with room.  Then the persistent pack grid
+// launched after them cannot seat all its CTAs, and those left over run a
+// whole pack-length second wave (measured with the router letting its
+// dependents launch early: r32 E256 top-8 step 2,654 -> 3,926 us).
+bool splits_pdl(const a2av_plan_s &p) { return p.few_tokens; }
 
 }  // namespace
 
@@ -745,10 +755,11 @@ cudaError_t launch_hist(const a2av_plan_s &p, const HistArgs &a, cudaStream_t s)
     cudaError_t e;
     if (p.splits_small) {
         cudaLaunchAttribute at[2];
-        cudaLaunchConfig_t lc = cluster_launch_config(p, at, s, true);
+        cudaLaunchConfig_t lc = cluster_launch_config(p, at, s, splits_pdl(p));
         e = cudaLaunchKernelEx(&lc, cluster_kernel_for(p.g, reo), a);
     } else {
-        e = launch_tiled(hist_kernel_for(reo), p, kHistThreads, hist_smem_bytes(p.g, reo, kHistWarps), a, s);
+        e = launch_tiled(hist_kernel_for(reo), p, kHistThreads, hist_smem_bytes(p.g, reo, kHistWarps), a, s,
+                         splits_pdl(p));
     }
     return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -765,8 +776,8 @@ cudaError_t launch_routed_hist(const a2av_plan_s &p, const HistArgs &a, cudaStre
     const int epl = routed_epl(p.g);
     if (!epl) return cudaErrorInvalidValue;
     const bool reo = a.sp.recv_expert_offsets != nullptr;
-    cudaError_t e =
-        launch_tiled(hist_kernel_for(reo, epl), p, kRoutedWarps * 32, hist_smem_bytes(p.g, reo, kRoutedWarps), a, s);
+    cudaError_t e = launch_tiled(hist_kernel_for(reo, epl), p, kRoutedWarps * 32,
+                                 hist_smem_bytes(p.g, reo, kRoutedWarps), a, s, splits_pdl(p));
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
