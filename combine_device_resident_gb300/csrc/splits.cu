@@ -131,9 +131,10 @@ __global__ void __launch_bounds__(NW * 32) hist_scan_kernel(const HistArgs a) {
     int *cnt = smem + warp * ES;
     for (int e = lane; e < E; e += 32) cnt[e] = 0;
     __syncwarp();
-    // Launched as a programmatic dependent of whatever kernel came before
-    // (the previous call's combine, a router): nothing global is read or
-    // written before its grid has completed, num_tokens included.
+    // On few-token calls launched as a programmatic dependent of whatever
+    // kernel came before (the previous call's combine, a router): nothing
+    // global is read or written before its grid has completed, num_tokens
+    // included.
     grid_dependency_wait();
     // The pack kernel (a programmatic dependent) may launch now.  Not
     // earlier: the pack loads x before its own dependency wait, and x may be
@@ -429,9 +430,9 @@ __global__ void __launch_bounds__(kClusterThreads, 1) splits_cluster_kernel(cons
     int *xb = wb + R;                    // [E] expert order: rows of expert e on ranks below s
     int *xt = xb + E;                    // [E] expert order: rows of e on all ranks, then e's block start
     constexpr bool by_expert = BY_EXPERT;
-    // Launched as a programmatic dependent of the kernel before it (the
-    // previous call's combine, a router): it is resident early and reads or
-    // writes nothing global before that grid has completed.  Meanwhile it
+    // On few-token calls launched as a programmatic dependent of the kernel
+    // before it (the previous call's combine, a router): it is resident early
+    // and reads or writes nothing global before that grid has completed.  Meanwhile it
     // asks L2 for its routing lines (a prefetch only warms L2, which stays
     // coherent with the predecessor's writes; the values are loaded after the
     // wait) and clears its counters.
