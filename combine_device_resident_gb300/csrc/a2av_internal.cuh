@@ -162,6 +162,7 @@ struct a2av_plan_s {
     int32_t pack_chunk_bytes = 0, pack_nchunks = 0, pack_stages = 0, pack_lag = 1;
     int pack_stream_rows = 0;  // the pack stores its rows evict-first (see configure_pack)
     int route_lane_kmax = 0;   // lane-per-token router instantiation (0: the warp-per-token kernel)
+    int route_lane_mw = 0;     // its candidate mask words per lane share
     int32_t route_lane_rsw = 0;  // its padded row stride in floats
     int64_t launches = 0;
     int64_t wait_polls = a2av::kWaitLimit;  // main-loop wait limit of the TMA kernels (a2av_set_wait_limit)

@@ -17,16 +17,16 @@
 //      2*KMAX group maxima of the row, 2*KMAX/P of them per share, found by
 //      merging the shares' sorted maxima over shuffles -- KMAX >= k distinct
 //      elements are >= tau.  (For k = 1, P > KMAX: the row's maximum.)
-//   2. the ids of the share's logits >= tau, ascending, into a candidate
-//      list (on Gaussian logits with E = 256, k = 8: 10.4 per token, 2.6
-//      per share, at most 6 in a warp on average; a bound from each share's
-//      own maxima let 16 per token through, and the minimum of KMAX group
-//      maxima 21, with 8% of one-lane-per-token lists overflowing);
-//   3. a sorted insertion of the candidates into KMAX registers, where only
-//      a strictly greater key moves up (of equal logits the lower id, which
-//      arrived first, stays ahead).
-// A share whose list overflows, or whose tau is -infinity (a group of only
-// -infinity or NaN logits), inserts every logit it holds instead.  Bitonic
+//   2. a bit per logit of the share: set where the logit is >= tau (on
+//      Gaussian logits with E = 256, k = 8: 10.4 per token, 2.6 per share,
+//      at most 6 in a warp on average; a bound from each share's own maxima
+//      let 16 per token through, and the minimum of KMAX group maxima 21);
+//   3. a sorted insertion of the candidates, taken in ascending id order
+//      from the bits, into KMAX registers, where only a strictly greater key
+//      moves up (of equal logits the lower id, which arrived first, stays
+//      ahead).
+// A share whose tau is -infinity (a group of only -infinity or NaN logits)
+// inserts every logit it holds instead.  Bitonic
 // merges over xor shuffles then give every lane of the token the token's
 // best KMAX, by key and then lower id.  Gates are computed as in
 // route_token, so the two kernels give the same bits.
@@ -42,7 +42,6 @@ namespace a2av {
 namespace {
 
 constexpr uint32_t kAllLanes = 0xffffffffu;
-constexpr int kLaneCap = 32;               // candidate list slots per lane (slot kLaneCap: overflow sink)
 constexpr size_t kLaneSmemMax = 96 * 1024;  // rows bigger than this take the warp kernel
 
 template <int EPL>
@@ -207,12 +206,29 @@ int lane_row_units(int E, int P) {
     while (S % (2 * P) != P) ++S;
     return S;
 }
-// One warp's shared memory: 32/P rows, the candidate lists, the barrier.
-size_t lane_warp_bytes(int E, int P) {
-    return (size_t)(32 / P) * lane_row_units(E, P) * 16 + (size_t)(kLaneCap + 1) * 32 * sizeof(uint16_t) + 16;
+// One warp's shared memory: 32/P rows and the barrier.
+size_t lane_warp_bytes(int E, int P) { return (size_t)(32 / P) * lane_row_units(E, P) * 16 + 16; }
+
+// Mask words per lane share: its logits (4 per 16-byte unit, units r, r+P,
+// ...) as bits, rounded up to 1, 2, 4 or 8 words; 0 when more are needed.
+int lane_mask_words(int E, int P) {
+    const int per = 4 * ((E / 4 + P - 1) / P);
+    const int w = (per + 31) / 32;
+    return w <= 1 ? 1 : w <= 2 ? 2 : w <= 4 ? 4 : w <= 8 ? 8 : 0;
 }
 
-template <int KMAX>
+// m[w] with a run-time w, by selects (a register array indexed at run time
+// would go to local memory).
+template <int MW>
+__device__ __forceinline__ uint32_t pick_word(const uint32_t (&m)[MW], int w) {
+    uint32_t v = m[0];
+#pragma unroll
+    for (int q = 1; q < MW; ++q)
+        if (w == q) v = m[q];
+    return v;
+}
+
+template <int KMAX, int MW>
 __global__ void __launch_bounds__(32 * kRouteWarps) route_lane_kernel(const RouteArgs a) {
     constexpr int P = lanes_per_token(KMAX);
     constexpr int TPW = 32 / P;  // tokens per warp task
@@ -220,10 +236,9 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_lane_kernel(const Rout
     const Geometry &g = a.g;
     const int E = g.E, k = g.k, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S4 = a.rsw;  // row stride in floats
-    const size_t wbytes = (size_t)TPW * S4 * 4 + (size_t)(kLaneCap + 1) * 32 * sizeof(uint16_t) + 16;
+    const size_t wbytes = (size_t)TPW * S4 * 4 + 16;
     unsigned char *base = sm + warp * wbytes;
-    float *stage = reinterpret_cast<float *>(base);                                // [TPW][S4]
-    uint16_t *lst = reinterpret_cast<uint16_t *>(base + (size_t)TPW * S4 * 4);   // [kLaneCap + 1][32]
+    float *stage = reinterpret_cast<float *>(base);  // [TPW][S4]
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + wbytes - 16);
     if (lane == 0) {
         mbar_init(bar, 1);
@@ -233,7 +248,6 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_lane_kernel(const Rout
     const int t = lane / P, r = lane - t * P;  // this lane: token t of the task, share r of its row
     const float4 *row4 = reinterpret_cast<const float4 *>(stage + (size_t)t * S4);
     const float *row = stage + (size_t)t * S4;
-    uint16_t *mine = lst + lane;
     const int nu = E / 4;
     const uint32_t rowb = (uint32_t)E * 4;
     const int ntok = g.R * g.T;
@@ -292,21 +306,31 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_lane_kernel(const Rout
             for (int m = 1; m < P; m <<= 1) tau = fmaxf(tau, __shfl_xor_sync(kAllLanes, tau, m));
         }
 
-        // 2. this share's candidates: ids of the logits >= tau, ascending
-        // (NaN never is; with tau = -infinity the share is scanned whole below)
+        // 2. this share's candidates, as bits: logit i of the share (unit
+        // r + P*(i/4), lane i%4 of it) >= tau sets bit i (NaN never does;
+        // with tau = -infinity the share is scanned whole below)
+        uint32_t msk[MW];
         int cnt = 0;
-#pragma unroll 4
-        for (int j = r; j < nu; j += P) {
-            const float4 v = row4[j];
-            const int e = 4 * j;
-            if (v.x >= tau) mine[min(cnt++, kLaneCap) * 32] = (uint16_t)e;
-            if (v.y >= tau) mine[min(cnt++, kLaneCap) * 32] = (uint16_t)(e + 1);
-            if (v.z >= tau) mine[min(cnt++, kLaneCap) * 32] = (uint16_t)(e + 2);
-            if (v.w >= tau) mine[min(cnt++, kLaneCap) * 32] = (uint16_t)(e + 3);
+#pragma unroll
+        for (int w = 0; w < MW; ++w) {
+            uint32_t bits = 0;
+#pragma unroll
+            for (int m8 = 0; m8 < 8; ++m8) {
+                const int j = r + P * (w * 8 + m8);
+                if (j < nu) {
+                    const float4 v = row4[j];
+                    bits |= ((uint32_t)(v.x >= tau) | (uint32_t)(v.y >= tau) << 1 | (uint32_t)(v.z >= tau) << 2 |
+                             (uint32_t)(v.w >= tau) << 3)
+                            << (4 * m8);
+                }
+            }
+            msk[w] = bits;
+            cnt += __popc(bits);
         }
-        const bool scan_all = act && (tau == -INFINITY || cnt > kLaneCap);
+        const bool scan_all = act && tau == -INFINITY;
 
-        // 3. sorted insertion of the share's candidates, ascending ids
+        // 3. sorted insertion of the share's candidates, ascending ids: the
+        // set bits in order, a cursor stepping through the words
         uint32_t kk[KMAX];
         int ii[KMAX];
 #pragma unroll
@@ -316,12 +340,19 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_lane_kernel(const Rout
         }
         const int nc = act && !scan_all ? cnt : 0;
         const int mc = (int)__reduce_max_sync(kAllLanes, (uint32_t)nc);
+        int cw = 0;
+        uint32_t cur = msk[0];
         for (int m = 0; m < mc; ++m) {
             uint32_t xk = 0u;
             int xi = 0;
             if (m < nc) {
-                xi = mine[m * 32];
-                xk = order_key(logit_key(row[xi]));
+                while (cur == 0 && cw < MW - 1) cur = pick_word<MW>(msk, ++cw);  // m < nc: bits are left
+                if (cur) {
+                    const int i = cw * 32 + __ffs(cur) - 1;
+                    cur &= cur - 1;
+                    xi = 4 * (r + P * (i >> 2)) + (i & 3);
+                    xk = order_key(logit_key(row[xi]));
+                }
             }
             insert_sorted<KMAX>(kk, ii, xk, xi);
         }
@@ -387,12 +418,22 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_lane_kernel(const Rout
     }
 }
 
-RouteKernel route_lane_kernel_for(int kmax) {
+template <int KMAX>
+RouteKernel route_lane_kernel_mw(int mw) {
+    switch (mw) {
+        case 1: return route_lane_kernel<KMAX, 1>;
+        case 2: return route_lane_kernel<KMAX, 2>;
+        case 4: return route_lane_kernel<KMAX, 4>;
+        case 8: return route_lane_kernel<KMAX, 8>;
+        default: return nullptr;
+    }
+}
+RouteKernel route_lane_kernel_for(int kmax, int mw) {
     switch (kmax) {
-        case 1: return route_lane_kernel<1>;
-        case 2: return route_lane_kernel<2>;
-        case 4: return route_lane_kernel<4>;
-        case 8: return route_lane_kernel<8>;
+        case 1: return route_lane_kernel_mw<1>(mw);
+        case 2: return route_lane_kernel_mw<2>(mw);
+        case 4: return route_lane_kernel_mw<4>(mw);
+        case 8: return route_lane_kernel_mw<8>(mw);
         default: return nullptr;
     }
 }
@@ -412,13 +453,15 @@ cudaError_t configure_route(a2av_plan_s &p) {
     if (kmax == 0 || E % 4 != 0 || E > 65535) return cudaSuccess;
     const int P = lanes_per_token(kmax);
     const size_t smem = kRouteWarps * lane_warp_bytes(E, P);
-    if (smem > kLaneSmemMax) return cudaSuccess;
-    RouteKernel kern = route_lane_kernel_for(kmax);
+    const int mw = lane_mask_words(E, P);
+    if (smem > kLaneSmemMax || mw == 0) return cudaSuccess;
+    RouteKernel kern = route_lane_kernel_for(kmax, mw);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * kRouteWarps, smem);
     if (e != cudaSuccess) return e;
     if (per_sm <= 0) return cudaSuccess;
     p.route_lane_kmax = kmax;
+    p.route_lane_mw = mw;
     p.route_lane_rsw = 4 * lane_row_units(E, P);
     p.route_lane.grid = p.num_sms * per_sm;
     p.route_lane.block = 32 * kRouteWarps;
@@ -432,7 +475,8 @@ cudaError_t launch_route(const a2av_plan_s &p, const RouteArgs &a, cudaStream_t 
     if (p.route_lane_kmax > 0 && reinterpret_cast<uintptr_t>(a.logits) % 16 == 0) {
         RouteArgs b = a;
         b.rsw = p.route_lane_rsw;
-        route_lane_kernel_for(p.route_lane_kmax)<<<p.route_lane.grid, p.route_lane.block, p.route_lane.smem, s>>>(b);
+        route_lane_kernel_for(p.route_lane_kmax, p.route_lane_mw)<<<p.route_lane.grid, p.route_lane.block,
+                                                                      p.route_lane.smem, s>>>(b);
     } else {
         route_kernel_for(p.g.E)<<<p.route.grid, p.route.block, 0, s>>>(a);
     }

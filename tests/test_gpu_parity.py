@@ -724,9 +724,10 @@ def test_router_then_dispatch_and_combine(wid, T, H):
 
 def _adversarial_logits(w, seed, dev):
     """Seeded Gaussian logits with rows built to reach every path of the
-    lane-per-token router: ties across the k-th place, exactly 32 and 33
-    logits at the top (the candidate list holds 32), infinities, NaN, -0 and
-    denormals, and rows where a group of 16-byte units holds only -inf."""
+    lane-per-token router: ties across the k-th place, 32 and 33 logits tied
+    at the top (every one a candidate), infinities, NaN, -0 and denormals,
+    and rows where a group of 16-byte units holds only -inf (the whole-share
+    fallback)."""
     import torch
 
     lg = W.make_logits(w, seed, device=dev)
@@ -735,9 +736,9 @@ def _adversarial_logits(w, seed, dev):
     if len(rows) > 0:
         rows[0][:] = 3.0                               # all equal
     if len(rows) > 1:
-        rows[1][: min(E, 32)] = 7.0                    # 32 at the top: a full list
+        rows[1][: min(E, 32)] = 7.0                    # 32 tied at the top
     if len(rows) > 2:
-        rows[2][: min(E, 33)] = 7.0                    # 33: one over, whole-row fallback
+        rows[2][: min(E, 33)] = 7.0                    # 33 tied at the top
     if len(rows) > 3:
         rows[3][::3] = 1.5                             # ties straddling the k-th place
     if len(rows) > 4:
