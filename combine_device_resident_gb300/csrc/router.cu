@@ -26,10 +26,10 @@
 //      moves up (of equal logits the lower id, which arrived first, stays
 //      ahead).
 // A share whose tau is -infinity (a group of only -infinity or NaN logits)
-// inserts every logit it holds instead.  Bitonic
-// merges over xor shuffles then give every lane of the token the token's
-// best KMAX, by key and then lower id.  Gates are computed as in
-// route_token, so the two kernels give the same bits.
+// inserts every logit it holds instead.  Bitonic merges over xor shuffles
+// then give every lane of the token the token's best KMAX, by key and then
+// lower id.  Gates are computed as in route_token, so the two kernels give
+// the same bits.
 //
 // Warp-per-token kernel (any shape): route_token in route_select.cuh, one
 // warp per token, grid-stride over all R*T tokens.
