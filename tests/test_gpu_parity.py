@@ -760,7 +760,8 @@ def _adversarial_logits(w, seed, dev):
 
 @pytest.mark.parametrize("R,T,E,k", [(2, 300, 4, 1), (8, 512, 16, 1), (16, 257, 128, 2), (4, 130, 256, 8),
                                      (4, 70, 8, 8), (2, 65, 12, 4), (2, 40, 512, 8), (1, 33, 64, 3),
-                                     (4, 31, 256, 7), (2, 50, 256, 1), (2, 50, 256, 2), (2, 45, 40, 5)])
+                                     (4, 31, 256, 7), (2, 50, 256, 1), (2, 50, 256, 2), (2, 45, 40, 5),
+                                     (2, 20, 640, 8), (2, 30, 320, 2), (4, 40, 1024, 4)])
 def test_router_lane_kernel_equals_warp_kernel(R, T, E, k):
     # The lane-per-token router (the default on these shapes) against the
     # warp-per-token one (A2AV_FLAG_ROUTE_WARP) and against the oracle: same
