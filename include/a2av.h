@@ -50,6 +50,13 @@
  *   - A plan's workspace is shared by its calls: use one plan from one
  *     stream at a time (or order the streams).  Calls that overlap on the
  *     device through one plan race.
+ *   - Stream order holds for every input: a call's kernels may become
+ *     resident before the kernel ahead of them on the stream has finished
+ *     (programmatic dependent launch), but none reads a tensor that kernel
+ *     may write before it has completed.  So one call's `out` may be the next
+ *     call's `x`, on the same stream, with nothing in between.  The pack and
+ *     combine grids fill every SM: other work on the GPU during a call makes
+ *     it slower, not wrong.
  *
  * Layouts (int32 unless said otherwise; R ranks, E experts, T tokens per
  * rank, H hidden, k experts per token, Epr = E/R):
