@@ -583,8 +583,9 @@ def run_layers(args, w: W.Workload, dev, rank: int, world: int, local: int):
 
 
 # ---------------------------------------------------------------------------
-def main():
-    args = parse_args()
+def resolve_workload(args) -> W.Workload:
+    """The workload the command names: --workload, scaled by --tokens and
+    --hidden (small cases for profiling), in the --recv-order asked for."""
     w = W.WORKLOADS[args.workload]
     if args.tokens or args.hidden:
         w = w.scaled(T=args.tokens or None, H=args.hidden or None)
@@ -592,6 +593,12 @@ def main():
         import dataclasses
 
         w = dataclasses.replace(w, recv_order=args.recv_order)
+    return w
+
+
+def main():
+    args = parse_args()
+    w = resolve_workload(args)
     if args.impl == "reference":
         return run_reference(args, w)
 

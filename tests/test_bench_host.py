@@ -79,3 +79,20 @@ def test_cpu_baseline_reports_both_settings():
     cb = bench.cpu_baseline(w, x, rg["topk_idx"], rg["gate_w"], budget_s=0.5, threads=4)
     assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] > 0
     assert cb["threads"] == 4 and cb["value_threaded"] > 0 and "4 threads" in cb["sample_threaded"]
+
+
+def test_tokens_and_hidden_options_scale_the_workload():
+    # --tokens and --hidden give the small cases the profiles use; the
+    # router's capture keeps every token and shrinks only the rows
+    import bench
+    import workloads as W
+
+    a = bench.parse_args(["--workload", "5", "--hidden", "64"])
+    assert (a.tokens, a.hidden) == (0, 64)
+    w = bench.resolve_workload(a)
+    base = W.WORKLOADS[5]
+    assert (w.R, w.E, w.T, w.k, w.H) == (base.R, base.E, base.T, base.k, 64)
+    a = bench.parse_args(["--workload", "3", "--tokens", "16"])
+    w = bench.resolve_workload(a)
+    assert (w.T, w.H, w.window_rows) == (16, W.WORKLOADS[3].H, W.WORKLOADS[3].R * 16 * W.WORKLOADS[3].k)
+    assert bench.resolve_workload(bench.parse_args([])) == W.WORKLOADS[bench.DEFAULT_WORKLOAD]
