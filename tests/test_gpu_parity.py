@@ -1047,3 +1047,53 @@ def _random_case(i):
 def test_random_shapes_and_options(i):
     w, nt, flags = _random_case(i)
     P.full_parity(w, seed=i, num_tokens=nt, flags=flags)
+
+
+def _random_router_case(i):
+    rng = np.random.default_rng(2000 + i)
+    R = int(rng.choice([1, 2, 3, 4, 8, 16]))
+    E = R * int(rng.choice([1, 2, 4, 8, 16, 32, 64]))
+    k = int(rng.integers(1, min(E, 8) + 1))  # 1..8: the lane kernel's range (other shapes fall back)
+    T = int(rng.choice([1, 3, 17, 64, 129]))
+    return R, E, k, T, rng
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_random_router_cases(i):
+    # seeded shapes, logits with random ties and special values, and random
+    # active counts: the default router against the oracle's ids and the
+    # warp-per-token kernel's ids and gate bits
+    import torch
+    from combine_device_resident_gb300 import FLAG_ROUTE_WARP, Plan
+
+    R, E, k, T, rng = _random_router_case(i)
+    dev = P.device()
+    lg = rng.standard_normal((R, T, E)).astype(np.float32)
+    lg = np.round(lg * 4) / 4  # coarse values: ties are common
+    specials = np.array([np.nan, np.inf, -np.inf, -0.0, 0.0, 1e-40], dtype=np.float32)
+    mask = rng.random(lg.shape) < 0.05
+    lg[mask] = rng.choice(specials, size=int(mask.sum()))
+    nt = rng.integers(0, T + 1, size=R).astype(np.int32) if rng.random() < 0.5 else None
+    logits = torch.from_numpy(lg).to(dev)
+    outs = []
+    for flags in (0, FLAG_ROUTE_WARP):
+        plan = Plan(R, E, T, 8, k, device=dev, flags=flags)
+        if nt is not None:
+            plan.set_active_tokens(torch.from_numpy(nt).to(dev))
+        idx = torch.full((R, T, k), -9, dtype=torch.int32, device=dev)
+        gate = torch.full((R, T, k), -1.0, dtype=torch.float32, device=dev)
+        plan.route(logits, idx, gate)
+        torch.cuda.synchronize()
+        assert plan.read_status() == 0
+        outs.append((idx.cpu().numpy(), gate.cpu().numpy().view(np.uint32)))
+        plan.close()
+    np.testing.assert_array_equal(outs[0][0], outs[1][0])
+    np.testing.assert_array_equal(outs[0][1], outs[1][1])
+    ridx, _ = oracle.route(lg, k, num_tokens=nt)
+    got = outs[0][0]
+    if nt is None:
+        np.testing.assert_array_equal(got, ridx)
+    else:
+        for s_ in range(R):
+            np.testing.assert_array_equal(got[s_, :nt[s_]], ridx[s_, :nt[s_]])
+            assert (got[s_, nt[s_]:] == -9).all()
