@@ -97,6 +97,9 @@ def parse_args(argv=None):
     ap.add_argument("--layers", type=int, default=0,
                     help="capture this many independent dispatch+combine pairs (own buffers each) in one graph "
                          "and report the time per pair (decode over several MoE layers)")
+    ap.add_argument("--chain", action="store_true",
+                    help="with --layers: each layer's x is the previous layer's out (written just before, "
+                         "so hot in L2, as a decode step's layer input is)")
     ap.add_argument("--cpu-threads", type=int, default=0,
                     help="threads of the CPU baseline's per-rank setting (0 = min(R, usable cores))")
     return ap.parse_args(argv)
@@ -437,6 +440,8 @@ def config_block(w: W.Workload, args) -> dict:
          "accumulate": "fp32", "parallelism": "replicas"}
     if getattr(args, "layers", 0) > 0:
         c["layers"] = args.layers
+        if getattr(args, "chain", False):
+            c["chain"] = "x of layer i = out of layer i-1"
     return c
 
 
@@ -475,6 +480,9 @@ def run_layers(args, w: W.Workload, dev, rank: int, world: int, local: int):
                            gate=torch.from_numpy(rg["gate_w"]).to(dev), sp=plan.new_splits(), recv=recv,
                            slot=slot_map, out=out))
     del x0
+    if args.chain:  # layer i reads what layer i-1 wrote, as in a decode step
+        for i in range(1, L):
+            layers[i]["x"] = layers[i - 1]["out"]
 
     def stage_fns(b):
         return [lambda s: plan.splits(b["idx"], b["sp"], b["slot"], stream=s),
@@ -571,7 +579,8 @@ def run_layers(args, w: W.Workload, dev, rank: int, world: int, local: int):
             "pct_of_peak": round(100 * job["gbs"] / world / peak, 2), "peak_gbs": peak, "peak_kind": peak_kind,
             "per_layer_stage_us": {n: round(v, 3) for n, v in per_stage.items()},
             "graph_floor_us": round(1e3 * t_ms[3], 3),
-            "timing": (f"one graph of {L} x [splits, pack, combine], each layer with its own buffers; "
+            "timing": (f"one graph of {L} x [splits, pack, combine], each layer with its own buffers"
+                       + (", x of each layer the previous layer's out" if args.chain else "") + "; "
                        f"{K} replays; stages from nested graphs of the first 1..3 stages of every layer, "
                        f"{KK} replays each, minus the graph-launch floor for the first"),
             "gpu_launches": int(kernels_per_step * K), "kernels_per_step": int(kernels_per_step),
